@@ -1,1 +1,226 @@
-"""W4A16 skinny GEMM for GB300 (sm_103a): Python binding of the C-ABI library."""
+"""W4A16 skinny GEMM for GB300 (sm_103a): Python binding of the C ABI.
+
+``Y[M, N] = X[M, K] . dequant(W)[N, K]^T`` with bf16 X and Y, int4 W packed two
+codes per byte (low nibble = even k), one bf16 scale per 128 weights along K,
+``dequant = scale * (code - 8)``, fp32 accumulation.
+
+Every function here only checks tensor metadata, allocates outputs and
+workspaces with torch, and calls the C ABI on the current torch stream: all
+arithmetic runs in the library's CUDA kernels.  There is no CPU path; a call
+with CPU tensors or without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import _lib
+from ._lib import Options, PlanInfo, W4A16Error
+
+GROUP = 128
+ARM_AUTO, ARM_DECODE, ARM_TENSOR = 0, 1, 2
+_ARMS = {None: ARM_AUTO, "auto": ARM_AUTO, "decode": ARM_DECODE, "tensor": ARM_TENSOR}
+
+__all__ = ["GROUP", "pack", "gemm", "gemm_partials", "gemm_grouped", "dequant_fp32", "dequant_bf16",
+           "splitk_reduce", "plan", "packed_weight_bytes", "layout_version", "W4A16Error"]
+
+
+def _stream_ptr(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need_cuda(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _opts(arm, split_k, tile_tokens):
+    if arm not in _ARMS:
+        raise ValueError(f"arm must be one of {list(_ARMS)}")
+    return Options(_ARMS[arm], int(split_k), int(tile_tokens))
+
+
+_ws_lock = threading.Lock()
+_ws_cache: dict = {}
+
+
+def _workspace(device, nbytes: int) -> torch.Tensor:
+    """A grow-only scratch buffer per device (contents need no initialisation)."""
+    key = torch.device(device).index
+    with _ws_lock:
+        buf = _ws_cache.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+            _ws_cache[key] = buf
+        return buf
+
+
+def layout_version() -> int:
+    return int(_lib.lib().w4a16_layout_version())
+
+
+def packed_weight_bytes(N: int, K: int) -> int:
+    return int(_lib.lib().w4a16_packed_weight_bytes(N, K))
+
+
+def pack(w_canon: torch.Tensor) -> torch.Tensor:
+    """Canonical uint8 [N, K/2] (CUDA) -> packed uint8 buffer for the kernels."""
+    _need_cuda(w_canon, "w_canon", torch.uint8)
+    N, half_k = w_canon.shape
+    K = 2 * half_k
+    nbytes = packed_weight_bytes(N, K)
+    if nbytes == 0:
+        raise ValueError(f"unsupported weight shape N={N} K={K} (K must be a multiple of 128)")
+    out = torch.empty(nbytes, dtype=torch.uint8, device=w_canon.device)
+    with torch.cuda.device(w_canon.device):
+        _lib.check(_lib.lib().w4a16_pack_weights(w_canon.data_ptr(), out.data_ptr(), N, K,
+                                                 _stream_ptr(w_canon.device)), "w4a16_pack_weights")
+    return out
+
+
+def plan(M: int, N: int, K: int, arm=None, split_k: int = 0, tile_tokens: int = 0,
+         device=None) -> dict:
+    """What the dispatcher picks for this shape on the (current) device."""
+    info = PlanInfo()
+    o = _opts(arm, split_k, tile_tokens)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _lib.check(_lib.lib().w4a16_plan(M, N, K, GROUP, ctypes.byref(o), ctypes.byref(info)),
+                   "w4a16_plan")
+    return {"arm": {1: "decode", 2: "tensor"}.get(info.arm, info.arm), "split_k": info.split_k,
+            "tile_tokens": info.tile_tokens, "ctas": info.ctas,
+            "workspace_bytes": int(info.workspace_bytes)}
+
+
+def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=None,
+         split_k: int = 0, tile_tokens: int = 0, out: torch.Tensor | None = None,
+         workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Y = X . dequant(W)^T.  x: bf16 [M, K]; scales: bf16 [N, K/128]; returns bf16 [M, N]."""
+    _need_cuda(x, "x", torch.bfloat16)
+    _need_cuda(scales, "scales", torch.bfloat16)
+    _need_cuda(w_packed, "w_packed", torch.uint8)
+    M, K = x.shape
+    N = scales.shape[0]
+    if scales.shape[1] * GROUP != K:
+        raise ValueError("scales must be [N, K/128]")
+    if w_packed.numel() < packed_weight_bytes(N, K):
+        raise ValueError("w_packed is smaller than packed_weight_bytes(N, K)")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need_cuda(out, "out", torch.bfloat16)
+    o = _opts(arm, split_k, tile_tokens)
+    L = _lib.lib()
+    with torch.cuda.device(x.device):
+        info = PlanInfo()
+        _lib.check(L.w4a16_plan(M, N, K, GROUP, ctypes.byref(o), ctypes.byref(info)), "w4a16_plan")
+        need = int(info.workspace_bytes)
+        if workspace is None:
+            ws = _workspace(x.device, need) if need else None
+        else:
+            ws = workspace
+        ws_ptr = ws.data_ptr() if ws is not None else None
+        ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+        _lib.check(L.w4a16_gemm_ex(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(),
+                                   out.data_ptr(), M, N, K, GROUP, ws_ptr, ws_bytes,
+                                   ctypes.byref(o), _stream_ptr(x.device)), "w4a16_gemm_ex")
+    return out
+
+
+def gemm_partials(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *,
+                  out: torch.Tensor, workspace: torch.Tensor, arm=None, split_k: int = 0,
+                  tile_tokens: int = 0) -> int:
+    """First launch of gemm() only (see w4a16_gemm_partials); returns SPLIT_K.
+
+    With SPLIT_K > 1 the fp32 partial sums land in ``workspace`` as
+    [SPLIT_K, M, N] and ``out`` is untouched; splitk_reduce() finishes the call."""
+    M, K = x.shape
+    N = scales.shape[0]
+    o = _opts(arm, split_k, tile_tokens)
+    sk = ctypes.c_int(0)
+    with torch.cuda.device(x.device):
+        _lib.check(_lib.lib().w4a16_gemm_partials(
+            x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), out.data_ptr(), M, N, K, GROUP,
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(), ctypes.byref(o),
+            ctypes.byref(sk), _stream_ptr(x.device)), "w4a16_gemm_partials")
+    return int(sk.value)
+
+
+def gemm_grouped(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor,
+                 m_sizes: torch.Tensor, *, out: torch.Tensor | None = None,
+                 status: torch.Tensor | None = None):
+    """Grouped product in one launch.
+
+    x: bf16 [M_total, K]; w_packed: num_groups packed blocks; scales: bf16
+    [num_groups, N, K/128]; m_sizes: int32 [num_groups] on the device (never
+    read on the host).  Returns (Y bf16 [M_total, N], status int32 tensor
+    whose element 0 the kernel sets; 0 = sizes consistent)."""
+    _need_cuda(x, "x", torch.bfloat16)
+    _need_cuda(scales, "scales", torch.bfloat16)
+    _need_cuda(w_packed, "w_packed", torch.uint8)
+    _need_cuda(m_sizes, "m_sizes", torch.int32)
+    M_total, K = x.shape
+    G, N, kg = scales.shape
+    if kg * GROUP != K or m_sizes.numel() != G:
+        raise ValueError("scales must be [num_groups, N, K/128] and m_sizes [num_groups]")
+    if w_packed.numel() < G * packed_weight_bytes(N, K):
+        raise ValueError("w_packed is smaller than num_groups * packed_weight_bytes(N, K)")
+    if out is None:
+        out = torch.empty((M_total, N), dtype=torch.bfloat16, device=x.device)
+    L = _lib.lib()
+    with torch.cuda.device(x.device):
+        nb = ctypes.c_size_t(0)
+        _lib.check(L.w4a16_grouped_workspace_bytes(G, M_total, N, K, GROUP, ctypes.byref(nb)),
+                   "w4a16_grouped_workspace_bytes")
+        if status is None:
+            status = torch.empty(max(4, (nb.value + 3) // 4), dtype=torch.int32, device=x.device)
+        _lib.check(L.w4a16_gemm_grouped(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(),
+                                        m_sizes.data_ptr(), out.data_ptr(), G, M_total, N, K,
+                                        GROUP, status.data_ptr(), status.numel() * 4,
+                                        _stream_ptr(x.device)), "w4a16_gemm_grouped")
+    return out, status
+
+
+def dequant_fp32(w_packed: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
+    """fp32 [N, K] = scale * (code - 8), computed by the kernels' bit trick."""
+    _need_cuda(w_packed, "w_packed", torch.uint8)
+    _need_cuda(scales, "scales", torch.bfloat16)
+    N, kg = scales.shape
+    K = kg * GROUP
+    out = torch.empty((N, K), dtype=torch.float32, device=scales.device)
+    with torch.cuda.device(scales.device):
+        _lib.check(_lib.lib().w4a16_dequant_fp32(w_packed.data_ptr(), scales.data_ptr(),
+                                                 out.data_ptr(), N, K, GROUP,
+                                                 _stream_ptr(scales.device)), "w4a16_dequant_fp32")
+    return out
+
+
+def dequant_bf16(w_packed: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
+    """bf16 [N, K] = round_nearest_even(scale * (code - 8)): the tensor arm's operand."""
+    _need_cuda(w_packed, "w_packed", torch.uint8)
+    _need_cuda(scales, "scales", torch.bfloat16)
+    N, kg = scales.shape
+    K = kg * GROUP
+    out = torch.empty((N, K), dtype=torch.bfloat16, device=scales.device)
+    with torch.cuda.device(scales.device):
+        _lib.check(_lib.lib().w4a16_dequant_bf16(w_packed.data_ptr(), scales.data_ptr(),
+                                                 out.data_ptr(), N, K, GROUP,
+                                                 _stream_ptr(scales.device)), "w4a16_dequant_bf16")
+    return out
+
+
+def splitk_reduce(ws: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """bf16 [M, N] = sum over slices of fp32 ws [S, M, N] (slices in order)."""
+    _need_cuda(ws, "ws", torch.float32)
+    S, M, N = ws.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=ws.device)
+    with torch.cuda.device(ws.device):
+        _lib.check(_lib.lib().w4a16_splitk_reduce(ws.data_ptr(), out.data_ptr(), S, M, N,
+                                                  _stream_ptr(ws.device)), "w4a16_splitk_reduce")
+    return out

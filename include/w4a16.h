@@ -1,0 +1,196 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) W4A16 skinny GEMM library.
+ *
+ *   Y[M][N] (bf16) = X[M][K] (bf16) . dequant(W)[N][K]^T,  fp32 accumulation,
+ *   dequant(W)[n][k] = scale[n][k / 128] * (code(n, k) - 8).
+ *
+ * The op: "[ROCm][Kernel] W4A16 skinny GEMM: hand-asm kernel for gfx1151"
+ * (opening paragraph: int4 weights, bf16 activations, N x K weight shapes;
+ * section 1 "Magic-constant bf16 dequant": weight = scale * (n - 8)).  The
+ * packing rule (low nibble = even k), the atomic-free split-K workspace
+ * [SPLIT_K][M][N] and the device-side grouped row starts come from "Add
+ * Triton BF16xINT4 rowwise GEMM for ROCm gfx942/gfx950", section
+ * "Implementation" (paragraphs "Fused A-operand dot", "Split-K without
+ * atomics", "Native fused grouped kernel").
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_dev, X, Y, W_*, scales, workspace and out are DEVICE
+ *    pointers; `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *    default stream).  All buffers are owned by the caller.
+ *  - Matrices are dense and row-major.  bf16 values travel as their raw
+ *    16-bit patterns (w4a16_bf16).
+ *  - The library never allocates, frees or synchronises, and never copies
+ *    between host and device inside a call; kernels are enqueued on `stream`
+ *    and the call returns.  No entry point reads the environment.
+ *  - Arguments are validated on the host before anything is enqueued; a
+ *    failed check returns an error status and launches nothing.  A launch
+ *    failure returns W4A16_ERR_CUDA.  Kernels never trap.
+ *  - group_size must be 128 (W4A16_ERR_UNSUPPORTED otherwise); K must be a
+ *    positive multiple of 128; N >= 1; M >= 0 (M == 0 launches nothing).
+ *  - X, W_packed and workspace must be 16-byte aligned; scales and Y 2-byte
+ *    aligned (W4A16_ERR_INVALID_ARG otherwise).
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t w4a16_bf16; /* raw bf16 bit pattern */
+
+typedef enum {
+    W4A16_OK = 0,
+    W4A16_ERR_INVALID_ARG = 1,          /* null pointer, bad shape, misalignment */
+    W4A16_ERR_UNSUPPORTED = 2,          /* group_size != 128, or an option not available */
+    W4A16_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below what the call needs */
+    W4A16_ERR_CUDA = 4                  /* a CUDA runtime call or launch failed */
+} w4a16_status;
+
+/* Which kernel family computes a plain (non-grouped) call. */
+typedef enum {
+    W4A16_ARM_AUTO = 0,     /* dispatcher decides (M <= 16: decode, else tensor) */
+    W4A16_ARM_DECODE = 1,   /* register-dequant mma.sync streaming arm */
+    W4A16_ARM_TENSOR = 2    /* TMA + TMEM + tcgen05.mma arm */
+} w4a16_arm;
+
+/* Overrides for tests and tuning.  Zero-initialised = automatic. */
+typedef struct {
+    int arm;          /* w4a16_arm */
+    int split_k;      /* 0 = automatic, else the number of K slices (clamped to K/128) */
+    int tile_tokens;  /* tensor arm only: 0 = automatic, else tokens per tile (16..256, multiple of 16) */
+} w4a16_options;
+
+/* What the dispatcher chose for a shape on the current device. */
+typedef struct {
+    int arm;              /* w4a16_arm actually used (never AUTO) */
+    int split_k;          /* K slices (1 = no workspace, output written directly) */
+    int tile_tokens;      /* tokens per tile (decode arm: 8 or 16 per pass) */
+    int ctas;             /* CTAs in the main launch */
+    size_t workspace_bytes;
+} w4a16_plan_info;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *w4a16_status_string(int status);
+
+/* Version of the packed-weight layout written by w4a16_pack_weights.  A packed
+ * buffer is only valid for a library reporting the same version. */
+int w4a16_layout_version(void);
+
+/* Bytes of the packed weight buffer for an N x K matrix: N rounded up to a
+ * multiple of 128, times K/2.  Returns 0 when N < 1 or K is not a positive
+ * multiple of 128.  Host only. */
+size_t w4a16_packed_weight_bytes(int N, int K);
+
+/* Rearrange canonical int4 weights into the kernels' layout.
+ *  w_canon:  device, uint8 [N][K/2]; byte j of row n holds the code of
+ *            k = 2j in bits 0-3 and of k = 2j+1 in bits 4-7 ("Add Triton
+ *            BF16xINT4 ...", "Fused A-operand dot": low nibble <-> even K).
+ *  w_packed: device, w4a16_packed_weight_bytes(N, K) bytes, written fully
+ *            (padding rows hold code 8, i.e. weight 0).  Must not overlap
+ *            w_canon.  The scales need no repacking: every entry point takes
+ *            them as bf16 [N][K/128].
+ * The CUTLASS path that page mentions also preshuffles the weights; this
+ * layout is this library's own. */
+w4a16_status w4a16_pack_weights(const uint8_t *w_canon, uint8_t *w_packed, int N, int K,
+                                void *stream);
+
+/* Plan a plain call on the current device (host only, no launch): fills
+ * *info (may be NULL) and, when bytes != NULL, the workspace size the call
+ * needs (0 when no split).  `opts` may be NULL. */
+w4a16_status w4a16_plan(int M, int N, int K, int group_size, const w4a16_options *opts,
+                        w4a16_plan_info *info);
+
+/* Workspace bytes w4a16_gemm needs for this shape on the current device
+ * (the split-K partial sums, fp32 [SPLIT_K][M][N]; 0 when no split). */
+w4a16_status w4a16_workspace_bytes(int M, int N, int K, int group_size, size_t *bytes);
+
+/* Y = X . dequant(W)^T.
+ *  X:        device bf16 [M][K].          Y: device bf16 [M][N].
+ *  W_packed: output of w4a16_pack_weights for (N, K).
+ *  scales:   device bf16 [N][K/128].
+ *  workspace/workspace_bytes: device scratch of at least
+ *            w4a16_workspace_bytes(M, N, K, 128) bytes (may be NULL when
+ *            that is 0).  Its contents need no initialisation.
+ * Split-K calls enqueue two kernels (partial products into the workspace,
+ * then a reduce that sums the slices in order 0..SPLIT_K-1 and rounds to
+ * bf16); the result does not depend on timing.  Output rounding is
+ * round-to-nearest-even. */
+w4a16_status w4a16_gemm(const w4a16_bf16 *X, const uint8_t *W_packed, const w4a16_bf16 *scales,
+                        w4a16_bf16 *Y, int M, int N, int K, int group_size, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/* w4a16_gemm with overrides (`opts` may be NULL = automatic).  The workspace
+ * requirement is the one w4a16_plan reports for the same opts. */
+w4a16_status w4a16_gemm_ex(const w4a16_bf16 *X, const uint8_t *W_packed,
+                           const w4a16_bf16 *scales, w4a16_bf16 *Y, int M, int N, int K,
+                           int group_size, void *workspace, size_t workspace_bytes,
+                           const w4a16_options *opts, void *stream);
+
+/* Only the first launch of w4a16_gemm_ex: when the plan for (M, N, K, opts)
+ * has SPLIT_K > 1 it writes the fp32 partial sums of every slice to
+ * workspace as [SPLIT_K][M][N] (slice s covers K groups [s*P, s*P + P), P
+ * from the plan) and leaves Y untouched; with one slice it writes Y exactly
+ * as w4a16_gemm_ex does.  Following it with w4a16_splitk_reduce(workspace,
+ * Y, SPLIT_K, M, N) gives the same bits as w4a16_gemm_ex.  Lets a caller
+ * time or fuse the two launches separately.  *split_k_out (may be NULL)
+ * receives SPLIT_K. */
+w4a16_status w4a16_gemm_partials(const w4a16_bf16 *X, const uint8_t *W_packed,
+                                 const w4a16_bf16 *scales, w4a16_bf16 *Y, int M, int N, int K,
+                                 int group_size, void *workspace, size_t workspace_bytes,
+                                 const w4a16_options *opts, int *split_k_out, void *stream);
+
+/* Workspace bytes of a grouped call: 16 bytes holding the device status word
+ * (see w4a16_gemm_grouped).  Host only. */
+w4a16_status w4a16_grouped_workspace_bytes(int num_groups, int M_total, int N, int K,
+                                           int group_size, size_t *bytes);
+
+/* Grouped product in one launch ("Add Triton BF16xINT4 ...", "Native fused
+ * grouped kernel"): group g owns rows [start_g, start_g + M_sizes[g]) of X
+ * and Y, start_g = sum of M_sizes[j] for j < g, and uses weight block g and
+ * scale block g.
+ *  X:         device bf16 [M_total][K].   Y: device bf16 [M_total][N].
+ *  W_packed:  num_groups consecutive blocks, each w4a16_packed_weight_bytes(N, K).
+ *  scales:    device bf16 [num_groups][N][K/128].
+ *  M_sizes_dev: device int32 [num_groups]; read only by the kernel (the host
+ *             never reads it, so the call needs no synchronisation).
+ *  workspace: >= w4a16_grouped_workspace_bytes(...) bytes.  The kernel writes
+ *             an int32 status word at workspace[0]: 0 = consistent; bit 0 =
+ *             a negative size (treated as 0); bit 1 = the sizes sum past
+ *             M_total (rows at or past M_total are not computed).  Rows no
+ *             group covers are left unwritten.
+ * 1 <= num_groups <= 4096. */
+w4a16_status w4a16_gemm_grouped(const w4a16_bf16 *X, const uint8_t *W_packed,
+                                const w4a16_bf16 *scales, const int32_t *M_sizes_dev,
+                                w4a16_bf16 *Y, int num_groups, int M_total, int N, int K,
+                                int group_size, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/* Dequantise a packed weight to fp32: out[n][k] = float(scale[n][k/128]) *
+ * (code - 8), computed with the same in-register bit trick the GEMM arms use
+ * (the code is OR-ed into the bf16 pattern of 128 + n and 136 is subtracted
+ * exactly, "[ROCm][Kernel] W4A16 ...", section 1).  Exact: the product of an
+ * 8-bit and a 4-bit significand fits binary32.  out: device fp32 [N][K]. */
+w4a16_status w4a16_dequant_fp32(const uint8_t *W_packed, const w4a16_bf16 *scales, float *out,
+                                int N, int K, int group_size, void *stream);
+
+/* Dequantise to the bf16 operand the tensor arm feeds its MMAs:
+ * out[n][k] = bf16_rne(scale[n][k/128] * (code - 8)).  out: device bf16 [N][K]. */
+w4a16_status w4a16_dequant_bf16(const uint8_t *W_packed, const w4a16_bf16 *scales,
+                                w4a16_bf16 *out, int N, int K, int group_size, void *stream);
+
+/* The split-K reduce on its own: Y[i] = bf16_rne(sum over s = 0..splits-1 of
+ * ws[s][i]) for i < M*N, slices summed in fp32 in ascending order ("Add Triton
+ * BF16xINT4 ...", "Split-K without atomics").  ws: device fp32
+ * [splits][M][N] (16-byte aligned); Y: device bf16 [M][N]. */
+w4a16_status w4a16_splitk_reduce(const float *ws, w4a16_bf16 *Y, int splits, int M, int N,
+                                 void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */
