@@ -42,6 +42,7 @@ SIGNATURES = {
     "w4a16_dequant_fp32": (I, [P, P, P, I, I, I, P]),
     "w4a16_dequant_bf16": (I, [P, P, P, I, I, I, P]),
     "w4a16_splitk_reduce": (I, [P, P, I, I, I, P]),
+    "w4a16_gemm_noalloc": (I, [P, P, P, P, I, I, I, I, P]),
 }
 
 

@@ -189,6 +189,27 @@ w4a16_status w4a16_dequant_bf16(const uint8_t *W_packed, const w4a16_bf16 *scale
 w4a16_status w4a16_splitk_reduce(const float *ws, w4a16_bf16 *Y, int splits, int M, int N,
                                  void *stream);
 
+/* w4a16_gemm for callers that cannot allocate device memory on the GEMM's
+ * path -- e.g. a framework plugin that receives only its inputs and outputs
+ * while the framework keeps the rest of device memory for its own arena, or
+ * code being captured into a CUDA graph, where cudaMalloc is not allowed.
+ * The pages have no counterpart of this entry point; it is this library's own.
+ * Arguments and result are those of w4a16_gemm minus the workspace: split-K
+ * partial sums go to a 4 MiB scratch array inside the library image (a
+ * file-scope __device__ array, held by every GPU that loads the library until
+ * the process exits).  Nothing is allocated or freed.
+ *  - Shapes whose plan needs more than 4 MiB of scratch (w4a16_workspace_bytes)
+ *    return W4A16_ERR_WORKSPACE_TOO_SMALL and launch nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture on the device.
+ *  - All calls on a device share the one array and it keeps the last call's
+ *    contents, so calls that may overlap on the GPU (different streams without
+ *    ordering between them) race; order them on one stream or by events. */
+w4a16_status w4a16_gemm_noalloc(const w4a16_bf16 *X, const uint8_t *W_packed,
+                                const w4a16_bf16 *scales, w4a16_bf16 *Y, int M, int N, int K,
+                                int group_size, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
