@@ -8,12 +8,13 @@
 // 128-wide scale groups (the occupancy argument of that page's "Split-K
 // without atomics" paragraph, here computed from the device's SM count rather
 // than autotuned).
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <cuda_runtime.h>
 
-#include "../../include/w4a16.h"
+#include "w4a16.h"
 #include "common.cuh"
 #include "internal.h"
 
@@ -42,9 +43,15 @@ using namespace w4a16;
 
 namespace {
 
-constexpr int kDecodeMaxM = 16;
-constexpr int kMaxSplit = 32;
-constexpr int kMaxDecodeGroupsPerSlice = 64;
+constexpr int kDecodeCtasPerSm = 2;           // resident decode CTAs per SM
+constexpr double kHbmBytesPerS = 6.5e12;      // planning figures, not measurements
+constexpr double kCtaBytesPerS = 50e9;        // one CTA's streaming rate (64 KB ring)
+constexpr double kL2BytesPerS = 20e12;
+constexpr double kReduceSeconds = 0.5e-6;
+constexpr int kDecodeMaxM = 16;               // auto dispatch: M <= 16 -> decode arm
+constexpr double kClockHz = 1.9e9;            // planning clock
+constexpr int kTensorMaxStages = 8;
+constexpr double kTcChainClk = 500.0;         // one CTA's per-K-block dependency chain
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -58,6 +65,7 @@ w4a16_status check_shape(int M, int N, int K, int group_size) {
 struct Plan {
     int arm;
     DecodePlan decode;
+    TensorPlan tensor;
     int split_k;
     size_t ws_bytes;
     int ctas;
@@ -66,46 +74,148 @@ struct Plan {
 
 int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
 
-// Slices of whole groups: at most `want` slices, each at most `max_gps` groups.
-void make_slices(int groups, int want, int max_gps, int *split, int *gps) {
-    if (want < 1) want = 1;
-    if (want > groups) want = groups;
-    int per = ceil_div(groups, want);
-    if (per > max_gps) per = max_gps;
-    *gps = per;
-    *split = ceil_div(groups, per);
+// Decode-arm grid: each CTA keeps one K slice (gps groups) and streams tiles
+// c, c + C, ... of it.  Modelled time = max(all weight bytes at HBM speed,
+// the busiest CTA's bytes at one CTA's streaming rate) + the split-K
+// workspace round trip; at most kDecodeCtasPerSm CTAs per SM are launched so
+// that all of them are resident at once.
+void plan_decode(int M, int N, int K, int sms, int forced_split, DecodePlan *d) {
+    const int groups = K / kGroup;
+    d->mt = M <= 8 ? 1 : 2;
+    d->token_blocks = ceil_div(M, 8 * d->mt);
+    d->n_tiles = ceil_div(N, kTileRows);
+    const long long slots = (long long)kDecodeCtasPerSm * sms;
+    const double w_bytes = double(d->n_tiles) * kTileRows * double(K) / 2.0;
+    double best = 1e30;
+    int min_split = ceil_div(groups, kDecodeMaxGps);
+    for (int gps = kDecodeMaxGps; gps >= 1; --gps) {
+        int sk = ceil_div(groups, gps);
+        if (forced_split > 0) sk = forced_split < min_split ? min_split : (forced_split > groups ? groups : forced_split);
+        const int gps_eff = ceil_div(groups, sk);
+        sk = ceil_div(groups, gps_eff);
+        const long long per_slice = slots / ((long long)sk * d->token_blocks);
+        const int cmax = int(per_slice < 1 ? 1 : (per_slice > d->n_tiles ? d->n_tiles : per_slice));
+        for (int C = cmax; C >= 1; --C) {
+            const int tiles_per = ceil_div(d->n_tiles, C);
+            if (C < cmax && ceil_div(d->n_tiles, C + 1) == tiles_per) continue;  // same critical path, fewer CTAs
+            const double cta_bytes = double(tiles_per) * 2.0 * gps_eff * kChunkBytes * d->token_blocks;
+            double t = w_bytes * d->token_blocks / kHbmBytesPerS;
+            const double t_cta = cta_bytes / kCtaBytesPerS;
+            if (t_cta > t) t = t_cta;
+            if (sk > 1)
+                t += 2.0 * double(sk) * M * N * 4.0 / kL2BytesPerS + kReduceSeconds;
+            if (t < best * 0.999) {
+                best = t;
+                d->split_k = sk;
+                d->groups_per_slice = gps_eff;
+                d->ctas_per_slice = C;
+            }
+        }
+        if (forced_split > 0) break;
+    }
+}
+
+// Tensor-arm tiles: 128 weight rows x bt tokens, K split into sk slices.
+// Modelled per-K-block cycles = max(MMA: 2 bt, dequant floor, weight bytes at
+// one SM's HBM share + activation bytes at one SM's L2 share); a CTA's time is
+// its tile count times (K blocks x that + a fixed per-tile cost), plus the
+// split-K round trip.
+int tensor_stages(int bt, int num_groups, int occupancy) {
+    const size_t budget = size_t(kTensorMaxSmem) / size_t(occupancy);
+    const size_t fixed = tensor_smem_bytes(bt, 0, num_groups);
+    const size_t stage = 2 * size_t(bt) * 128 + 2 * kChunkBytes;   // one 128-column group
+    if (budget <= fixed) return 0;
+    size_t n = (budget - fixed) / stage;
+    if (n > size_t(kTensorMaxStages)) n = kTensorMaxStages;
+    return int(n);
+}
+
+// Tensor-arm tiles: 128 weight rows x bt tokens, K split into sk slices, one
+// or two CTAs per SM (two when a CTA's TMEM and shared memory fit twice).
+// Per K block an SM needs at least max(MMA: 2 bt cycles, a dequant floor,
+// weight bytes at its HBM share + activation bytes at its L2 share), and a
+// CTA cannot go faster than its dependency chain (kTcChainClk per K block),
+// which a second resident CTA hides.
+w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int forced_bt,
+                         int num_groups, TensorPlan *t) {
+    const int groups = K / kGroup;
+    t->n_tiles = ceil_div(N, kTileRows);
+    double best = 1e30;
+    int found = 0;
+    for (int bt = 32; bt <= 256; bt += 32) {
+        if (forced_bt > 0 && bt != forced_bt) continue;
+        const int occ_max = tensor_tmem_cols(bt) <= 256 ? 2 : 1;
+        for (int occ = 1; occ <= occ_max; ++occ) {
+            const int stages = tensor_stages(bt, num_groups, occ);
+            if (stages < 2) continue;
+            const int max_sk = num_groups > 1 ? 1 : (groups < 16 ? groups : 16);
+            for (int sk_req = 1; sk_req <= max_sk; ++sk_req) {
+                int sk = sk_req;
+                if (forced_split > 0) sk = forced_split > groups ? groups : forced_split;
+                if (num_groups > 1) sk = 1;
+                const int gps = ceil_div(groups, sk);
+                sk = ceil_div(groups, gps);
+                // grouped: rows per group vary; plan with the average
+                const double rows_per_unit = double(M) / num_groups;
+                const long long t_tiles =
+                    (long long)num_groups * (long long)ceil_div((long long)(rows_per_unit + 0.999), bt);
+                const long long tiles = (long long)t->n_tiles * t_tiles * sk;
+                const long long slots = (long long)occ * sms;
+                const long long ctas = tiles < slots ? tiles : slots;
+                const int conc = int(ceil_div(ctas, sms));
+                const double kb_tp = std::max(std::max(2.0 * bt, 150.0),
+                                              kChunkBytes / 22.0 + bt * 128.0 / 64.0);
+                const double kb = std::max(kb_tp, kTcChainClk / conc);
+                const double per_cta_tiles = double(ceil_div(tiles, ctas));
+                double time = (per_cta_tiles * conc * 2.0 * gps * kb + per_cta_tiles * 1500.0) / kClockHz;
+                if (sk > 1) time += 2.0 * sk * double(M) * N * 4.0 / kL2BytesPerS + kReduceSeconds;
+                if (time < best * 0.999) {
+                    best = time;
+                    t->tile_tokens = bt;
+                    t->split_k = sk;
+                    t->groups_per_slice = gps;
+                    t->t_tiles = int(t_tiles);
+                    t->ctas = int(ctas);
+                    t->stages = stages;
+                    t->smem_bytes = tensor_smem_bytes(bt, stages, num_groups);
+                    found = 1;
+                }
+                if (forced_split > 0 || num_groups > 1) break;
+            }
+        }
+    }
+    return found ? W4A16_OK : W4A16_ERR_UNSUPPORTED;
 }
 
 w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p) {
     std::memset(p, 0, sizeof *p);
     int sms = 0;
     if (device_sm_count(&sms) != 0 || sms < 1) return W4A16_ERR_CUDA;
-    const int arm_req = opts ? opts->arm : W4A16_ARM_AUTO;
-    if (arm_req == W4A16_ARM_TENSOR) return W4A16_ERR_UNSUPPORTED;
-    if (arm_req != W4A16_ARM_AUTO && arm_req != W4A16_ARM_DECODE) return W4A16_ERR_INVALID_ARG;
-    if (opts && (opts->split_k < 0 || opts->tile_tokens != 0)) return W4A16_ERR_INVALID_ARG;
-
-    const int groups = K / kGroup;
-    DecodePlan &d = p->decode;
-    d.mt = M <= 8 ? 1 : 2;
-    d.token_blocks = ceil_div(M, 8 * d.mt);
-    d.n_tiles = ceil_div(N, kTileRows);
-    int want;
-    if (opts && opts->split_k > 0) {
-        want = opts->split_k;
+    int arm = opts ? opts->arm : W4A16_ARM_AUTO;
+    if (arm != W4A16_ARM_AUTO && arm != W4A16_ARM_DECODE && arm != W4A16_ARM_TENSOR)
+        return W4A16_ERR_INVALID_ARG;
+    if (opts && opts->split_k < 0) return W4A16_ERR_INVALID_ARG;
+    const int forced_bt = opts ? opts->tile_tokens : 0;
+    if (forced_bt != 0 && (forced_bt < 32 || forced_bt > 256 || forced_bt % 32))
+        return W4A16_ERR_UNSUPPORTED;
+    if (arm == W4A16_ARM_AUTO) arm = M <= kDecodeMaxM ? W4A16_ARM_DECODE : W4A16_ARM_TENSOR;
+    if (arm == W4A16_ARM_DECODE && forced_bt != 0) return W4A16_ERR_INVALID_ARG;
+    p->arm = arm;
+    if (arm == W4A16_ARM_DECODE) {
+        DecodePlan &d = p->decode;
+        plan_decode(M, N, K, sms, opts ? opts->split_k : 0, &d);
+        p->split_k = d.split_k;
+        p->ctas = d.ctas_per_slice * d.split_k * d.token_blocks;
+        p->tile_tokens = 8 * d.mt;
     } else {
-        // Aim for two resident CTAs per SM; one slice when the grid already fills it.
-        const long long base = (long long)d.n_tiles * d.token_blocks;
-        want = ceil_div(2LL * sms, base);
-        if (want > kMaxSplit) want = kMaxSplit;
-        if (M > kDecodeMaxM) want = 1;
+        TensorPlan &t = p->tensor;
+        w4a16_status st = plan_tensor(M, N, K, sms, opts ? opts->split_k : 0, forced_bt, 1, &t);
+        if (st != W4A16_OK) return st;
+        p->split_k = t.split_k;
+        p->ctas = t.ctas;
+        p->tile_tokens = t.tile_tokens;
     }
-    make_slices(groups, want, kMaxDecodeGroupsPerSlice, &d.split_k, &d.groups_per_slice);
-    p->arm = W4A16_ARM_DECODE;
-    p->split_k = d.split_k;
-    p->ws_bytes = d.split_k > 1 ? size_t(d.split_k) * size_t(M) * size_t(N) * sizeof(float) : 0;
-    p->ctas = d.n_tiles * d.split_k * d.token_blocks;
-    p->tile_tokens = 8 * d.mt;
+    p->ws_bytes = p->split_k > 1 ? size_t(p->split_k) * size_t(M) * size_t(N) * sizeof(float) : 0;
     return W4A16_OK;
 }
 
@@ -192,7 +302,11 @@ static w4a16_status gemm_impl(const w4a16_bf16 *X, const uint8_t *W_packed,
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float *ws = static_cast<float *>(workspace);
-    cudaError_t e = launch_decode(p.decode, X, W_packed, scales, Y, ws, M, N, K, s);
+    cudaError_t e;
+    if (p.arm == W4A16_ARM_DECODE)
+        e = launch_decode(p.decode, X, W_packed, scales, Y, ws, M, N, K, s);
+    else
+        e = launch_tensor(p.tensor, X, W_packed, scales, Y, ws, nullptr, nullptr, 1, M, N, K, s);
     if (e != cudaSuccess) return W4A16_ERR_CUDA;
     if (with_reduce && p.split_k > 1) {
         e = launch_reduce(ws, Y, p.split_k, (long long)M * N, true, s);
@@ -229,7 +343,7 @@ w4a16_status w4a16_grouped_workspace_bytes(int num_groups, int M_total, int N, i
     if (!bytes) return W4A16_ERR_INVALID_ARG;
     w4a16_status st = check_shape(M_total, N, K, group_size);
     if (st != W4A16_OK) return st;
-    if (num_groups < 1 || num_groups > 4096) return W4A16_ERR_INVALID_ARG;
+    if (num_groups < 1 || num_groups > kMaxGroups) return W4A16_ERR_INVALID_ARG;
     *bytes = 16;
     return W4A16_OK;
 }
@@ -241,15 +355,27 @@ w4a16_status w4a16_gemm_grouped(const w4a16_bf16 *X, const uint8_t *W_packed,
                                 void *stream) {
     w4a16_status st = check_shape(M_total, N, K, group_size);
     if (st != W4A16_OK) return st;
-    if (num_groups < 1 || num_groups > 4096) return W4A16_ERR_INVALID_ARG;
+    if (num_groups < 1 || num_groups > kMaxGroups) return W4A16_ERR_INVALID_ARG;
     if (!X || !W_packed || !scales || !M_sizes_dev || !Y) return W4A16_ERR_INVALID_ARG;
     if (!aligned(X, 16) || !aligned(W_packed, 16) || !aligned(scales, 2) || !aligned(Y, 2) ||
         !aligned(M_sizes_dev, 4))
         return W4A16_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < 16) return W4A16_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(workspace, 16)) return W4A16_ERR_INVALID_ARG;
-    (void)stream;
-    return W4A16_ERR_UNSUPPORTED;
+    if (M_total == 0) return W4A16_OK;
+    int sms = 0;
+    if (device_sm_count(&sms) != 0 || sms < 1) return W4A16_ERR_CUDA;
+    TensorPlan t;
+    st = plan_tensor(M_total, N, K, sms, 1, 0, num_groups, &t);
+    if (st != W4A16_OK) return st;
+    // Enough CTAs for any split of M_total into the groups: the tile count is
+    // at most n_tiles * (ceil(M_total / bt) + num_groups).
+    const long long bound = (long long)t.n_tiles * (ceil_div(M_total, t.tile_tokens) + num_groups);
+    t.ctas = int(bound < sms ? bound : sms);
+    cudaError_t e = launch_tensor(t, X, W_packed, scales, Y, nullptr, M_sizes_dev,
+                                  static_cast<int *>(workspace), num_groups, M_total, N, K,
+                                  static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
 w4a16_status w4a16_dequant_fp32(const uint8_t *W_packed, const w4a16_bf16 *scales, float *out,

@@ -1,20 +1,21 @@
 // common.cuh -- device helpers shared by the W4A16 kernels (sm_103a).
 //
-// Packed weight layout (layout version 1), written by pack.cu:
+// Packed weight layout (layout version 2), written by pack.cu:
 //   W is cut into 128-row tiles (N padded up to a multiple of 128 with code 8)
 //   and 64-column K chunks.  One (tile, chunk) is 4096 contiguous bytes: eight
 //   16-row blocks of 512 bytes.  Inside a block, lane L = 4*g + t (g = L/4,
 //   t = L%4) owns 16 bytes = 4 words; word j covers rows {g, g+8} of the block
-//   and columns k0 + 16t + 4j + {0,1,2,3} (k0 = 64 * chunk).  Nibble slots of
+//   and columns k0 + 16j + 4t + {0,1,2,3} (k0 = 64 * chunk).  Nibble slots of
 //   a word (bit offset: row, column offset):
 //       0: g,0   4: g+8,0   8: g,2   12: g+8,2
 //      16: g,1  20: g+8,1  24: g,3   28: g+8,3
 //   so (w >> s) & 0x000F000F (s = 0, 4, 8, 12) picks a (k, k+1) pair of one
-//   row in the two 16-bit halves: exactly the A-fragment registers of an
-//   m16n8k16 bf16 mma.sync (rows g / g+8, column pairs 2t / 2t+8), with the
-//   MMA's K slots mapped to the columns this lane's X loads cover.  A
-//   tensor-arm thread that owns one row reads the 64 contiguous bytes of its
-//   g and uses the halves of its row.
+//   row in the two 16-bit halves.  Word j of lane (g, t) is then exactly
+//   (a) the 16x256b TMEM fragment of the 16-column slice j of the block
+//       ({row g: pairs 2t, 2t+1}, {row g+8: pairs 2t, 2t+1}), which the tensor
+//       arm stores as the A operand of one K=16 MMA, and
+//   (b) an m16n8k16 mma.sync A fragment whose K slots 2t,2t+1 / 2t+8,2t+9 map
+//       to columns 16j + 4t + {0,1} / {2,3}, which the decode arm uses.
 //
 // Dequantisation trick ("[ROCm][Kernel] W4A16 skinny GEMM: hand-asm kernel
 // for gfx1151", section 1 "Magic-constant bf16 dequant"): OR-ing a 4-bit code
@@ -35,7 +36,7 @@ constexpr int kTileRows = 128;       // rows per packed tile
 constexpr int kChunkK = 64;          // K elements per packed chunk
 constexpr int kChunkBytes = 4096;    // bytes per (tile, chunk)
 constexpr int kBlockBytes = 512;     // bytes per 16-row block of a chunk
-constexpr int kLayoutVersion = 1;
+constexpr int kLayoutVersion = 2;
 
 constexpr uint32_t kNibblePairMask = 0x000F000Fu;
 constexpr uint32_t kMagic128 = 0x43004300u;      // bf16x2 {128, 128}
@@ -112,10 +113,12 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 }
 
 // Streaming 16-byte load that does not allocate in L1 (weights are read once).
+// volatile: the load is issued where it is written, so a prefetch ring stays a
+// prefetch ring instead of being sunk next to its first use.
 __device__ __forceinline__ uint4 ldg_stream16(const void *p) {
     uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
     return r;
 }
 

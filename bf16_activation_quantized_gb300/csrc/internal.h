@@ -10,9 +10,10 @@ namespace w4a16 {
 struct DecodePlan {
     int mt;               // token octets per warp pass (1: 8 tokens, 2: 16 tokens)
     int token_blocks;     // passes over the tokens (grid.z)
-    int n_tiles;          // 128-row tiles (grid.x)
+    int n_tiles;          // 128-row tiles
+    int ctas_per_slice;   // grid.x: CTA c of a slice takes tiles c, c + ctas_per_slice, ...
     int split_k;          // K slices (grid.y)
-    int groups_per_slice; // 128-wide K groups per slice
+    int groups_per_slice; // 128-wide K groups per slice (<= kDecodeMaxGps)
 };
 
 struct TensorPlan {
@@ -27,6 +28,14 @@ struct TensorPlan {
 };
 
 int device_sm_count(int *sms);  // returns cudaError_t as int
+int *device_error_word();        // device address of the error word (nullptr on failure)
+
+// Decode arm shared memory: the staged X slice, its per-group sums and the
+// slice's scales.  The planner keeps a CTA under kDecodeSmemTarget so that
+// several CTAs share an SM; kDecodeMaxSmem is the hard limit.
+constexpr int kDecodeMaxGps = 8;
+constexpr int kDecodeMaxSmem = 110 * 1024;
+int decode_smem_needed(int M, int mt, int groups_per_slice);
 
 size_t packed_bytes(int N, int K);
 
@@ -36,6 +45,15 @@ cudaError_t launch_dequant(const uint8_t *w_packed, const uint16_t *scales, void
 cudaError_t launch_decode(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, int M, int N, int K,
                           cudaStream_t s);
+// Tensor arm (tensor.cu).
+constexpr int kTensorMaxSmem = 227 * 1024;
+constexpr int kMaxGroups = 1024;
+size_t tensor_smem_bytes(int bt, int stages, int num_groups);
+int tensor_tmem_cols(int bt);     // TMEM columns a CTA allocates for tiles of bt tokens
+cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t *Wp,
+                          const uint16_t *S, uint16_t *Y, float *ws, const int32_t *m_sizes,
+                          int *status, int num_groups, int M_total, int N, int K, cudaStream_t s);
+
 cudaError_t launch_reduce(const float *ws, uint16_t *Y, int splits, long long count, bool pdl,
                           cudaStream_t s);
 

@@ -15,7 +15,7 @@
 #include <atomic>
 #include <cuda_runtime.h>
 
-#include "../../include/w4a16.h"
+#include "w4a16.h"
 
 namespace {
 

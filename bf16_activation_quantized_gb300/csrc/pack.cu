@@ -33,7 +33,7 @@ __device__ __forceinline__ WordCoord word_coord(size_t idx, int KC) {
     const int g = lane >> 2, t = lane & 3;
     WordCoord c;
     c.row0 = tile * kTileRows + block * 16 + g;
-    c.k = chunk * kChunkK + 16 * t + 4 * j;
+    c.k = chunk * kChunkK + 16 * j + 4 * t;
     return c;
 }
 

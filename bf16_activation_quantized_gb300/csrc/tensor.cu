@@ -1,0 +1,555 @@
+// tensor.cu -- compute arm: TMA-staged activations, register-dequantised weights
+// in TMEM, tcgen05.mma with fp32 accumulators in TMEM.  One persistent kernel
+// serves the plain product (optionally split along K) and the grouped product.
+//
+// Roles in a CTA (320 threads):
+//   warp 8      producer: per K block (64 columns) one TMA 2-D load of the X
+//               tile [tokens x 64] (128-byte swizzle) and one 4 KB bulk copy of
+//               the packed weight chunk, both completing on full[stage].
+//   warp 9      TMEM owner and MMA issuer: four tcgen05.mma (K = 16 each) per
+//               K block, A = weights from TMEM, B = X from shared memory,
+//               D = fp32 in TMEM; tcgen05.commit releases the stages.
+//   warps 0-7   dequantisers, then the epilogue: warp w owns 16 weight rows,
+//               turns each packed word into its 16x256b TMEM fragment (one
+//               LOP3 per bf16 pair gives 128 + code; one bf16x2 FMA removes
+//               136 exactly; one bf16x2 multiply applies the group scale with a
+//               single rounding) and stores it with tcgen05.st.
+// The page this follows for the data flow is "[ROCm][Kernel] W4A16 skinny
+// GEMM: hand-asm kernel for gfx1151" (magic-constant dequant, section 1;
+// loads pipelined ahead of the math, section 2); the tile, the TMEM operand
+// and the tensor-core instructions are this library's sm_103a design.
+//
+// Grouped product ("Add Triton BF16xINT4 rowwise GEMM for ROCm gfx942/gfx950",
+// "Native fused grouped kernel"): each CTA reads M_sizes from device memory,
+// forms the exclusive prefix sum of the (clamped) sizes and of the groups'
+// tile counts in shared memory, and walks the flattened tile list; no host
+// synchronisation is needed.
+//
+// Every mbarrier wait is bounded (async.cuh); a timeout records an error bit
+// and the CTA winds down, waits for its own copies and MMAs, frees TMEM and
+// exits.
+#include <atomic>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "async.cuh"
+#include "common.cuh"
+#include "internal.h"
+#include "tc05.cuh"
+
+namespace w4a16 {
+
+namespace {
+
+constexpr int kTcDequantWarps = 8;
+constexpr int kTcProducerWarp = 8;
+constexpr int kTcMmaWarp = 9;
+constexpr int kTcThreads = 10 * 32;
+constexpr uint32_t kTcDCol = 0;      // accumulator: columns [0, bt); A stage sa: [bt + 32 sa, bt + 32 sa + 32)
+
+struct TcArgs {
+    const uint8_t *Wp;
+    const uint16_t *S;
+    uint16_t *Y;
+    float *ws;
+    const int32_t *m_sizes;   // nullptr: plain product over M_total rows
+    int *status;              // grouped status word (nullptr for the plain product)
+    int *err;
+    int M_total, N, K, num_groups;
+    int bt;                   // tokens per tile = MMA N (multiple of 32, <= 256)
+    int n_tiles;              // 128-row weight tiles
+    int split_k, gps;         // K slices and 128-wide groups per slice
+    int stages;               // shared-memory ring depth (one 128-column group per stage)
+    int a_stages;             // TMEM A ring depth (one group = 64 columns per stage)
+    int tmem_cols;            // TMEM columns allocated (power of two >= bt + 64 * a_stages)
+    int vec_store;            // Y rows are 16-byte aligned: stage the epilogue for 16-byte stores
+    unsigned long long w_group_stride;  // bytes between groups' packed weights
+    unsigned long long s_group_stride;  // elements between groups' scales
+};
+
+// Shared memory per stage: two X boxes (one per 64-column K block, 1024-byte
+// aligned, 128-byte swizzle) and the 8 KB of packed weights of the group.
+struct TcSmem {
+    int x_stage, off_x, off_w, off_epi, off_bar, off_misc, off_tab, total;
+};
+
+constexpr int kGroupBytes = 2 * kChunkBytes;           // packed weights of one 128-column group
+constexpr int kEpiBytesPerWarp = 32 * 32 * 2;          // 32 tokens x 32 rows of bf16
+
+__host__ __device__ inline TcSmem tc_smem_layout(int bt, int stages, int a_stages, int num_groups) {
+    TcSmem L;
+    L.x_stage = 2 * bt * 128;
+    L.off_x = 0;
+    L.off_w = L.off_x + stages * L.x_stage;
+    L.off_epi = L.off_w + stages * kGroupBytes;
+    L.off_bar = L.off_epi + kTcDequantWarps * kEpiBytesPerWarp;
+    L.off_misc = L.off_bar + (2 * stages + 2 * a_stages + 3) * 8;
+    L.off_tab = (L.off_misc + 16 + 15) & ~15;           // group tables: 2 x (G + 1) ints
+    L.total = L.off_tab + 2 * (num_groups + 1) * 4;
+    return L;
+}
+
+struct TileInfo {
+    int group, ft, tt, slice;
+    int x_row0;       // first X/Y row of the tile
+    int rows;         // valid rows (<= bt)
+};
+
+// Flattened tile order: feature tile fastest, then token tile, then slice
+// (plain) or group (grouped), so CTAs running together share X tiles in L2.
+__device__ __forceinline__ bool tc_tile(const TcArgs &a, const int *tab_tiles, const int *tab_rows,
+                                        int id, TileInfo &ti) {
+    if (a.m_sizes == nullptr) {
+        const int t_tiles = (a.M_total + a.bt - 1) / a.bt;
+        const int per_slice = t_tiles * a.n_tiles;
+        ti.group = 0;
+        ti.slice = id / per_slice;
+        const int r = id - ti.slice * per_slice;
+        ti.tt = r / a.n_tiles;
+        ti.ft = r - ti.tt * a.n_tiles;
+        ti.x_row0 = ti.tt * a.bt;
+        ti.rows = min(a.bt, a.M_total - ti.x_row0);
+        return ti.slice < a.split_k;
+    }
+    // binary search: largest g with tab_tiles[g] <= id
+    int lo = 0, hi = a.num_groups;
+    if (id >= tab_tiles[a.num_groups]) return false;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tab_tiles[mid] <= id) lo = mid; else hi = mid;
+    }
+    ti.group = lo;
+    ti.slice = 0;
+    const int r = id - tab_tiles[lo];
+    ti.tt = r / a.n_tiles;
+    ti.ft = r - ti.tt * a.n_tiles;
+    const int g_rows = tab_rows[lo + 1] - tab_rows[lo];
+    ti.x_row0 = tab_rows[lo] + ti.tt * a.bt;
+    ti.rows = min(a.bt, g_rows - ti.tt * a.bt);
+    return true;
+}
+
+__device__ __forceinline__ uint32_t scale_pair(const uint16_t *S, int row, int N, size_t idx) {
+    if (row >= N) return 0u;
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(S + idx));
+    return uint32_t(v) | (uint32_t(v) << 16);
+}
+
+__device__ __forceinline__ void drain_wait_tc(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > 100000000ull) break;
+}
+
+__device__ __forceinline__ void tc_st_16x256b_x8(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+        "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+template <bool kSplit>
+__global__ void __launch_bounds__(kTcThreads, 2)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte alignment for the swizzled X tiles (the host adds the slack).
+    unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const TcSmem L = tc_smem_layout(a.bt, a.stages, a.a_stages, a.num_groups);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = a.stages;
+    const int SA = a.a_stages;
+    const uint32_t bar0 = smem_u32(smem + L.off_bar);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto afull_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
+    auto aempty_bar = [&](int s) { return bar0 + 8u * (2 * S + SA + s); };
+    const uint32_t dfull_bar = bar0 + 8u * (2 * S + 2 * SA);
+    const uint32_t dempty_bar = dfull_bar + 8;
+    const uint32_t done_bar = dfull_bar + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
+    int *tab_tiles = reinterpret_cast<int *>(smem + L.off_tab);
+    int *tab_rows = tab_tiles + a.num_groups + 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            // Released by the MMA commit alone: the MMA of a stage starts only
+            // after every dequantiser has read its weights (they signal the A
+            // stage only after that), so the commit covers both readers.
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(afull_bar(s), kTcDequantWarps);
+            mbar_init(aempty_bar(s), 1);
+        }
+        mbar_init(dfull_bar, 1);
+        mbar_init(dempty_bar, kTcDequantWarps);
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kTcMmaWarp) {
+        tc_alloc(smem_u32(tmem_slot), uint32_t(a.tmem_cols));
+        tc_relinquish();
+    }
+    if (warp == kTcProducerWarp && lane == 0) tma_prefetch_desc(&tmap_x);
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // Group tables (grouped product): clamped row starts and tile prefix sums.
+    if (a.m_sizes != nullptr && threadIdx.x == 0) {
+        int rows = 0, tiles = 0, status = 0;
+        for (int g = 0; g < a.num_groups; ++g) {
+            int sz = a.m_sizes[g];
+            if (sz < 0) { status |= 1; sz = 0; }
+            if (rows + sz > a.M_total) { status |= 2; sz = a.M_total - rows; }
+            tab_rows[g] = rows;
+            tab_tiles[g] = tiles;
+            rows += sz;
+            tiles += ((sz + a.bt - 1) / a.bt) * a.n_tiles;
+        }
+        tab_rows[a.num_groups] = rows;
+        tab_tiles[a.num_groups] = tiles;
+        if (blockIdx.x == 0 && a.status) *a.status = status;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int n_groups = a.K / kGroup;
+    const int KC = a.K / kChunkK;
+    const uint32_t x_bytes = uint32_t(a.bt) * 128u;          // one X box
+    const uint32_t idesc = tc_idesc_bf16(128, a.bt);
+
+    if (warp == kTcProducerWarp) {
+        if (lane == 0) {
+            int st = 0, q = 0;            // q: stage uses so far
+            TileInfo ti;
+            for (int id = blockIdx.x; tc_tile(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
+                const int g0 = ti.slice * a.gps;
+                const int g1 = min(n_groups, (ti.slice + 1) * a.gps);
+                const uint8_t *wg = a.Wp + (unsigned long long)ti.group * a.w_group_stride;
+                for (int grp = g0; grp < g1; ++grp) {
+                    if (q >= S && !mbar_wait(empty_bar(st), ((q / S) - 1) & 1, abort_flag, a.err))
+                        goto producer_done;
+                    const uint32_t xs = smem_u32(smem + L.off_x + st * L.x_stage);
+                    mbar_arrive_expect_tx(full_bar(st), 2 * x_bytes + kGroupBytes);
+                    tma_load_2d(xs, &tmap_x, grp * kGroup, ti.x_row0, full_bar(st));
+                    tma_load_2d(xs + x_bytes, &tmap_x, grp * kGroup + kChunkK, ti.x_row0, full_bar(st));
+                    bulk_g2s(smem_u32(smem + L.off_w + st * kGroupBytes),
+                             wg + ((size_t)ti.ft * KC + 2 * grp) * kChunkBytes, kGroupBytes, full_bar(st));
+                    ++q;
+                    st = (st + 1 == S) ? 0 : st + 1;
+                }
+            }
+        producer_done:
+            if (*abort_flag) {
+                for (int u = q > S ? q - S : 0; u < q; ++u) drain_wait_tc(full_bar(u % S), (u / S) & 1);
+            }
+        }
+    } else if (warp == kTcMmaWarp) {
+        if (lane == 0) {
+            int st = 0, q = 0, sa = 0, qa = 0, tiles = 0;
+            TileInfo ti;
+            for (int id = blockIdx.x; tc_tile(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
+                if (tiles > 0 && !mbar_wait(dempty_bar, (tiles - 1) & 1, abort_flag, a.err)) break;
+                tc_fence_after();
+                const int g0 = ti.slice * a.gps;
+                const int g1 = min(n_groups, (ti.slice + 1) * a.gps);
+                bool ok = true;
+                for (int grp = g0; grp < g1; ++grp) {
+                    if (!mbar_wait(full_bar(st), (q / S) & 1, abort_flag, a.err) ||
+                        !mbar_wait(afull_bar(sa), (qa / SA) & 1, abort_flag, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xs = smem_u32(smem + L.off_x + st * L.x_stage);
+                    const uint32_t acol = tmem_base + uint32_t(a.bt) + 64u * sa;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint64_t bdesc = tc_sdesc_sw128(xs + h * x_bytes);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            tc_mma_ts(tmem_base + kTcDCol, acol + 32u * h + 8u * j, bdesc + 2u * j,
+                                      idesc, (grp > g0 || h > 0 || j > 0) ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(st));
+                    tc_commit(aempty_bar(sa));
+                    ++q;
+                    st = (st + 1 == S) ? 0 : st + 1;
+                    ++qa;
+                    sa = (sa + 1 == SA) ? 0 : sa + 1;
+                }
+                if (!ok) break;
+                tc_commit(dfull_bar);
+                ++tiles;
+            }
+            // Every MMA this thread issued has completed before TMEM is freed.
+            tc_commit(done_bar);
+            drain_wait_tc(done_bar, 0);
+        }
+    } else {
+        // Dequantisers and epilogue.
+        const int sub = warp & 3;                   // TMEM sub-partition of this warp
+        const int half = warp >> 2;                 // which 16 lanes of the sub-partition
+        const int block = 2 * sub + half;           // 16-row block of the tile
+        const int g = lane >> 2;
+        const uint32_t lane_base = uint32_t(32 * sub + 16 * half) << 16;
+        unsigned char *epi = smem + L.off_epi + warp * kEpiBytesPerWarp;
+        int st = 0, q = 0, sa = 0, qa = 0, tiles = 0;
+        // Scales of the next group (possibly in the next tile), loaded one group
+        // ahead so the dequantisers never wait on them.
+        uint32_t n0 = 0, n1 = 0;
+        bool have_next = false;
+        // An A stage whose TMEM store is still in flight: its completion is
+        // waited for only after the next group is dequantised, so the store
+        // latency overlaps the ALU work.
+        bool pending = false;
+        int sa_pend = 0;
+        auto flush = [&]() {
+            if (pending) {
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(afull_bar(sa_pend));
+                pending = false;
+            }
+        };
+        TileInfo ti, nx;
+        for (int id = blockIdx.x; tc_tile(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
+            const bool nx_ok = tc_tile(a, tab_tiles, tab_rows, id + gridDim.x, nx);
+            const int g0 = ti.slice * a.gps;
+            const int g1 = min(n_groups, (ti.slice + 1) * a.gps);
+            const int r0 = ti.ft * kTileRows + 16 * block + g;     // weight rows r0, r0 + 8
+            const uint16_t *sg = a.S + (unsigned long long)ti.group * a.s_group_stride;
+            bool ok = true;
+            for (int grp = g0; grp < g1; ++grp) {
+                uint32_t s0, s1;
+                if (have_next) {
+                    s0 = n0;
+                    s1 = n1;
+                } else {
+                    s0 = scale_pair(sg, r0, a.N, size_t(r0) * n_groups + grp);
+                    s1 = scale_pair(sg, r0 + 8, a.N, size_t(r0 + 8) * n_groups + grp);
+                }
+                have_next = false;
+                if (grp + 1 < g1) {
+                    n0 = scale_pair(sg, r0, a.N, size_t(r0) * n_groups + grp + 1);
+                    n1 = scale_pair(sg, r0 + 8, a.N, size_t(r0 + 8) * n_groups + grp + 1);
+                    have_next = true;
+                } else if (nx_ok) {
+                    const int rn = nx.ft * kTileRows + 16 * block + g;
+                    const int gn = nx.slice * a.gps;
+                    const uint16_t *sn = a.S + (unsigned long long)nx.group * a.s_group_stride;
+                    n0 = scale_pair(sn, rn, a.N, size_t(rn) * n_groups + gn);
+                    n1 = scale_pair(sn, rn + 8, a.N, size_t(rn + 8) * n_groups + gn);
+                    have_next = true;
+                }
+                if (!mbar_wait(full_bar(st), (q / S) & 1, abort_flag, a.err)) { ok = false; break; }
+                const unsigned char *wsrc = smem + L.off_w + st * kGroupBytes + block * kBlockBytes + lane * 16;
+                const uint4 wa = *reinterpret_cast<const uint4 *>(wsrc);
+                const uint4 wb = *reinterpret_cast<const uint4 *>(wsrc + kChunkBytes);
+                const uint32_t wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+                uint32_t frag[32];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    // Repetition j of the 16x256b store: {row g: pair 0, pair 1},
+                    // {row g+8: pair 0, pair 1} of columns 16j + 4t of the group.
+                    frag[4 * j + 0] = bf16x2_mul(minus136(magic_pair(wv[j])), s0);
+                    frag[4 * j + 1] = bf16x2_mul(minus136(magic_pair(wv[j] >> 8)), s0);
+                    frag[4 * j + 2] = bf16x2_mul(minus136(magic_pair(wv[j] >> 4)), s1);
+                    frag[4 * j + 3] = bf16x2_mul(minus136(magic_pair(wv[j] >> 12)), s1);
+                }
+                ++q;
+                st = (st + 1 == S) ? 0 : st + 1;
+                flush();
+                if (qa >= SA && !mbar_wait(aempty_bar(sa), ((qa / SA) - 1) & 1, abort_flag, a.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                tc_st_16x256b_x8(tmem_base + lane_base + uint32_t(a.bt) + 64u * sa, frag);
+                pending = true;
+                sa_pend = sa;
+                ++qa;
+                sa = (sa + 1 == SA) ? 0 : sa + 1;
+            }
+            flush();
+            if (!ok) break;
+            // Epilogue: warp (sub, half) reads lanes 32 sub .. 32 sub + 31 (its
+            // weight rows) for every other 32-token column block.
+            if (!mbar_wait(dfull_bar, tiles & 1, abort_flag, a.err)) break;
+            tc_fence_after();
+            const int fb = ti.ft * kTileRows + 32 * sub;           // first weight row of the warp
+            for (int cb = half; cb * 32 < a.bt; cb += 2) {
+                uint32_t v[32];
+                tc_ld_32x32b_x32(tmem_base + (uint32_t(32 * sub) << 16) + kTcDCol + 32u * cb, v);
+                tc_wait_ld();
+                const int t0 = ti.x_row0 + cb * 32;                // token of v[0]
+                const int nt = min(32, ti.rows - cb * 32);         // valid tokens of the block
+                if (kSplit || !a.vec_store) {
+                    const int f = fb + lane;
+                    if (f < a.N) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            if (i < nt) {
+                                const size_t off = size_t(t0 + i) * a.N + f;
+                                if (kSplit)
+                                    a.ws[size_t(ti.slice) * a.M_total * a.N + off] = __uint_as_float(v[i]);
+                                else
+                                    a.Y[off] = f32_to_bf16_rn(__uint_as_float(v[i]));
+                            }
+                        }
+                    }
+                } else {
+                    // Transpose through shared memory: [token][32 rows] bf16, then
+                    // each lane writes 16 bytes (8 rows) of four tokens.
+                    uint16_t *tile = reinterpret_cast<uint16_t *>(epi);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) tile[i * 32 + lane] = f32_to_bf16_rn(__uint_as_float(v[i]));
+                    __syncwarp();
+                    const int chunk = lane & 3;
+                    const int f8 = fb + 8 * chunk;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int i = (lane >> 2) + 8 * c;
+                        if (i < nt && f8 < a.N) {
+                            const uint4 val = *reinterpret_cast<const uint4 *>(tile + i * 32 + 8 * chunk);
+                            *reinterpret_cast<uint4 *>(a.Y + size_t(t0 + i) * a.N + f8) = val;
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dempty_bar);
+            ++tiles;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kTcMmaWarp) tc_dealloc(tmem_base, uint32_t(a.tmem_cols));
+}
+
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiledFn encode_tiled() {
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        f = reinterpret_cast<EncodeTiledFn>(p);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
+}  // namespace
+
+// A ring depth: four group stages when a CTA has the TMEM to itself, two when
+// the tile is small enough for two CTAs to share an SM's 512 columns.
+int tensor_a_stages(int bt) { return bt <= 128 ? 2 : 4; }
+
+int tensor_tmem_cols(int bt) {
+    const int need = bt + 64 * tensor_a_stages(bt);
+    int cols = 32;
+    while (cols < need) cols <<= 1;
+    return cols;
+}
+
+size_t tensor_smem_bytes(int bt, int stages, int num_groups) {
+    return size_t(tc_smem_layout(bt, stages, tensor_a_stages(bt), num_groups).total) + 1024;  // + alignment slack
+}
+
+cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t *Wp,
+                          const uint16_t *S, uint16_t *Y, float *ws, const int32_t *m_sizes,
+                          int *status, int num_groups, int M_total, int N, int K, cudaStream_t s) {
+    if (p.tile_tokens < 32 || p.tile_tokens > 256 || p.tile_tokens % 32 || p.stages < 2 ||
+        p.ctas < 1 || num_groups < 1 || num_groups > kMaxGroups)
+        return cudaErrorInvalidValue;
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap tmap;
+    const cuuint64_t gdim[2] = {cuuint64_t(K), cuuint64_t(M_total)};
+    const cuuint64_t gstride[1] = {cuuint64_t(K) * 2};
+    const cuuint32_t box[2] = {64u, cuuint32_t(p.tile_tokens)};
+    const cuuint32_t estride[2] = {1u, 1u};
+    CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(X), gdim,
+                     gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+    TcArgs a;
+    a.Wp = Wp;
+    a.S = S;
+    a.Y = Y;
+    a.ws = ws;
+    a.m_sizes = m_sizes;
+    a.status = status;
+    a.err = device_error_word();
+    if (!a.err) return cudaErrorUnknown;
+    a.M_total = M_total;
+    a.N = N;
+    a.K = K;
+    a.num_groups = num_groups;
+    a.bt = p.tile_tokens;
+    a.n_tiles = p.n_tiles;
+    a.split_k = p.split_k;
+    a.gps = p.groups_per_slice;
+    a.stages = p.stages;
+    a.a_stages = tensor_a_stages(p.tile_tokens);
+    a.tmem_cols = tensor_tmem_cols(p.tile_tokens);
+    a.vec_store = (N % 8 == 0) && (reinterpret_cast<uintptr_t>(Y) % 16 == 0);
+    a.w_group_stride = packed_bytes(N, K);
+    a.s_group_stride = (unsigned long long)N * (K / kGroup);
+
+    const bool split = p.split_k > 1;
+    auto kern = split ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
+    static std::atomic<unsigned long long> opted[2];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(opted[split].load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTensorMaxSmem);
+        if (e != cudaSuccess) return e;
+        opted[split].fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const size_t smem = tensor_smem_bytes(p.tile_tokens, p.stages, num_groups);
+    if (smem > size_t(kTensorMaxSmem)) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.ctas);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmap, a);
+}
+
+}  // namespace w4a16

@@ -60,8 +60,9 @@ typedef enum {
 /* Overrides for tests and tuning.  Zero-initialised = automatic. */
 typedef struct {
     int arm;          /* w4a16_arm */
-    int split_k;      /* 0 = automatic, else the number of K slices (clamped to K/128) */
-    int tile_tokens;  /* tensor arm only: 0 = automatic, else tokens per tile (16..256, multiple of 16) */
+    int split_k;      /* 0 = automatic, else the number of K slices: clamped to K/128, and
+                         for the decode arm raised to at least K/1024 (8 groups per slice) */
+    int tile_tokens;  /* tensor arm only: 0 = automatic, else tokens per tile (32..256, multiple of 32) */
 } w4a16_options;
 
 /* What the dispatcher chose for a shape on the current device. */
@@ -162,7 +163,7 @@ w4a16_status w4a16_grouped_workspace_bytes(int num_groups, int M_total, int N, i
  *             a negative size (treated as 0); bit 1 = the sizes sum past
  *             M_total (rows at or past M_total are not computed).  Rows no
  *             group covers are left unwritten.
- * 1 <= num_groups <= 4096. */
+ * 1 <= num_groups <= 1024. */
 w4a16_status w4a16_gemm_grouped(const w4a16_bf16 *X, const uint8_t *W_packed,
                                 const w4a16_bf16 *scales, const int32_t *M_sizes_dev,
                                 w4a16_bf16 *Y, int num_groups, int M_total, int N, int K,

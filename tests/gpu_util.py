@@ -49,7 +49,7 @@ def layout_model(w_canon: np.ndarray, N: int, K: int) -> np.ndarray:
 
     Tiles of 128 rows x 64 columns, 4096 bytes each, tile-major then chunk;
     inside, 8 blocks of 16 rows; lane L = 4g + t holds 4 words; word j covers
-    rows {g, g+8} and columns 64*chunk + 16t + 4j + {0..3} with nibble slots
+    rows {g, g+8} and columns 64*chunk + 16j + 4t + {0..3} with nibble slots
     (bit: row, column offset) 0:g,0 4:g+8,0 8:g,2 12:g+8,2 16:g,1 20:g+8,1
     24:g,3 28:g+8,3.  Padding rows hold code 8."""
     n_pad = (N + 127) // 128 * 128
@@ -62,7 +62,7 @@ def layout_model(w_canon: np.ndarray, N: int, K: int) -> np.ndarray:
     g, t = lane // 4, lane % 4
     r0 = tile * 128 + block * 16 + g
     r1 = r0 + 8
-    k = chunk * 64 + 16 * t + 4 * j
+    k = chunk * 64 + 16 * j + 4 * t
     w = (codes[r0, k] | (codes[r1, k] << 4) | (codes[r0, k + 2] << 8) | (codes[r1, k + 2] << 12)
          | (codes[r0, k + 1] << 16) | (codes[r1, k + 1] << 20) | (codes[r0, k + 3] << 24)
          | (codes[r1, k + 3] << 28))

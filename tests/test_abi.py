@@ -53,7 +53,7 @@ def test_library_does_not_need_libcudart_or_libcuda(L):
 
 
 def test_host_only_queries(L):
-    assert L.w4a16_layout_version() == 1
+    assert L.w4a16_layout_version() == 2
     assert L.w4a16_packed_weight_bytes(8192, 8192) == 8192 * 4096
     assert L.w4a16_packed_weight_bytes(200, 256) == 256 * 128      # rows padded to 128
     assert L.w4a16_packed_weight_bytes(1, 128) == 128 * 64

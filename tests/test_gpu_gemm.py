@@ -108,6 +108,43 @@ def test_decode_arm_splits_on_workload_shapes(M, N, K, split_k):
     assert_close(bf16_to_f64(y), reference(p), what=f"decode M{M} N{N} K{K} SK{split_k}")
 
 
+@pytest.mark.parametrize("M", [1, 16, 17, 32, 33, 64, 100, 300])
+@pytest.mark.parametrize("tile_tokens", [32, 96, 256])
+@pytest.mark.parametrize("split_k", [1, 2, 5])
+def test_tensor_arm_tiles_and_splits(M, tile_tokens, split_k):
+    N, K = 300, 640        # 3 weight tiles with a ragged last one, 5 groups
+    p = problem(M, N, K, seed=M + 1)
+    y = run(p, arm="tensor", split_k=split_k, tile_tokens=tile_tokens)
+    plan = w4.plan(M, N, K, arm="tensor", split_k=split_k, tile_tokens=tile_tokens)
+    assert plan["arm"] == "tensor" and plan["tile_tokens"] == tile_tokens
+    assert plan["split_k"] == split_k
+    assert_close(bf16_to_f64(y), reference(p), what=f"tensor M{M} BT{tile_tokens} SK{split_k}")
+
+
+@pytest.mark.parametrize("M,N,K", [(32, 19456, 2560), (128, 2560, 9728), (1322, 2560, 9728)])
+@pytest.mark.parametrize("tile_tokens", [64, 224])
+def test_tensor_arm_workload_shapes(M, N, K, tile_tokens):
+    p = problem(M, N, K)
+    y = bf16_to_f64(run(p, arm="tensor", tile_tokens=tile_tokens))
+    cols = sample_cols(N, 128)
+    assert_close(y[:, cols], reference(p, cols), what=f"tensor M{M} N{N} K{K} BT{tile_tokens}")
+
+
+def test_tensor_arm_matches_bf16_operand_exactly_on_one_group():
+    # With unit activations on one column and K = 128 the output is the bf16
+    # weight operand itself (one product, exact accumulation): compare bits.
+    M, N, K = 32, 256, 128
+    inp = syn.make_gemm_inputs(M, N, K, seed=9)
+    inp.x[:] = 0
+    for m in range(M):
+        inp.x[m, (m * 5) % K] = 0x3F80
+    p = DeviceProblem(inp)
+    y = bf16_to_u16(run(p, arm="tensor"))
+    wq = oracle.dequant_bf16(inp.w_canon, inp.scales, N, K)
+    for m in range(M):
+        assert np.array_equal(y[m], wq[:, (m * 5) % K])
+
+
 @pytest.mark.parametrize("M", [17, 40, 100])
 def test_decode_arm_many_token_blocks(M):
     p = problem(M, 256, 512, seed=M)
