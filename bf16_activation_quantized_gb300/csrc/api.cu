@@ -45,9 +45,10 @@ namespace {
 
 constexpr int kDecodeCtasPerSm = 2;           // resident decode CTAs per SM
 constexpr double kHbmBytesPerS = 6.5e12;      // planning figures, not measurements
-constexpr double kCtaBytesPerS = 50e9;        // one CTA's streaming rate (64 KB ring)
+constexpr double kCtaBytesPerS = 25e9;        // one CTA's streaming rate (32 KB in flight)
 constexpr double kL2BytesPerS = 20e12;
 constexpr double kReduceSeconds = 0.5e-6;
+constexpr double kReducePerSliceSeconds = 0.04e-6;  // reduce latency per extra slice
 constexpr int kDecodeMaxM = 16;               // auto dispatch: M <= 16 -> decode arm
 constexpr double kClockHz = 1.9e9;            // planning clock
 constexpr int kTensorMaxStages = 8;
@@ -87,31 +88,41 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, DecodePlan *d) 
     const long long slots = (long long)kDecodeCtasPerSm * sms;
     const double w_bytes = double(d->n_tiles) * kTileRows * double(K) / 2.0;
     double best = 1e30;
-    int min_split = ceil_div(groups, kDecodeMaxGps);
-    for (int gps = kDecodeMaxGps; gps >= 1; --gps) {
-        int sk = ceil_div(groups, gps);
-        if (forced_split > 0) sk = forced_split < min_split ? min_split : (forced_split > groups ? groups : forced_split);
-        const int gps_eff = ceil_div(groups, sk);
-        sk = ceil_div(groups, gps_eff);
+    d->split_k = groups;
+    d->groups_per_slice = 1;
+    d->ctas_per_slice = 1;
+    // Slices hold 1, 2, 4 or 8 groups and divide K exactly (the kernel unrolls
+    // a slice at compile time).  A forced split picks the feasible slice count
+    // closest to the request from above.
+    int forced_gps = 0;
+    if (forced_split > 0) {
+        for (int gps : {8, 4, 2, 1})
+            if (groups % gps == 0 && groups / gps >= forced_split) { forced_gps = gps; break; }
+        if (!forced_gps) forced_gps = 1;
+    }
+    for (int gps : {8, 4, 2, 1}) {
+        if (groups % gps) continue;
+        if (forced_gps && gps != forced_gps) continue;
+        const int sk = groups / gps;
         const long long per_slice = slots / ((long long)sk * d->token_blocks);
         const int cmax = int(per_slice < 1 ? 1 : (per_slice > d->n_tiles ? d->n_tiles : per_slice));
         for (int C = cmax; C >= 1; --C) {
             const int tiles_per = ceil_div(d->n_tiles, C);
             if (C < cmax && ceil_div(d->n_tiles, C + 1) == tiles_per) continue;  // same critical path, fewer CTAs
-            const double cta_bytes = double(tiles_per) * 2.0 * gps_eff * kChunkBytes * d->token_blocks;
+            const double cta_bytes = double(tiles_per) * 2.0 * gps * kChunkBytes * d->token_blocks;
             double t = w_bytes * d->token_blocks / kHbmBytesPerS;
             const double t_cta = cta_bytes / kCtaBytesPerS;
             if (t_cta > t) t = t_cta;
             if (sk > 1)
-                t += 2.0 * double(sk) * M * N * 4.0 / kL2BytesPerS + kReduceSeconds;
+                t += 2.0 * double(sk) * M * N * 4.0 / kL2BytesPerS + kReduceSeconds +
+                     kReducePerSliceSeconds * sk;
             if (t < best * 0.999) {
                 best = t;
                 d->split_k = sk;
-                d->groups_per_slice = gps_eff;
+                d->groups_per_slice = gps;
                 d->ctas_per_slice = C;
             }
         }
-        if (forced_split > 0) break;
     }
 }
 

@@ -30,11 +30,11 @@ struct TensorPlan {
 int device_sm_count(int *sms);  // returns cudaError_t as int
 int *device_error_word();        // device address of the error word (nullptr on failure)
 
-// Decode arm shared memory: the staged X slice, its per-group sums and the
-// slice's scales.  The planner keeps a CTA under kDecodeSmemTarget so that
-// several CTAs share an SM; kDecodeMaxSmem is the hard limit.
+// Decode arm shared memory: the weight ring, the staged X slice and its
+// per-group sums.  kDecodeMaxSmem lets two CTAs share an SM (228 KB, of which
+// 1 KB per CTA is reserved).
 constexpr int kDecodeMaxGps = 8;
-constexpr int kDecodeMaxSmem = 110 * 1024;
+constexpr int kDecodeMaxSmem = 113 * 1024;
 int decode_smem_needed(int M, int mt, int groups_per_slice);
 
 size_t packed_bytes(int N, int K);

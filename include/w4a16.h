@@ -60,8 +60,9 @@ typedef enum {
 /* Overrides for tests and tuning.  Zero-initialised = automatic. */
 typedef struct {
     int arm;          /* w4a16_arm */
-    int split_k;      /* 0 = automatic, else the number of K slices: clamped to K/128, and
-                         for the decode arm raised to at least K/1024 (8 groups per slice) */
+    int split_k;      /* 0 = automatic, else the requested number of K slices, clamped to
+                         K/128.  The decode arm rounds it up to the nearest count whose
+                         slices hold 1, 2, 4 or 8 of the 128-wide groups each. */
     int tile_tokens;  /* tensor arm only: 0 = automatic, else tokens per tile (32..256, multiple of 32) */
 } w4a16_options;
 

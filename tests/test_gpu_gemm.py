@@ -96,7 +96,18 @@ def test_decode_arm_every_split(M, split_k):
     p = problem(M, N, K, seed=M)
     y = run(p, arm="decode", split_k=split_k)
     plan = w4.plan(M, N, K, arm="decode", split_k=split_k)
-    assert plan["split_k"] == split_k
+    # 5 groups: every slice holds one group, whatever split is requested
+    assert plan["split_k"] == 5
+    assert_close(bf16_to_f64(y), reference(p), what=f"decode M{M} SK{split_k}")
+
+
+@pytest.mark.parametrize("M", [1, 5, 8, 12, 16])
+@pytest.mark.parametrize("split_k", [1, 2, 4, 8])
+def test_decode_arm_slice_sizes(M, split_k):
+    N, K = 300, 1024       # 8 groups: slices of 8, 4, 2 and 1 groups
+    p = problem(M, N, K, seed=M + 100)
+    y = run(p, arm="decode", split_k=split_k)
+    assert w4.plan(M, N, K, arm="decode", split_k=split_k)["split_k"] == split_k
     assert_close(bf16_to_f64(y), reference(p), what=f"decode M{M} SK{split_k}")
 
 
@@ -171,15 +182,32 @@ def test_empty_m_is_a_noop():
     assert st == 0
 
 
+def _bf16_bits_to_f64(bits):
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
 def test_all_eights_and_zero_scales_give_zero():
-    inp = syn.make_gemm_inputs(5, 300, 640, seed=3)
+    M, N, K = 5, 300, 640
+    inp = syn.make_gemm_inputs(M, N, K, seed=3)
     inp.w_canon[:] = 0x88
     p = DeviceProblem(inp)
-    assert np.all(bf16_to_f64(run(p)) == 0.0)
-    inp2 = syn.make_gemm_inputs(5, 300, 640, seed=3)
+    # The tensor arm multiplies exact zeros (code - 8 = 0): exactly 0.
+    assert np.all(bf16_to_f64(run(p, arm="tensor")) == 0.0)
+    # The decode arm feeds the tensor core 128 + code and removes 136 * sum(x)
+    # per 128-wide group, so zero codes cancel only up to fp32 rounding of
+    # terms of size 136 * sum|x|: bound each output by that, with margin
+    # (2^-18 relative; the observed residue is near 2^-24).
+    x = _bf16_bits_to_f64(inp.x).reshape(M, K // 128, 128)
+    s = _bf16_bits_to_f64(inp.scales)                        # [N][K/128]
+    bound = 136.0 * np.abs(x).sum(axis=2) @ np.abs(s).T * 2.0 ** -18   # [M][N]
+    y = bf16_to_f64(run(p, arm="decode"))
+    assert np.all(np.abs(y) <= bound)
+    assert np.max(np.abs(y)) < 1e-4
+    inp2 = syn.make_gemm_inputs(M, N, K, seed=3)
     inp2.scales[:] = 0
     p2 = DeviceProblem(inp2)
-    assert np.all(bf16_to_f64(run(p2)) == 0.0)
+    for arm in ("decode", "tensor"):
+        assert np.all(bf16_to_f64(run(p2, arm=arm)) == 0.0)
 
 
 def test_unit_scales_one_hot_is_exact():
