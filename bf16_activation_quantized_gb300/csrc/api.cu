@@ -44,11 +44,13 @@ using namespace w4a16;
 namespace {
 
 constexpr int kDecodeCtasPerSm = 2;           // resident decode CTAs per SM
+constexpr int kDecodeRing = 8;                // weight-ring stages per decode CTA
+constexpr int kDecodeInFlight = 3;            // bulk copies in the air per decode CTA
 constexpr double kHbmBytesPerS = 6.5e12;      // planning figures, not measurements
 constexpr double kCtaBytesPerS = 25e9;        // one CTA's streaming rate (32 KB in flight)
 constexpr double kL2BytesPerS = 20e12;
 constexpr double kReduceSeconds = 0.5e-6;
-constexpr double kReducePerSliceSeconds = 0.04e-6;  // reduce latency per extra slice
+constexpr double kReducePerSliceSeconds = 0.01e-6;  // reduce latency per extra slice
 constexpr int kDecodeMaxM = 16;               // auto dispatch: M <= 16 -> decode arm
 constexpr double kClockHz = 1.9e9;            // planning clock
 constexpr int kTensorMaxStages = 8;
@@ -75,6 +77,20 @@ struct Plan {
 
 int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
 
+// Measured on GB300 across the decode workloads (1 to 16 tokens, N 2560 to
+// 19456, K 2560 to 9728): at equal modelled time, 4-group slices run fastest
+// (more tiles per CTA keep its copy ring busy without long unrolled slices),
+// then 8, 2, 16 and 1.  The factor breaks near-ties in that order.
+double decode_slice_preference(int gps) {
+    switch (gps) {
+        case 4: return 1.0;
+        case 8: return 1.04;
+        case 2: return 1.06;
+        case 16: return 1.08;
+        default: return 1.12;
+    }
+}
+
 // Decode-arm grid: each CTA keeps one K slice (gps groups) and streams tiles
 // c, c + C, ... of it.  Modelled time = max(all weight bytes at HBM speed,
 // the busiest CTA's bytes at one CTA's streaming rate) + the split-K
@@ -91,17 +107,24 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, DecodePlan *d) 
     d->split_k = groups;
     d->groups_per_slice = 1;
     d->ctas_per_slice = 1;
-    // Slices hold 1, 2, 4 or 8 groups and divide K exactly (the kernel unrolls
-    // a slice at compile time).  A forced split picks the feasible slice count
+    d->ring = kDecodeRing;
+    d->in_flight = kDecodeInFlight;
+    // Slices hold 1, 2, 4, 8 or 16 groups and divide K exactly (the kernel
+    // unrolls a slice at compile time).  A forced split picks the feasible slice count
     // closest to the request from above.
+    // 16-group slices only for one token octet (register budget).
+    const int gps_max = d->mt == 1 ? 16 : 8;
     int forced_gps = 0;
     if (forced_split > 0) {
-        for (int gps : {8, 4, 2, 1})
-            if (groups % gps == 0 && groups / gps >= forced_split) { forced_gps = gps; break; }
+        for (int gps : {16, 8, 4, 2, 1})
+            if (gps <= gps_max && groups % gps == 0 && groups / gps >= forced_split) {
+                forced_gps = gps;
+                break;
+            }
         if (!forced_gps) forced_gps = 1;
     }
-    for (int gps : {8, 4, 2, 1}) {
-        if (groups % gps) continue;
+    for (int gps : {16, 8, 4, 2, 1}) {
+        if (gps > gps_max || groups % gps) continue;
         if (forced_gps && gps != forced_gps) continue;
         const int sk = groups / gps;
         const long long per_slice = slots / ((long long)sk * d->token_blocks);
@@ -116,6 +139,7 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, DecodePlan *d) 
             if (sk > 1)
                 t += 2.0 * double(sk) * M * N * 4.0 / kL2BytesPerS + kReduceSeconds +
                      kReducePerSliceSeconds * sk;
+            t *= decode_slice_preference(gps);
             if (t < best * 0.999) {
                 best = t;
                 d->split_k = sk;

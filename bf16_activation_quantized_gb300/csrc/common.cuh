@@ -135,6 +135,16 @@ __device__ __forceinline__ void mma_16816_c(float (&d)[4], const uint32_t (&a)[4
           "f"(c[2]), "f"(c[3]));
 }
 
+// Same with fp16 operands.
+__device__ __forceinline__ void mma_16816_f16_c(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                uint32_t b1, const float (&c)[4]) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+          "f"(c[2]), "f"(c[3]));
+}
+
 __device__ __forceinline__ uint4 ldg_nc16(const void *p) {
     uint4 r;
     asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

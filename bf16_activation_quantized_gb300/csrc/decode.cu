@@ -40,37 +40,64 @@ namespace w4a16 {
 namespace {
 
 constexpr int kDecodeWarps = 8;                                 // consumer warps
+constexpr uint32_t kMagicF16x2_1024 = 0x64006400u;              // fp16x2 {1024, 1024}
 constexpr int kDecodeThreads = (kDecodeWarps + 1) * 32;         // + one producer warp
 constexpr int kStageBytes = 2 * kChunkBytes;                    // one 128-wide group of a tile
 constexpr int kDecodeMaxStages = 16;
 
-// Shared memory: the weight ring first (a whole number of tiles' worth of
-// groups, as many as the budget allows, at most kDecodeMaxStages stages), then
-// its barriers, the abort flag, the staged X slice and the per-group
-// correction table.
+// Shared memory: the weight ring first (as many 8 KB stages as the budget
+// leaves, at most kDecodeMaxStages), then its barriers, the abort flag, the
+// per-token maxima, the staged X rows of the token block and the per-group
+// correction table.  Host and kernel size it from the same row count,
+// min(8 * MT, M).
 struct DecodeSmem {
-    int x_stride;      // bf16 elements per staged X row: slice + 32 (row stride = 64 B mod 128 B)
-    int ring_tiles;    // tiles of the slice held by the ring
-    int stages;        // ring_tiles * groups per slice
-    int off_ring, off_bar, off_abort, off_x, off_corr, total;
+    int x_stride;      // 16-bit elements per staged X row: slice + 32 (row stride = 64 B mod 128 B)
+    int stages;
+    int off_ring, off_bar, off_abort, off_xmax, off_x, off_corr, total;
 };
 
-__host__ __device__ inline DecodeSmem decode_smem_layout(int mt, int gps) {
+__host__ __device__ inline DecodeSmem decode_smem_layout(int mt, int rows, int gps) {
     DecodeSmem L;
-    const int rows = 8 * mt;
     L.x_stride = gps * kGroup + 32;
-    const int rest = 2 * kDecodeMaxStages * 8 + 16 + rows * L.x_stride * 2 + rows * gps * 4;
-    int kt = (kDecodeMaxSmem - rest) / (gps * kStageBytes);
-    if (kt > kDecodeMaxStages / gps) kt = kDecodeMaxStages / gps;
-    L.ring_tiles = kt;
-    L.stages = kt * gps;
+    const int corr_bytes = gps * mt * 4 * 16;        // one float4 per (group, octet, quad)
+    const int rest = 2 * kDecodeMaxStages * 8 + 16 + 64 + rows * L.x_stride * 2 + corr_bytes;
+    int n = (kDecodeMaxSmem - rest) / kStageBytes;
+    L.stages = n > kDecodeMaxStages ? kDecodeMaxStages : n;
     L.off_ring = 0;
     L.off_bar = L.stages * kStageBytes;
     L.off_abort = L.off_bar + 2 * kDecodeMaxStages * 8;
-    L.off_x = L.off_abort + 16;
+    L.off_xmax = L.off_abort + 16;
+    L.off_x = L.off_xmax + 64;
     L.off_corr = L.off_x + rows * L.x_stride * 2;
-    L.total = L.off_corr + rows * gps * 4;
+    L.total = L.off_corr + corr_bytes;
     return L;
+}
+
+// Power-of-two exponent sh for a token's slice of X: x * 2^-sh puts the
+// largest |x| in [2^14, 2^15), so every bf16 value down to 2^-31 of it is
+// exact in fp16 (fp16 keeps 11 significant bits, bf16 has 8, and fp16
+// subnormals still hold 8 bits down to 2^-17).  Clamped so that 2^-sh and
+// 2^sh are normal fp32 numbers.
+__device__ __forceinline__ int slice_shift(int max_abs_bits) {
+    int sh = ((max_abs_bits >> 7) & 0xFF) - 127 - 14;
+    return sh < -100 ? -100 : (sh > 114 ? 114 : sh);
+}
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// 16-byte shared load done only when pred != 0; otherwise v keeps its value.
+__device__ __forceinline__ void lds128_if(uint4 &v, const void *p, uint32_t pred) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %4, 0;\n\t"
+        "@q ld.shared.v4.u32 {%0,%1,%2,%3}, [%5];\n\t}"
+        : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+        : "r"(pred), "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void consumer_bar() {
@@ -98,7 +125,15 @@ __device__ __forceinline__ ScaleRow<GPS> load_scale_row(const uint16_t *p, bool 
 #pragma unroll
     for (int i = 0; i < (GPS + 1) / 2; ++i) r.w[i] = 0;
     if (!ok) return r;
-    if constexpr (GPS == 8) {
+    if constexpr (GPS == 16) {
+        if (vec) {
+            asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]) : "l"(p));
+            asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(r.w[4]), "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7]) : "l"(p + 8));
+            return r;
+        }
+    } else if constexpr (GPS == 8) {
         if (vec) {
             asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
                          : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]) : "l"(p));
@@ -133,22 +168,30 @@ __device__ __forceinline__ float scale_of(const ScaleRow<GPS> &r, int gi) {
 // GPS groups (GPS divides K/128, so every slice is full).  A producer warp
 // streams the 8 KB (tile, group) blocks, in order, through a ring that holds
 // ring_tiles tiles' worth of groups, so a group's slot is fixed within a tile.
-// Each consumer warp owns one 16-row block of a tile.  Per group it waits for
-// the stage, reads its 16 B of each chunk, turns the 8 words into 32 A
-// fragments, releases the stage and runs a chain of 8 MMAs whose accumulator
-// starts at -136 * sum(x) for the group, so the chain yields
-// sum_k (code_k - 8) x_k directly.  The group scales are applied when the tile
-// (or, for 16 tokens, a batch of groups) is done, so the scale loads -- issued
-// a tile ahead -- are off the critical path.
+//
+// The slice of X is staged once, as fp16 x * 2^-sh per token (exact, see
+// slice_shift), so the weights can be fp16 too: in fp16 two of a 16-bit
+// half's four nibbles lie inside the 10-bit mantissa, so a 32-bit word gives
+// its four A fragments with one shift and four LOP3s -- 1024 + code for rows
+// g (nibbles at bits 0-3) and 1024 + 16 code for rows g + 8 (bits 4-7) --
+// where bf16's 7-bit mantissa would need three shifts.  Each consumer warp
+// owns one 16-row block of a tile.  Per group it waits for the stage, reads
+// its 16 B of each chunk, builds the 32 A fragments, releases the stage and
+// runs a chain of 8 MMAs whose accumulator starts at -1032 S (rows g) or
+// -1152 S (rows g + 8), S the group's scaled sum of x, so the chain yields
+// sum_k (code_k - 8) x_k, times 16 for rows g + 8.  The group scales, the
+// 1/16 and 2^sh are applied when the tile (or, for 16 tokens, a batch of
+// groups) is done, so the scale loads -- issued a tile ahead -- are off the
+// critical path.
 template <int MT, int GPS, bool kSplit>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
               const uint16_t *__restrict__ S, uint16_t *__restrict__ Y, float *__restrict__ ws,
-              int M, int N, int K, int n_tiles, int s_vec, int *err) {
+              int M, int N, int K, int n_tiles, int ring_stages, int in_flight, int s_vec, int *err) {
     extern __shared__ __align__(128) unsigned char smem[];
-    // Groups between scale applications: the whole slice for 8 tokens, at
-    // most 4 groups for 16 (register budget).
-    constexpr int D = (MT == 1) ? GPS : (GPS < 4 ? GPS : 4);
+    // Groups between scale applications (register budget): up to 8 for 8
+    // tokens, up to 4 for 16.
+    constexpr int D = (MT == 1) ? (GPS < 8 ? GPS : 8) : (GPS < 4 ? GPS : 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -160,15 +203,16 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
     const int c0 = blockIdx.x;
     const int n_my = c0 < n_tiles ? (n_tiles - c0 + C - 1) / C : 0;
     const int KC = K / kChunkK;
-    const DecodeSmem L = decode_smem_layout(MT, GPS);
-    const int NS = L.stages;
-    const int KT = L.ring_tiles;
+    const int rows_alloc = min(8 * MT, M);
+    const DecodeSmem L = decode_smem_layout(MT, rows_alloc, GPS);
+    const int NS = min(L.stages, ring_stages);
     unsigned char *ring = smem + L.off_ring;
     const uint32_t full0 = smem_u32(smem + L.off_bar);
     const uint32_t empty0 = full0 + 8 * kDecodeMaxStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_abort);
     uint16_t *s_x = reinterpret_cast<uint16_t *>(smem + L.off_x);
     float *s_corr = reinterpret_cast<float *>(smem + L.off_corr);
+    int *s_xmax = reinterpret_cast<int *>(smem + L.off_xmax);
 
     // Let the next kernel in the stream be scheduled while this grid runs.
     pdl_launch_dependents();
@@ -178,6 +222,7 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
             mbar_init(empty0 + 8 * s, kDecodeWarps);
         }
         *abort_flag = 0;
+        for (int r = 0; r < 16; ++r) s_xmax[r] = 0;
         fence_barrier_init();
     }
     __syncthreads();
@@ -195,103 +240,171 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         dst[0] = load_scale_row<GPS>(p0, f0 < N, vec_scales);
         dst[1] = load_scale_row<GPS>(p0 + 8 * size_t(n_groups), f0 + 8 < N, vec_scales);
     };
-    if (warp < kDecodeWarps && n_my > 0) load_scales(c0, s_cur);
-
     if (warp == kDecodeWarps) {
-        // Producer: one lane streams every (tile, group) block of this CTA.
+        // Producer: one lane streams every (tile, group) block of this CTA,
+        // starting once the consumers have issued their X and scale loads so
+        // that those small reads are not queued behind the weight stream.
+        named_bar_sync(2, kDecodeThreads);
         if (lane == 0) {
             const size_t tile_step = size_t(C) * KC * kChunkBytes;
             const uint8_t *src = Wp + (size_t(c0) * KC + size_t(2 * grp0)) * kChunkBytes;
-            int issued = 0, ts = 0;
+            // At most in_flight copies are in the air at once (the ring may
+            // hold more that have landed): a small burst per CTA lets the
+            // first stages land early instead of all of them near the end.
+            const int total = n_my * GPS;
+            int issued = 0, st = 0, gi = 0, lst = 0;
             uint32_t epar = 1;   // parity of the empty phase to wait for (first lap: none)
-            bool ok = true;
-            for (int it = 0; it < n_my && ok; ++it) {
-                const int base = ts * GPS;
-#pragma unroll
-                for (int gi = 0; gi < GPS; ++gi) {
-                    const int slot = base + gi;
-                    if (it >= KT && !mbar_wait(empty0 + 8 * slot, epar, abort_flag, err)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(full0 + 8 * slot, kStageBytes);
-                    bulk_g2s(smem_u32(ring + slot * kStageBytes), src + gi * kStageBytes,
-                             kStageBytes, full0 + 8 * slot);
-                    ++issued;
+            uint32_t lpar = 0;   // parity of the full phase of copy q - in_flight
+            for (int q = 0; q < total; ++q) {
+                if (q >= NS && !mbar_wait(empty0 + 8 * st, epar, abort_flag, err)) break;
+                if (q >= in_flight) {
+                    if (!mbar_wait(full0 + 8 * lst, lpar, abort_flag, err)) break;
+                    if (++lst == NS) { lst = 0; lpar ^= 1; }
                 }
-                src += tile_step;
-                if (++ts == KT) { ts = 0; epar ^= 1; }
+                mbar_arrive_expect_tx(full0 + 8 * st, kStageBytes);
+                bulk_g2s(smem_u32(ring + st * kStageBytes), src + gi * kStageBytes, kStageBytes,
+                         full0 + 8 * st);
+                ++issued;
+                if (++gi == GPS) { gi = 0; src += tile_step; }
+                if (++st == NS) { st = 0; epar ^= 1; }
             }
             if (*abort_flag) {
-                for (int q = issued > NS ? issued - NS : 0; q < issued; ++q) {
-                    const int it = q / GPS, gi = q - it * GPS;
-                    drain_wait(full0 + 8 * ((it % KT) * GPS + gi), (it / KT) & 1);
-                }
+                for (int q = issued > NS ? issued - NS : 0; q < issued; ++q)
+                    drain_wait(full0 + 8 * (q % NS), (q / NS) & 1);
             }
         }
         return;
     }
 
+
     // Consumers: stage X[m0 .. m0+rows)[slice], permuted so that a lane's B
     // fragments for word pair q of a group are 16 contiguous bytes: natural
     // column cc of a group (chunk h, 16-column slice s, quad t, element e) goes
-    // to 32 (2h + s/2) + 8t + 4 (s % 2) + e.
+    // to 32 (2h + s/2) + 8t + 4 (s % 2) + e.  All of a thread's loads are
+    // issued before the first store, so their latencies overlap.
+    // A vector's two 8-byte halves go to pos and pos + 8; lanes of the second
+    // chunk (h = 1) store them in the other order, so each store instruction
+    // of a warp covers every bank once per 128 bytes.  The row maximum of |x|
+    // is reduced across the lanes of a row before one shared atomic.
     constexpr int vec_per_row = GPS * (kGroup / 8);
-    for (int i = threadIdx.x; i < rows * vec_per_row; i += kDecodeWarps * 32) {
+    constexpr int lanes_per_row = vec_per_row < 32 ? vec_per_row : 32;
+    constexpr int kVecPerThread = (8 * MT * vec_per_row + kDecodeWarps * 32 - 1) / (kDecodeWarps * 32);
+    const int n_vec = rows * vec_per_row;
+    uint4 xval[kVecPerThread];
+#pragma unroll
+    for (int k = 0; k < kVecPerThread; ++k) {
+        const int i = threadIdx.x + k * kDecodeWarps * 32;
+        if (i < n_vec) {
+            const int r = i / vec_per_row, v = i - r * vec_per_row;
+            xval[k] = ldg_nc16(X + size_t(m0 + r) * K + size_t(grp0) * kGroup + v * 8);
+        }
+    }
+    if (warp < kDecodeWarps && n_my > 0) load_scales(c0, s_cur);
+    named_bar_arrive(2, kDecodeThreads);
+#pragma unroll
+    for (int k = 0; k < kVecPerThread; ++k) {
+        const int i = threadIdx.x + k * kDecodeWarps * 32;
         const int r = i / vec_per_row, v = i - r * vec_per_row;
-        const uint4 val = ldg_nc16(X + size_t(m0 + r) * K + size_t(grp0) * kGroup + v * 8);
-        const int gi = v >> 4, u = v & 15;           // 16 vectors per group
-        const int h = u >> 3, s16 = (u >> 1) & 3, t0 = (u & 1) * 2;
-        const int pos = gi * kGroup + 32 * (2 * h + (s16 >> 1)) + 8 * t0 + 4 * (s16 & 1);
-        uint16_t *dst = s_x + r * L.x_stride + pos;
-        *reinterpret_cast<uint2 *>(dst) = make_uint2(val.x, val.y);
-        *reinterpret_cast<uint2 *>(dst + 8) = make_uint2(val.z, val.w);
+        uint32_t mx = 0;
+        if (i < n_vec) {
+            const uint4 val = xval[k];
+            const int gi = v >> 4, u = v & 15;           // 16 vectors per group
+            const int h = u >> 3, s16 = (u >> 1) & 3, t0 = (u & 1) * 2;
+            const int pos = gi * kGroup + 32 * (2 * h + (s16 >> 1)) + 8 * t0 + 4 * (s16 & 1);
+            uint16_t *dst = s_x + r * L.x_stride + pos;
+            const uint2 lo = make_uint2(val.x, val.y), hi = make_uint2(val.z, val.w);
+            *reinterpret_cast<uint2 *>(dst + (h ? 8 : 0)) = h ? hi : lo;
+            *reinterpret_cast<uint2 *>(dst + (h ? 0 : 8)) = h ? lo : hi;
+            // bf16 magnitudes order like their bit patterns.
+            const uint32_t m01 = max(val.x & 0x7FFFu, (val.x >> 16) & 0x7FFFu);
+            const uint32_t m23 = max(val.y & 0x7FFFu, (val.y >> 16) & 0x7FFFu);
+            const uint32_t m45 = max(val.z & 0x7FFFu, (val.z >> 16) & 0x7FFFu);
+            const uint32_t m67 = max(val.w & 0x7FFFu, (val.w >> 16) & 0x7FFFu);
+            mx = max(max(m01, m23), max(m45, m67));
+        }
+        // Whole warps take part (i < n_vec is uniform per group of lanes_per_row).
+#pragma unroll
+        for (int off = 1; off < lanes_per_row; off <<= 1)
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (i < n_vec && (lane & (lanes_per_row - 1)) == 0) atomicMax(s_xmax + r, int(mx));
     }
     if (n_my > 1) load_scales(c0 + C, s_next);
     consumer_bar();
     {
-        // Correction table s_corr[gi][token] = -136 * sum of the group's x:
-        // 8 lanes per sum, 16 values each, then a shuffle reduction.
+        // Per (token, group): 8 lanes take 16 values each, convert them in
+        // place to fp16 x * 2^-sh, and sum them (fp32, then a shuffle
+        // reduction) for the correction table: token r, group gi ->
+        // s_corr[(gi * MT + r / 8) * 4 + (r % 8) / 2] = {-1032 S(r), -1032 S(r^1),
+        // -1152 S(r), -1152 S(r^1)} (pairs of tokens 2t, 2t + 1), S the scaled sum.
         const int pairs = 8 * MT * GPS;
         const int part = threadIdx.x & 7;
         for (int base = 0; base < pairs; base += kDecodeWarps * 32 / 8) {
             const int pi = base + (threadIdx.x >> 3);
+            const int r = pi / GPS, gi = pi - r * GPS;
             float a = 0.f;
-            if (pi < pairs && pi / GPS < rows) {   // absent tokens: 0 (their rows are never read)
-                const int r = pi / GPS, gi = pi - r * GPS;
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    s_x + r * L.x_stride + gi * kGroup + part * 16);
-                const uint4 q0 = src[0], q1 = src[1];
-                a = ((bf16_lo_to_f32(q0.x) + bf16_hi_to_f32(q0.x)) +
-                     (bf16_lo_to_f32(q0.y) + bf16_hi_to_f32(q0.y))) +
-                    ((bf16_lo_to_f32(q0.z) + bf16_hi_to_f32(q0.z)) +
-                     (bf16_lo_to_f32(q0.w) + bf16_hi_to_f32(q0.w))) +
-                    (((bf16_lo_to_f32(q1.x) + bf16_hi_to_f32(q1.x)) +
-                      (bf16_lo_to_f32(q1.y) + bf16_hi_to_f32(q1.y))) +
-                     ((bf16_lo_to_f32(q1.z) + bf16_hi_to_f32(q1.z)) +
-                      (bf16_lo_to_f32(q1.w) + bf16_hi_to_f32(q1.w))));
+            if (pi < pairs && r < rows) {   // absent tokens: 0 (their rows are never stored)
+                const float down = pow2f(-slice_shift(s_xmax[r]));
+                // Lane `part` takes 8-element pieces part and 8 + part, so each
+                // access of 8 lanes covers 128 contiguous bytes.
+                uint4 *src = reinterpret_cast<uint4 *>(s_x + r * L.x_stride + gi * kGroup) + part;
+#pragma unroll
+                for (int h = 0; h < 16; h += 8) {
+                    const uint4 q = src[h];
+                    const uint32_t qv[4] = {q.x, q.y, q.z, q.w};
+                    uint32_t hv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo = bf16_lo_to_f32(qv[e]), hi = bf16_hi_to_f32(qv[e]);
+                        a += lo + hi;
+                        uint32_t pk;
+                        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(pk) : "f"(hi * down), "f"(lo * down));
+                        hv[e] = pk;
+                    }
+                    src[h] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                }
+                a *= down;
             }
             a += __shfl_xor_sync(0xffffffffu, a, 1);
             a += __shfl_xor_sync(0xffffffffu, a, 2);
             a += __shfl_xor_sync(0xffffffffu, a, 4);
             if (pi < pairs && part == 0) {
-                const int r = pi / GPS, gi = pi - r * GPS;
-                s_corr[gi * 8 * MT + r] = -136.f * a;
+                float *e = s_corr + ((gi * MT + (r >> 3)) * 4 + ((r & 7) >> 1)) * 4 + (r & 1);
+                e[0] = -1032.f * a;
+                e[2] = -1152.f * a;
             }
         }
     }
     consumer_bar();
 
     // Fragment sources: X rows 8o + g (B), correction for tokens 8o + 2t, +1 (C).
-    const bool xok0 = g < rows, xok1 = MT > 1 && 8 + g < rows;
-    const uint16_t *xs = s_x + g * L.x_stride + 8 * t;
-    const float *cs = s_corr + 2 * t;
+    // Lanes of rows past the staged ones read the last staged row instead
+    // (their tokens' columns are never stored).
+    const uint16_t *xs = s_x + t * 8;
+    int xrow[MT];
+#pragma unroll
+    for (int o = 0; o < MT; ++o) xrow[o] = min(8 * o + g, rows_alloc - 1) * L.x_stride;
+    const float4 *cs = reinterpret_cast<const float4 *>(s_corr) + t;
+    // Per-token factors of this lane's C columns (tokens 8o + 2t + e): undo the
+    // slice shift, and for rows g + 8 (whose codes carry weight 16) also 1/16.
+    float fac[MT][2], fac16[MT][2];
+#pragma unroll
+    for (int o = 0; o < MT; ++o)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 8 * o + 2 * t + e;
+            fac[o][e] = r < rows ? pow2f(slice_shift(s_xmax[r])) : 0.f;
+            fac16[o][e] = 0.0625f * fac[o][e];
+        }
 
-    int ts = 0;
+    const uint32_t xload = g < rows;
+    uint4 xkeep[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) xkeep[q] = make_uint4(0, 0, 0, 0);
+
+    int st = 0;
     uint32_t fpar = 0;
     const unsigned char *wlane = ring + warp * kBlockBytes + lane * 16;
     for (int it = 0; it < n_my; ++it) {
-        const int base = ts * GPS;
         float acc[MT][4];
 #pragma unroll
         for (int o = 0; o < MT; ++o)
@@ -303,37 +416,50 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
 #pragma unroll
             for (int db = 0; db < D; ++db) {
                 const int gi = b0 + db;
-                const int slot = base + gi;
-                if (!mbar_wait(full0 + 8 * slot, fpar, abort_flag, err)) return;
+                const int slot = st;
+                const uint32_t par = fpar;
+                if (++st == NS) { st = 0; fpar ^= 1; }
+                if (!mbar_wait(full0 + 8 * slot, par, abort_flag, err)) return;
                 const unsigned char *wsrc = wlane + slot * kStageBytes;
                 const uint4 wa = *reinterpret_cast<const uint4 *>(wsrc);
                 const uint4 wb = *reinterpret_cast<const uint4 *>(wsrc + kChunkBytes);
                 const uint32_t wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+                // fp16 A fragments: rows g hold 1024 + code (nibble in mantissa
+                // bits 0-3), rows g + 8 hold 1024 + 16 code (bits 4-7), so one
+                // shift per word serves both halves of the upper byte pair.
                 uint32_t af[8][4];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    af[j][0] = magic_pair(wv[j]);
-                    af[j][1] = magic_pair((wv[j] >> 4));
-                    af[j][2] = magic_pair((wv[j] >> 8));
-                    af[j][3] = magic_pair((wv[j] >> 12));
+                    const uint32_t w8 = wv[j] >> 8;
+                    af[j][0] = lop3_and_or(wv[j], 0x000F000Fu, kMagicF16x2_1024);
+                    af[j][1] = lop3_and_or(wv[j], 0x00F000F0u, kMagicF16x2_1024);
+                    af[j][2] = lop3_and_or(w8, 0x000F000Fu, kMagicF16x2_1024);
+                    af[j][3] = lop3_and_or(w8, 0x00F000F0u, kMagicF16x2_1024);
                 }
                 // The stage's bytes are now in registers: release it.
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty0 + 8 * slot);
 #pragma unroll
                 for (int o = 0; o < MT; ++o) {
-                    const bool xok = o == 0 ? xok0 : xok1;
-                    const float2 cc = *reinterpret_cast<const float2 *>(cs + gi * 8 * MT + 8 * o);
-                    float c[4] = {cc.x, cc.y, cc.x, cc.y};
+                    const float4 cc = cs[(gi * MT + o) * 4];
+                    float c[4] = {cc.x, cc.y, cc.z, cc.w};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        uint4 xv = make_uint4(0, 0, 0, 0);
-                        if (xok)
-                            xv = *reinterpret_cast<const uint4 *>(xs + 8 * o * L.x_stride +
-                                                                  gi * kGroup + 32 * q);
+                        // Rows of absent tokens hold stale bytes: they reach
+                        // only those tokens' output columns, which are never
+                        // stored.  With one token octet, lanes of absent rows
+                        // skip the load and keep stale registers instead.
+                        uint4 xv;
+                        const uint16_t *xp = xs + xrow[o] + gi * kGroup + 32 * q;
+                        if constexpr (MT == 1) {
+                            lds128_if(xkeep[q], xp, xload);
+                            xv = xkeep[q];
+                        } else {
+                            xv = *reinterpret_cast<const uint4 *>(xp);
+                        }
                         float d[4];
-                        mma_16816_c(d, af[2 * q], xv.x, xv.y, c);
-                        mma_16816_c(c, af[2 * q + 1], xv.z, xv.w, d);
+                        mma_16816_f16_c(d, af[2 * q], xv.x, xv.y, c);
+                        mma_16816_f16_c(c, af[2 * q + 1], xv.z, xv.w, d);
                     }
 #pragma unroll
                     for (int r = 0; r < 4; ++r) p[db][o][r] = c[r];
@@ -352,6 +478,13 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
                     acc[o][3] = fmaf(s1, p[db][o][3], acc[o][3]);
                 }
             }
+        }
+#pragma unroll
+        for (int o = 0; o < MT; ++o) {
+            acc[o][0] *= fac[o][0];
+            acc[o][1] *= fac[o][1];
+            acc[o][2] *= fac16[o][0];
+            acc[o][3] *= fac16[o][1];
         }
         // C fragment: {row g: tokens 2t, 2t+1}, {row g+8: tokens 2t, 2t+1}.
         const int f0 = (c0 + it * C) * kTileRows + warp * 16 + g;
@@ -374,60 +507,61 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         s_cur[0] = s_next[0];
         s_cur[1] = s_next[1];
         if (it + 2 < n_my) load_scales(c0 + (it + 2) * C, s_next);
-        if (++ts == KT) { ts = 0; fpar ^= 1; }
     }
 }
 
-// Split-K reduce: each thread owns 4 consecutive outputs (one float4 per
-// slice).  Loads are issued 8 slices at a time so their latencies overlap; the
-// sum itself runs over the slices in ascending order, so the result is the
-// same whatever the unrolling.
-template <bool kVec>
+// Split-K reduce: each thread owns VEC consecutive outputs (one VEC-wide load
+// per slice).  VEC shrinks for small outputs so that enough threads run;
+// loads are issued 16 slices at a time so their latencies overlap, and the
+// sum runs over the slices in ascending order, so the result does not depend
+// on VEC or the unrolling.
+template <int VEC>
+struct FloatVec;
+template <> struct FloatVec<1> { using T = float; };
+template <> struct FloatVec<2> { using T = float2; };
+template <> struct FloatVec<4> { using T = float4; };
+
+__device__ __forceinline__ void vadd(float &a, float b) { a += b; }
+__device__ __forceinline__ void vadd(float2 &a, float2 b) { a.x += b.x; a.y += b.y; }
+__device__ __forceinline__ void vadd(float4 &a, float4 b) { a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w; }
+__device__ __forceinline__ void vstore(uint16_t *y, float a) { *y = f32_to_bf16_rn(a); }
+__device__ __forceinline__ void vstore(uint16_t *y, float2 a) {
+    *reinterpret_cast<uint32_t *>(y) = pack_bf16x2_rn(a.x, a.y);
+}
+__device__ __forceinline__ void vstore(uint16_t *y, float4 a) {
+    *reinterpret_cast<uint2 *>(y) = make_uint2(pack_bf16x2_rn(a.x, a.y), pack_bf16x2_rn(a.z, a.w));
+}
+
+template <int VEC>
 __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float *__restrict__ ws, uint16_t *__restrict__ Y, int splits,
                      long long count) {
+    using T = typename FloatVec<VEC>::T;
     pdl_launch_dependents();
     pdl_wait();
-    const long long i = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    const long long i = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * VEC;
     if (i >= count) return;
-    if (kVec) {
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        int s = 0;
-        for (; s + 8 <= splits; s += 8) {
-            float4 b[8];
+    T a;
+    for (int s = 0; s < splits; s += 16) {
+        T b[16];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                b[u] = *reinterpret_cast<const float4 *>(ws + size_t(s + u) * count + i);
+        for (int u = 0; u < 16; ++u)
+            if (s + u < splits) b[u] = *reinterpret_cast<const T *>(ws + size_t(s + u) * count + i);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (s + u == 0) { a = b[u]; continue; }
-                a.x += b[u].x; a.y += b[u].y; a.z += b[u].z; a.w += b[u].w;
-            }
-        }
-        for (; s < splits; ++s) {
-            const float4 b = *reinterpret_cast<const float4 *>(ws + size_t(s) * count + i);
-            if (s == 0) { a = b; continue; }
-            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-        }
-        uint2 o;
-        o.x = pack_bf16x2_rn(a.x, a.y);
-        o.y = pack_bf16x2_rn(a.z, a.w);
-        *reinterpret_cast<uint2 *>(Y + i) = o;
-    } else {
-        const long long end = i + 4 < count ? i + 4 : count;
-        for (long long e = i; e < end; ++e) {
-            float a = ws[e];
-            for (int s = 1; s < splits; ++s) a += ws[size_t(s) * count + e];
-            Y[e] = f32_to_bf16_rn(a);
+        for (int u = 0; u < 16; ++u) {
+            if (s + u >= splits) break;
+            if (s + u == 0) a = b[u];
+            else vadd(a, b[u]);
         }
     }
+    vstore(Y + i, a);
 }
 
 template <int MT, int GPS, bool kSplit>
 cudaError_t launch_decode_t(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
                             const uint16_t *S, uint16_t *Y, float *ws, int M, int N, int K,
                             cudaStream_t s) {
-    const int smem = decode_smem_layout(MT, GPS).total;
+    const int smem = decode_smem_layout(MT, M < 8 * MT ? M : 8 * MT, GPS).total;
     auto kern = decode_kernel<MT, GPS, kSplit>;
     if (smem > 48 * 1024) {
         // Opt in to more than 48 KB of shared memory once per device (not a
@@ -456,7 +590,8 @@ cudaError_t launch_decode_t(const DecodePlan &p, const uint16_t *X, const uint8_
     int *err = device_error_word();
     if (!err) return cudaErrorUnknown;
     const int s_vec = (reinterpret_cast<uintptr_t>(S) % (2 * GPS)) == 0;
-    return cudaLaunchKernelEx(&cfg, kern, X, Wp, S, Y, ws, M, N, K, p.n_tiles, s_vec, err);
+    return cudaLaunchKernelEx(&cfg, kern, X, Wp, S, Y, ws, M, N, K, p.n_tiles, p.ring, p.in_flight,
+                              s_vec, err);
 }
 
 template <int MT, bool kSplit>
@@ -468,6 +603,9 @@ cudaError_t launch_decode_gps(const DecodePlan &p, const uint16_t *X, const uint
         case 2: return launch_decode_t<MT, 2, kSplit>(p, X, Wp, S, Y, ws, M, N, K, s);
         case 4: return launch_decode_t<MT, 4, kSplit>(p, X, Wp, S, Y, ws, M, N, K, s);
         case 8: return launch_decode_t<MT, 8, kSplit>(p, X, Wp, S, Y, ws, M, N, K, s);
+        case 16:
+            if constexpr (MT == 1) return launch_decode_t<MT, 16, kSplit>(p, X, Wp, S, Y, ws, M, N, K, s);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
@@ -475,13 +613,13 @@ cudaError_t launch_decode_gps(const DecodePlan &p, const uint16_t *X, const uint
 }  // namespace
 
 int decode_smem_needed(int M, int mt, int groups_per_slice) {
-    (void)M;
-    return decode_smem_layout(mt, groups_per_slice).total;
+    return decode_smem_layout(mt, M < 8 * mt ? M : 8 * mt, groups_per_slice).total;
 }
 
 cudaError_t launch_decode(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, int M, int N, int K,
                           cudaStream_t s) {
+    if (p.ring < 2 || p.in_flight < 1 || p.in_flight > p.ring) return cudaErrorInvalidValue;
     if (p.groups_per_slice < 1 || p.groups_per_slice > kDecodeMaxGps || p.ctas_per_slice < 1 ||
         decode_smem_needed(M, p.mt, p.groups_per_slice) > kDecodeMaxSmem)
         return cudaErrorInvalidValue;
@@ -497,12 +635,20 @@ cudaError_t launch_decode(const DecodePlan &p, const uint16_t *X, const uint8_t 
 cudaError_t launch_reduce(const float *ws, uint16_t *Y, int splits, long long count, bool pdl,
                           cudaStream_t s) {
     if (count <= 0) return cudaSuccess;
-    const bool vec = (count % 4 == 0) && (reinterpret_cast<uintptr_t>(Y) % 8 == 0) &&
-                     (reinterpret_cast<uintptr_t>(ws) % 16 == 0);
+    // Widest VEC that keeps about two threads per SM slot of 256 busy and
+    // that the addresses allow.
+    const long long want_threads = 2LL * 152 * 256;
+    int vec = 1;
+    if (count % 4 == 0 && reinterpret_cast<uintptr_t>(Y) % 8 == 0 &&
+        reinterpret_cast<uintptr_t>(ws) % 16 == 0 && count / 4 >= want_threads)
+        vec = 4;
+    else if (count % 2 == 0 && reinterpret_cast<uintptr_t>(Y) % 4 == 0 &&
+             reinterpret_cast<uintptr_t>(ws) % 8 == 0 && count / 2 >= want_threads)
+        vec = 2;
     const int threads = 256;
-    const long long quads = (count + 3) / 4;
+    const long long items = count / vec;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned((quads + threads - 1) / threads));
+    cfg.gridDim = dim3(unsigned((items + threads - 1) / threads));
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -511,8 +657,9 @@ cudaError_t launch_reduce(const float *ws, uint16_t *Y, int splits, long long co
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (vec) return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<true>, ws, Y, splits, count);
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<false>, ws, Y, splits, count);
+    if (vec == 4) return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<4>, ws, Y, splits, count);
+    if (vec == 2) return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<2>, ws, Y, splits, count);
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<1>, ws, Y, splits, count);
 }
 
 }  // namespace w4a16

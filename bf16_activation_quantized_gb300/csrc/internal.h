@@ -14,6 +14,8 @@ struct DecodePlan {
     int ctas_per_slice;   // grid.x: CTA c of a slice takes tiles c, c + ctas_per_slice, ...
     int split_k;          // K slices (grid.y)
     int groups_per_slice; // 128-wide K groups per slice (<= kDecodeMaxGps)
+    int ring;             // weight-ring stages to use (capped by shared memory)
+    int in_flight;        // bulk copies a CTA keeps in the air (<= ring)
 };
 
 struct TensorPlan {
@@ -33,7 +35,7 @@ int *device_error_word();        // device address of the error word (nullptr on
 // Decode arm shared memory: the weight ring, the staged X slice and its
 // per-group sums.  kDecodeMaxSmem lets two CTAs share an SM (228 KB, of which
 // 1 KB per CTA is reserved).
-constexpr int kDecodeMaxGps = 8;
+constexpr int kDecodeMaxGps = 16;
 constexpr int kDecodeMaxSmem = 113 * 1024;
 int decode_smem_needed(int M, int mt, int groups_per_slice);
 

@@ -62,7 +62,8 @@ typedef struct {
     int arm;          /* w4a16_arm */
     int split_k;      /* 0 = automatic, else the requested number of K slices, clamped to
                          K/128.  The decode arm rounds it up to the nearest count whose
-                         slices hold 1, 2, 4 or 8 of the 128-wide groups each. */
+                         slices hold 1, 2, 4, 8 or (up to 8 tokens) 16 of the 128-wide
+                         groups each. */
     int tile_tokens;  /* tensor arm only: 0 = automatic, else tokens per tile (32..256, multiple of 32) */
 } w4a16_options;
 

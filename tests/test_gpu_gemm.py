@@ -111,6 +111,15 @@ def test_decode_arm_slice_sizes(M, split_k):
     assert_close(bf16_to_f64(y), reference(p), what=f"decode M{M} SK{split_k}")
 
 
+@pytest.mark.parametrize("M", [1, 3, 8, 12])
+def test_decode_arm_sixteen_group_slices(M):
+    N, K = 300, 2048       # 16 groups: one 16-group slice for up to 8 tokens, else two of 8
+    p = problem(M, N, K, seed=M + 200)
+    y = run(p, arm="decode", split_k=1)
+    assert w4.plan(M, N, K, arm="decode", split_k=1)["split_k"] == (1 if M <= 8 else 2)
+    assert_close(bf16_to_f64(y), reference(p), what=f"decode M{M} one slice")
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 19456, 2560), (16, 2560, 9728), (8, 8192, 8192)])
 @pytest.mark.parametrize("split_k", [1, 4, 16])
 def test_decode_arm_splits_on_workload_shapes(M, N, K, split_k):
@@ -193,13 +202,14 @@ def test_all_eights_and_zero_scales_give_zero():
     p = DeviceProblem(inp)
     # The tensor arm multiplies exact zeros (code - 8 = 0): exactly 0.
     assert np.all(bf16_to_f64(run(p, arm="tensor")) == 0.0)
-    # The decode arm feeds the tensor core 128 + code and removes 136 * sum(x)
-    # per 128-wide group, so zero codes cancel only up to fp32 rounding of
-    # terms of size 136 * sum|x|: bound each output by that, with margin
-    # (2^-18 relative; the observed residue is near 2^-24).
+    # The decode arm feeds the tensor core 1024 + code (or 1024 + 16 code) and
+    # removes 1032 (or 1152) times the group's sum of x, so zero codes cancel
+    # only up to fp32 rounding of terms of size 1152 * sum|x|: bound each
+    # output by that, with margin (2^-18 relative; the observed residue is
+    # near 2^-22).
     x = _bf16_bits_to_f64(inp.x).reshape(M, K // 128, 128)
     s = _bf16_bits_to_f64(inp.scales)                        # [N][K/128]
-    bound = 136.0 * np.abs(x).sum(axis=2) @ np.abs(s).T * 2.0 ** -18   # [M][N]
+    bound = 1152.0 * np.abs(x).sum(axis=2) @ np.abs(s).T * 2.0 ** -18   # [M][N]
     y = bf16_to_f64(run(p, arm="decode"))
     assert np.all(np.abs(y) <= bound)
     assert np.max(np.abs(y)) < 1e-4
