@@ -22,7 +22,8 @@ from pinned host memory and Y copied back every step, per-shape figures for
 every workload shape, and the CPU oracle's throughput on the host cores.
 
 ``--impl reference`` times the CPU oracle instead (the only reference this
-method has), on a bounded sample of every step.
+method has), on a bounded sample of every step.  ``--shape M,N,K`` times one
+GEMM shape the way the per-shape table does and prints that row only.
 """
 from __future__ import annotations
 
@@ -58,6 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-shapes", action="store_true", help="skip the per-shape table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline budget")
+    ap.add_argument("--shape", type=str, default=None, metavar="M,N,K",
+                    help="time one GEMM shape (graph of back-to-back calls) and print its row only")
     return ap.parse_args(argv)
 
 
@@ -360,13 +363,16 @@ def end_to_end(torch, w4, shapes, steps, step_bytes):
                     "back every step; packed weights stay resident"}
 
 
-def per_shape_table(torch, w4, syn, metrics, device, peaks):
+def per_shape_table(torch, w4, syn, metrics, device, peaks, only=None):
     shapes = [("tiny", 4, 256, 512)]
     for name, lst in (("decode_gemv", syn.WORKLOADS["decode_gemv"]),
                       ("decode_sweep_gate_up", syn.WORKLOADS["decode_sweep_gate_up"]),
                       ("decode_sweep_down", syn.WORKLOADS["decode_sweep_down"]),
                       ("prefill", syn.WORKLOADS["prefill"])):
         shapes += [(name, M, N, K) for (M, N, K) in lst]
+    if only is not None:
+        named = [sh for sh in shapes if sh[1:] == tuple(only)]
+        shapes = named[:1] or [("custom",) + tuple(only)]
     rows = []
     for name, M, N, K in shapes:
         wb = metrics.weight_bytes(N, K)
@@ -464,6 +470,21 @@ def main(argv=None):
         if rank != 0:
             return 0
         print(json.dumps(reference_arm(args, world, rank)), flush=True)
+        return 0
+    if args.shape:
+        import torch
+        import bf16_activation_quantized_gb300 as w4
+        from bf16_activation_quantized_gb300 import build as build_mod
+        from bf16_activation_quantized_gb300 import metrics
+        from bf16_activation_quantized_gb300 import synthetic as syn
+        build_mod.build()
+        device = torch.device("cuda", local)
+        torch.cuda.set_device(device)
+        peaks, _ = load_peaks()
+        only = [int(v) for v in args.shape.split(",")]
+        if rank == 0:
+            print(json.dumps(per_shape_table(torch, w4, syn, metrics, device, peaks, only)[0]),
+                  flush=True)
         return 0
     dist = maybe_init_dist(world, local)
     out = our_arm(args, world, rank, local, dist)

@@ -156,8 +156,8 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, DecodePlan *d) 
 // its tile count times (K blocks x that + a fixed per-tile cost), plus the
 // split-K round trip.
 int tensor_stages(int bt, int num_groups, int occupancy) {
-    const size_t budget = size_t(kTensorMaxSmem) / size_t(occupancy);
-    const size_t fixed = tensor_smem_bytes(bt, 0, num_groups);
+    const size_t budget = size_t(tensor_smem_budget(occupancy));
+    const size_t fixed = tensor_smem_bytes(bt, 0, occupancy, num_groups);
     const size_t stage = 2 * size_t(bt) * 128 + 2 * kChunkBytes;   // one 128-column group
     if (budget <= fixed) return 0;
     size_t n = (budget - fixed) / stage;
@@ -179,8 +179,8 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
     int found = 0;
     for (int bt = 32; bt <= 256; bt += 32) {
         if (forced_bt > 0 && bt != forced_bt) continue;
-        const int occ_max = tensor_tmem_cols(bt) <= 256 ? 2 : 1;
-        for (int occ = 1; occ <= occ_max; ++occ) {
+        for (int occ = 1; occ <= 2; ++occ) {
+            if (tensor_a_stages(bt, occ) < 2) continue;       // TMEM share too small
             const int stages = tensor_stages(bt, num_groups, occ);
             if (stages < 2) continue;
             const int max_sk = num_groups > 1 ? 1 : (groups < 16 ? groups : 16);
@@ -212,7 +212,8 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                     t->t_tiles = int(t_tiles);
                     t->ctas = int(ctas);
                     t->stages = stages;
-                    t->smem_bytes = tensor_smem_bytes(bt, stages, num_groups);
+                    t->occupancy = occ;
+                    t->smem_bytes = tensor_smem_bytes(bt, stages, occ, num_groups);
                     found = 1;
                 }
                 if (forced_split > 0 || num_groups > 1) break;
@@ -406,7 +407,8 @@ w4a16_status w4a16_gemm_grouped(const w4a16_bf16 *X, const uint8_t *W_packed,
     // Enough CTAs for any split of M_total into the groups: the tile count is
     // at most n_tiles * (ceil(M_total / bt) + num_groups).
     const long long bound = (long long)t.n_tiles * (ceil_div(M_total, t.tile_tokens) + num_groups);
-    t.ctas = int(bound < sms ? bound : sms);
+    const long long slots = (long long)t.occupancy * sms;
+    t.ctas = int(bound < slots ? bound : slots);
     cudaError_t e = launch_tensor(t, X, W_packed, scales, Y, nullptr, M_sizes_dev,
                                   static_cast<int *>(workspace), num_groups, M_total, N, K,
                                   static_cast<cudaStream_t>(stream));

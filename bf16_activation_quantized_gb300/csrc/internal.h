@@ -26,6 +26,7 @@ struct TensorPlan {
     int t_tiles;          // token tiles (per group for the grouped op: an upper bound)
     int ctas;             // persistent CTAs launched
     int stages;           // shared-memory ring depth
+    int occupancy;        // CTAs per SM the resources are sized for (1 or 2)
     size_t smem_bytes;
 };
 
@@ -48,10 +49,18 @@ cudaError_t launch_decode(const DecodePlan &p, const uint16_t *X, const uint8_t 
                           const uint16_t *S, uint16_t *Y, float *ws, int M, int N, int K,
                           cudaStream_t s);
 // Tensor arm (tensor.cu).
-constexpr int kTensorMaxSmem = 227 * 1024;
+constexpr int kTensorMaxSmem = 227 * 1024;     // per-CTA opt-in maximum
+constexpr int kSmemPerSm = 228 * 1024;         // shared memory of one SM
+constexpr int kSmemReservedPerCta = 1024;      // the runtime's share of each resident CTA
 constexpr int kMaxGroups = 1024;
-size_t tensor_smem_bytes(int bt, int stages, int num_groups);
-int tensor_tmem_cols(int bt);     // TMEM columns a CTA allocates for tiles of bt tokens
+// Dynamic shared memory a CTA may use when `occupancy` CTAs share an SM.
+inline int tensor_smem_budget(int occupancy) {
+    const int b = kSmemPerSm / occupancy - kSmemReservedPerCta;
+    return b < kTensorMaxSmem ? b : kTensorMaxSmem;
+}
+size_t tensor_smem_bytes(int bt, int stages, int occupancy, int num_groups);
+int tensor_a_stages(int bt, int occupancy);   // TMEM A ring depth (0: does not fit)
+int tensor_tmem_cols(int bt, int occupancy);  // TMEM columns a CTA allocates
 cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, const int32_t *m_sizes,
                           int *status, int num_groups, int M_total, int N, int K, cudaStream_t s);

@@ -467,26 +467,33 @@ EncodeTiledFn encode_tiled() {
 
 }  // namespace
 
-// A ring depth: four group stages when a CTA has the TMEM to itself, two when
-// the tile is small enough for two CTAs to share an SM's 512 columns.
-int tensor_a_stages(int bt) { return bt <= 128 ? 2 : 4; }
+// A ring depth: as many 64-column group stages (at most four) as fit next to
+// the bt accumulator columns in the CTA's share of the SM's 512 TMEM columns
+// (all of them with one CTA per SM, half with two); 0 if none fits.
+int tensor_a_stages(int bt, int occupancy) {
+    const int share = 512 / occupancy;
+    int sa = (share - bt) / 64;
+    return sa > 4 ? 4 : (sa < 0 ? 0 : sa);
+}
 
-int tensor_tmem_cols(int bt) {
-    const int need = bt + 64 * tensor_a_stages(bt);
+int tensor_tmem_cols(int bt, int occupancy) {
+    const int need = bt + 64 * tensor_a_stages(bt, occupancy);
     int cols = 32;
     while (cols < need) cols <<= 1;
     return cols;
 }
 
-size_t tensor_smem_bytes(int bt, int stages, int num_groups) {
-    return size_t(tc_smem_layout(bt, stages, tensor_a_stages(bt), num_groups).total) + 1024;  // + alignment slack
+size_t tensor_smem_bytes(int bt, int stages, int occupancy, int num_groups) {
+    return size_t(tc_smem_layout(bt, stages, tensor_a_stages(bt, occupancy), num_groups).total) +
+           1024;  // + alignment slack
 }
 
 cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, const int32_t *m_sizes,
                           int *status, int num_groups, int M_total, int N, int K, cudaStream_t s) {
     if (p.tile_tokens < 32 || p.tile_tokens > 256 || p.tile_tokens % 32 || p.stages < 2 ||
-        p.ctas < 1 || num_groups < 1 || num_groups > kMaxGroups)
+        p.ctas < 1 || num_groups < 1 || num_groups > kMaxGroups || p.occupancy < 1 ||
+        p.occupancy > 2 || tensor_a_stages(p.tile_tokens, p.occupancy) < 2)
         return cudaErrorInvalidValue;
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return cudaErrorNotSupported;
@@ -519,8 +526,8 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
     a.split_k = p.split_k;
     a.gps = p.groups_per_slice;
     a.stages = p.stages;
-    a.a_stages = tensor_a_stages(p.tile_tokens);
-    a.tmem_cols = tensor_tmem_cols(p.tile_tokens);
+    a.a_stages = tensor_a_stages(p.tile_tokens, p.occupancy);
+    a.tmem_cols = tensor_tmem_cols(p.tile_tokens, p.occupancy);
     a.vec_store = (N % 8 == 0) && (reinterpret_cast<uintptr_t>(Y) % 16 == 0);
     a.w_group_stride = packed_bytes(N, K);
     a.s_group_stride = (unsigned long long)N * (K / kGroup);
@@ -537,8 +544,8 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
         if (e != cudaSuccess) return e;
         opted[split].fetch_or(bit, std::memory_order_acq_rel);
     }
-    const size_t smem = tensor_smem_bytes(p.tile_tokens, p.stages, num_groups);
-    if (smem > size_t(kTensorMaxSmem)) return cudaErrorInvalidValue;
+    const size_t smem = tensor_smem_bytes(p.tile_tokens, p.stages, p.occupancy, num_groups);
+    if (smem > size_t(tensor_smem_budget(p.occupancy))) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.ctas);
     cfg.blockDim = dim3(kTcThreads);
