@@ -327,11 +327,19 @@ def our_arm(args, world, rank, local, dist):
 
 
 def load_traffic():
-    """DRAM bytes per step of the decode kernel from the committed ncu summary, if current."""
+    """DRAM bytes per step of the decode kernel from the committed ncu summary,
+    or None when the kernel's sources changed after that capture."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
+        h = hashlib.sha256()
+        for src in d["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != d["sources_sha256"]:
+            return None
         return d.get("decode_gemv_bytes_per_step")
     except Exception:
         return None
