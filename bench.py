@@ -60,7 +60,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline budget")
     ap.add_argument("--shape", type=str, default=None, metavar="M,N,K",
-                    help="time one GEMM shape (graph of back-to-back calls) and print its row only")
+                    help="time one GEMM shape (graph of back-to-back calls) and print its row "
+                         "only; 'grouped' times the grouped workload")
     return ap.parse_args(argv)
 
 
@@ -379,6 +380,8 @@ def per_shape_table(torch, w4, syn, metrics, device, peaks, only=None):
                       ("prefill", syn.WORKLOADS["prefill"])):
         shapes += [(name, M, N, K) for (M, N, K) in lst]
     if only is not None:
+        if len(only) == 4:    # G, M_total, N, K: the grouped workload
+            return [grouped_row(torch, w4, syn, metrics, device, peaks)]
         named = [sh for sh in shapes if sh[1:] == tuple(only)]
         shapes = named[:1] or [("custom",) + tuple(only)]
     rows = []
@@ -400,7 +403,39 @@ def per_shape_table(torch, w4, syn, metrics, device, peaks, only=None):
                      "arm": s.plan["arm"], "split_k": s.plan["split_k"], "copies": C})
         del g, s
         torch.cuda.empty_cache()
+    if only is None:
+        rows.append(grouped_row(torch, w4, syn, metrics, device, peaks))
     return rows
+
+
+def grouped_row(torch, w4, syn, metrics, device, peaks):
+    """The grouped workload: one launch over all groups, sizes read on the device."""
+    G, MT, N, K = (syn.GROUPED_WORKLOAD[k] for k in ("num_groups", "M_total", "N", "K"))
+    inp = syn.make_grouped_inputs(G, MT, N, K, seed=0)
+    bits = lambda a: torch.from_numpy(a.view("int16").copy()).view(torch.bfloat16).to(device)
+    x = bits(inp.x)
+    s = bits(inp.scales)
+    w = torch.stack([w4.pack(torch.from_numpy(inp.w_canon[g].copy()).to(device)) for g in range(G)])
+    sizes = torch.from_numpy(inp.m_sizes.copy()).to(device)
+    y = torch.empty((MT, N), dtype=torch.bfloat16, device=device)
+    _, st = w4.gemm_grouped(x, w, s, sizes, out=y)      # sizes the status word once
+    torch.cuda.synchronize()
+    C = copies_for(torch, device, G * metrics.weight_bytes(N, K))
+    ws = [w] + [w.clone() for _ in range(C - 1)]
+    R = max(C, (40 // C) * C)
+    g = capture(torch, lambda i: w4.gemm_grouped(x, ws[i % C], s, sizes, out=y, status=st), R)
+    g.replay()
+    t = statistics.median(time_graph(torch, g) for _ in range(5)) / R
+    nbytes = metrics.grouped_algorithmic_bytes(G, MT, N, K)
+    fl = metrics.flops(MT, N, K)
+    t_roof = metrics.roofline_seconds(fl, nbytes, peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
+    row = {"workload": "grouped", "M": MT, "N": N, "K": K, "groups": G,
+           "us": round(t * 1e6, 3), "tflops": round(fl / t / 1e12, 3), "gbs": round(nbytes / t / 1e9, 1),
+           "roofline_frac": round(t_roof / t, 4), "bound": "tensor", "arm": "tensor (grouped)",
+           "split_k": 1, "copies": C}
+    del g, ws
+    torch.cuda.empty_cache()
+    return row
 
 
 # ----------------------------------------------------------- CPU baseline
@@ -489,7 +524,8 @@ def main(argv=None):
         device = torch.device("cuda", local)
         torch.cuda.set_device(device)
         peaks, _ = load_peaks()
-        only = [int(v) for v in args.shape.split(",")]
+        only = ([0, 0, 0, 0] if args.shape == "grouped" else
+                [int(v) for v in args.shape.split(",")])
         if rank == 0:
             print(json.dumps(per_shape_table(torch, w4, syn, metrics, device, peaks, only)[0]),
                   flush=True)

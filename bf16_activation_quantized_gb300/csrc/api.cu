@@ -53,7 +53,7 @@ constexpr double kReduceSeconds = 0.5e-6;
 constexpr double kReducePerSliceSeconds = 0.01e-6;  // reduce latency per extra slice
 constexpr int kDecodeMaxM = 16;               // auto dispatch: M <= 16 -> decode arm
 constexpr double kClockHz = 1.9e9;            // planning clock
-constexpr int kTensorMaxStages = 8;
+constexpr int kTensorMaxWStages = 8;
 constexpr double kTcChainClk = 500.0;         // one CTA's per-K-block dependency chain
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -155,14 +155,28 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, DecodePlan *d) 
 // one SM's HBM share + activation bytes at one SM's L2 share); a CTA's time is
 // its tile count times (K blocks x that + a fixed per-tile cost), plus the
 // split-K round trip.
-int tensor_stages(int bt, int num_groups, int occupancy) {
+// Ring depths for the CTA's shared-memory budget: the deepest X ring of 4, 3
+// or 2 stages that still leaves at least 3 W stages, then as many W stages
+// (8 KB each, up to kTensorMaxWStages) as fit.  Returns false if even 2 + 2
+// does not fit.
+bool tensor_rings(int bt, int num_groups, int occupancy, int *x_stages, int *w_stages) {
     const size_t budget = size_t(tensor_smem_budget(occupancy));
-    const size_t fixed = tensor_smem_bytes(bt, 0, occupancy, num_groups);
-    const size_t stage = 2 * size_t(bt) * 128 + 2 * kChunkBytes;   // one 128-column group
-    if (budget <= fixed) return 0;
-    size_t n = (budget - fixed) / stage;
-    if (n > size_t(kTensorMaxStages)) n = kTensorMaxStages;
-    return int(n);
+    const size_t fixed = tensor_smem_bytes(bt, 0, 0, occupancy, num_groups);
+    if (budget <= fixed) return false;
+    const size_t avail = budget - fixed;
+    const size_t x_stage = 2 * size_t(bt) * 128 + 16;     // + its two barriers
+    const size_t w_stage = size_t(kChunkBytes) * 2 + 16;
+    for (int sx = 4; sx >= 2; --sx) {
+        if (sx * x_stage > avail) continue;
+        size_t sw = (avail - sx * x_stage) / w_stage;
+        if (sw > size_t(kTensorMaxWStages)) sw = kTensorMaxWStages;
+        if (sw >= 3 || (sx == 2 && sw >= 2)) {
+            *x_stages = sx;
+            *w_stages = int(sw);
+            return true;
+        }
+    }
+    return false;
 }
 
 // Tensor-arm tiles: 128 weight rows x bt tokens, K split into sk slices, one
@@ -181,8 +195,8 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
         if (forced_bt > 0 && bt != forced_bt) continue;
         for (int occ = 1; occ <= 2; ++occ) {
             if (tensor_a_stages(bt, occ) < 2) continue;       // TMEM share too small
-            const int stages = tensor_stages(bt, num_groups, occ);
-            if (stages < 2) continue;
+            int sx = 0, sw = 0;
+            if (!tensor_rings(bt, num_groups, occ, &sx, &sw)) continue;
             const int max_sk = num_groups > 1 ? 1 : (groups < 16 ? groups : 16);
             for (int sk_req = 1; sk_req <= max_sk; ++sk_req) {
                 int sk = sk_req;
@@ -211,9 +225,10 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                     t->groups_per_slice = gps;
                     t->t_tiles = int(t_tiles);
                     t->ctas = int(ctas);
-                    t->stages = stages;
+                    t->x_stages = sx;
+                    t->w_stages = sw;
                     t->occupancy = occ;
-                    t->smem_bytes = tensor_smem_bytes(bt, stages, occ, num_groups);
+                    t->smem_bytes = tensor_smem_bytes(bt, sx, sw, occ, num_groups);
                     found = 1;
                 }
                 if (forced_split > 0 || num_groups > 1) break;

@@ -60,6 +60,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test: true if the phase with the given parity has completed.
+// (try_wait may suspend the thread for a while when the phase is incomplete;
+// a thread that polls several barriers must not be held on one of them.)
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // As mbar_try_wait, but the thread may sleep in the instruction (up to
 // kSuspendHintNs) until the phase completes, instead of spinning.
 constexpr uint32_t kSuspendHintNs = 1000000;
@@ -99,6 +113,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
             "r"(dst),
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// Warm L2 with `bytes` of global memory (bytes % 16 == 0, 16-byte aligned);
+// nothing is written anywhere, so it is safe before a dependency wait (L2 is
+// coherent: a later write by another kernel replaces the prefetched lines).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // 2-D tiled TMA load: box at (x = innermost element index, y = row) -> shared.

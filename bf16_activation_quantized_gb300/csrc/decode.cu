@@ -225,8 +225,20 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         for (int r = 0; r < 16; ++r) s_xmax[r] = 0;
         fence_barrier_init();
     }
+    if (warp == kDecodeWarps && lane == 0 && n_my > 0) {
+        // While the previous grid finishes, pull this CTA's first weight
+        // stages into L2 (a prefetch reads nothing into the CTA and writes
+        // nothing, so it needs no dependency wait); the copies after the wait
+        // then hit L2.
+        const uint8_t *src = Wp + (size_t(c0) * KC + size_t(2 * grp0)) * kChunkBytes;
+        const size_t tile_step = size_t(C) * KC * kChunkBytes;
+        const int first = min(n_my * GPS, NS);
+        for (int q = 0; q < first; ++q)
+            bulk_prefetch_l2(src + (q / GPS) * tile_step + (q % GPS) * kStageBytes, kStageBytes);
+    }
     __syncthreads();
-    // Touch no global memory before the previous grid in the stream has completed.
+    // Read no global memory into the CTA before the previous grid in the
+    // stream has completed (it may have written X, W or the scales).
     pdl_wait();
 
     const int g = lane >> 2, t = lane & 3;

@@ -25,7 +25,8 @@ struct TensorPlan {
     int n_tiles;          // 128-row feature tiles
     int t_tiles;          // token tiles (per group for the grouped op: an upper bound)
     int ctas;             // persistent CTAs launched
-    int stages;           // shared-memory ring depth
+    int x_stages;         // X ring depth (groups of X in shared memory)
+    int w_stages;         // W ring depth (groups of packed weights in shared memory)
     int occupancy;        // CTAs per SM the resources are sized for (1 or 2)
     size_t smem_bytes;
 };
@@ -58,7 +59,7 @@ inline int tensor_smem_budget(int occupancy) {
     const int b = kSmemPerSm / occupancy - kSmemReservedPerCta;
     return b < kTensorMaxSmem ? b : kTensorMaxSmem;
 }
-size_t tensor_smem_bytes(int bt, int stages, int occupancy, int num_groups);
+size_t tensor_smem_bytes(int bt, int x_stages, int w_stages, int occupancy, int num_groups);
 int tensor_a_stages(int bt, int occupancy);   // TMEM A ring depth (0: does not fit)
 int tensor_tmem_cols(int bt, int occupancy);  // TMEM columns a CTA allocates
 cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t *Wp,

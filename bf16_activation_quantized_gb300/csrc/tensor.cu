@@ -3,9 +3,13 @@
 // serves the plain product (optionally split along K) and the grouped product.
 //
 // Roles in a CTA (320 threads):
-//   warp 8      producer: per K block (64 columns) one TMA 2-D load of the X
-//               tile [tokens x 64] (128-byte swizzle) and one 4 KB bulk copy of
-//               the packed weight chunk, both completing on full[stage].
+//   warp 8      producer: per 128-wide group two TMA 2-D loads of the X tile
+//               [tokens x 64] (128-byte swizzle) into the X ring and one 8 KB
+//               bulk copy of the packed weights into the W ring.  The rings are
+//               separate: the W ring is released by the dequantisers as soon as
+//               they have read it and can run many groups ahead of the MMA
+//               (HBM latency), the X ring is released by the MMA commit.  One
+//               thread polls both rings and issues whichever has room.
 //   warp 9      TMEM owner and MMA issuer: four tcgen05.mma (K = 16 each) per
 //               K block, A = weights from TMEM, B = X from shared memory,
 //               D = fp32 in TMEM; tcgen05.commit releases the stages.
@@ -59,7 +63,8 @@ struct TcArgs {
     int bt;                   // tokens per tile = MMA N (multiple of 32, <= 256)
     int n_tiles;              // 128-row weight tiles
     int split_k, gps;         // K slices and 128-wide groups per slice
-    int stages;               // shared-memory ring depth (one 128-column group per stage)
+    int x_stages;             // X ring depth (one 128-column group of X per stage)
+    int w_stages;             // W ring depth (8 KB of packed weights per stage)
     int a_stages;             // TMEM A ring depth (one group = 64 columns per stage)
     int tmem_cols;            // TMEM columns allocated (power of two >= bt + 64 * a_stages)
     int vec_store;            // Y rows are 16-byte aligned: stage the epilogue for 16-byte stores
@@ -67,8 +72,9 @@ struct TcArgs {
     unsigned long long s_group_stride;  // elements between groups' scales
 };
 
-// Shared memory per stage: two X boxes (one per 64-column K block, 1024-byte
-// aligned, 128-byte swizzle) and the 8 KB of packed weights of the group.
+// Shared memory: the X ring (per stage two X boxes, one per 64-column K block,
+// 1024-byte aligned, 128-byte swizzle), the W ring (8 KB of packed weights of a
+// group per stage), the epilogue staging, the barriers and the group tables.
 struct TcSmem {
     int x_stage, off_x, off_w, off_epi, off_bar, off_misc, off_tab, total;
 };
@@ -76,14 +82,15 @@ struct TcSmem {
 constexpr int kGroupBytes = 2 * kChunkBytes;           // packed weights of one 128-column group
 constexpr int kEpiBytesPerWarp = 32 * 32 * 2;          // 32 tokens x 32 rows of bf16
 
-__host__ __device__ inline TcSmem tc_smem_layout(int bt, int stages, int a_stages, int num_groups) {
+__host__ __device__ inline TcSmem tc_smem_layout(int bt, int x_stages, int w_stages, int a_stages,
+                                                 int num_groups) {
     TcSmem L;
     L.x_stage = 2 * bt * 128;
     L.off_x = 0;
-    L.off_w = L.off_x + stages * L.x_stage;
-    L.off_epi = L.off_w + stages * kGroupBytes;
+    L.off_w = L.off_x + x_stages * L.x_stage;
+    L.off_epi = L.off_w + w_stages * kGroupBytes;
     L.off_bar = L.off_epi + kTcDequantWarps * kEpiBytesPerWarp;
-    L.off_misc = L.off_bar + (2 * stages + 2 * a_stages + 3) * 8;
+    L.off_misc = L.off_bar + (2 * x_stages + 2 * w_stages + 2 * a_stages + 3) * 8;
     L.off_tab = (L.off_misc + 16 + 15) & ~15;           // group tables: 2 x (G + 1) ints
     L.total = L.off_tab + 2 * (num_groups + 1) * 4;
     return L;
@@ -129,12 +136,18 @@ __device__ __forceinline__ bool tc_tile(const TcArgs &a, const int *tab_tiles, c
     return true;
 }
 
-__device__ __forceinline__ uint32_t scale_pair(const uint16_t *S, int row, int N, size_t idx) {
-    if (row >= N) return 0u;
-    unsigned short v;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(S + idx));
-    return uint32_t(v) | (uint32_t(v) << 16);
+// A group scale, loaded raw (bits in the low half, 0 past the last row).  The
+// bf16x2 pair is formed only where it is used (scale_pair2), so a load issued a
+// group ahead is not waited for by an instruction right behind it.
+__device__ __forceinline__ uint32_t scale_raw(const uint16_t *S, int row, int N, size_t idx) {
+    uint32_t v = 0;
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.lt.s32 p, %1, %2;\n\t"
+                 "@p ld.global.nc.u16 %0, [%3];\n\t}"
+                 : "+r"(v)
+                 : "r"(row), "r"(N), "l"(S + idx));
+    return v;
 }
+__device__ __forceinline__ uint32_t scale_pair2(uint32_t raw) { return raw | (raw << 16); }
 
 __device__ __forceinline__ void drain_wait_tc(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = global_timer_ns();
@@ -161,17 +174,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled X tiles (the host adds the slack).
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    const TcSmem L = tc_smem_layout(a.bt, a.stages, a.a_stages, a.num_groups);
+    const TcSmem L = tc_smem_layout(a.bt, a.x_stages, a.w_stages, a.a_stages, a.num_groups);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int S = a.stages;
+    const int SX = a.x_stages;
+    const int SW = a.w_stages;
     const int SA = a.a_stages;
     const uint32_t bar0 = smem_u32(smem + L.off_bar);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
-    auto afull_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
-    auto aempty_bar = [&](int s) { return bar0 + 8u * (2 * S + SA + s); };
-    const uint32_t dfull_bar = bar0 + 8u * (2 * S + 2 * SA);
+    auto xfull_bar = [&](int s) { return bar0 + 8u * s; };
+    auto xempty_bar = [&](int s) { return bar0 + 8u * (SX + s); };
+    auto wfull_bar = [&](int s) { return bar0 + 8u * (2 * SX + s); };
+    auto wempty_bar = [&](int s) { return bar0 + 8u * (2 * SX + SW + s); };
+    auto afull_bar = [&](int s) { return bar0 + 8u * (2 * SX + 2 * SW + s); };
+    auto aempty_bar = [&](int s) { return bar0 + 8u * (2 * SX + 2 * SW + SA + s); };
+    const uint32_t dfull_bar = bar0 + 8u * (2 * SX + 2 * SW + 2 * SA);
     const uint32_t dempty_bar = dfull_bar + 8;
     const uint32_t done_bar = dfull_bar + 16;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
@@ -180,12 +196,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     int *tab_rows = tab_tiles + a.num_groups + 1;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), 1);
-            // Released by the MMA commit alone: the MMA of a stage starts only
-            // after every dequantiser has read its weights (they signal the A
-            // stage only after that), so the commit covers both readers.
-            mbar_init(empty_bar(s), 1);
+        for (int s = 0; s < SX; ++s) {
+            mbar_init(xfull_bar(s), 1);
+            mbar_init(xempty_bar(s), 1);                  // the MMA commit
+        }
+        for (int s = 0; s < SW; ++s) {
+            mbar_init(wfull_bar(s), 1);
+            mbar_init(wempty_bar(s), kTcDequantWarps);    // every dequantiser has read it
         }
         for (int s = 0; s < SA; ++s) {
             mbar_init(afull_bar(s), kTcDequantWarps);
@@ -233,33 +250,68 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
 
     if (warp == kTcProducerWarp) {
         if (lane == 0) {
-            int st = 0, q = 0;            // q: stage uses so far
-            TileInfo ti;
-            for (int id = blockIdx.x; tc_tile(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
-                const int g0 = ti.slice * a.gps;
-                const int g1 = min(n_groups, (ti.slice + 1) * a.gps);
-                const uint8_t *wg = a.Wp + (unsigned long long)ti.group * a.w_group_stride;
-                for (int grp = g0; grp < g1; ++grp) {
-                    if (q >= S && !mbar_wait(empty_bar(st), ((q / S) - 1) & 1, abort_flag, a.err))
-                        goto producer_done;
-                    const uint32_t xs = smem_u32(smem + L.off_x + st * L.x_stage);
-                    mbar_arrive_expect_tx(full_bar(st), 2 * x_bytes + kGroupBytes);
-                    tma_load_2d(xs, &tmap_x, grp * kGroup, ti.x_row0, full_bar(st));
-                    tma_load_2d(xs + x_bytes, &tmap_x, grp * kGroup + kChunkK, ti.x_row0, full_bar(st));
-                    bulk_g2s(smem_u32(smem + L.off_w + st * kGroupBytes),
-                             wg + ((size_t)ti.ft * KC + 2 * grp) * kChunkBytes, kGroupBytes, full_bar(st));
-                    ++q;
-                    st = (st + 1 == S) ? 0 : st + 1;
+            // Two cursors over the same (tile, group) sequence, one per ring.
+            // Each step issues at most one copy per ring; a stalled ring does
+            // not hold back the other.  The wait is bounded: no progress on
+            // either ring for kWaitLimitNs aborts the CTA.
+            TileInfo tx, tw;
+            int idx = blockIdx.x, idw = blockIdx.x;
+            bool x_more = tc_tile(a, tab_tiles, tab_rows, idx, tx);
+            bool w_more = tc_tile(a, tab_tiles, tab_rows, idw, tw);
+            int gx = x_more ? tx.slice * a.gps : 0, gw = w_more ? tw.slice * a.gps : 0;
+            int xq = 0, wq = 0, xs = 0, ws = 0;
+            uint32_t xpar = 1, wpar = 1;     // parity of the empty phase to wait for (first lap: none)
+            unsigned long long t_progress = global_timer_ns();
+            while (x_more || w_more) {
+                bool progressed = false;
+                if (x_more && (xq < SX || mbar_test_wait(xempty_bar(xs), xpar))) {
+                    const uint32_t xdst = smem_u32(smem + L.off_x + xs * L.x_stage);
+                    mbar_arrive_expect_tx(xfull_bar(xs), 2 * x_bytes);
+                    tma_load_2d(xdst, &tmap_x, gx * kGroup, tx.x_row0, xfull_bar(xs));
+                    tma_load_2d(xdst + x_bytes, &tmap_x, gx * kGroup + kChunkK, tx.x_row0, xfull_bar(xs));
+                    ++xq;
+                    if (++xs == SX) { xs = 0; xpar ^= 1; }
+                    if (++gx == min(n_groups, (tx.slice + 1) * a.gps)) {
+                        idx += gridDim.x;
+                        x_more = tc_tile(a, tab_tiles, tab_rows, idx, tx);
+                        if (x_more) gx = tx.slice * a.gps;
+                    }
+                    progressed = true;
+                }
+                if (w_more && (wq < SW || mbar_test_wait(wempty_bar(ws), wpar))) {
+                    const uint8_t *wg = a.Wp + (unsigned long long)tw.group * a.w_group_stride;
+                    mbar_arrive_expect_tx(wfull_bar(ws), kGroupBytes);
+                    bulk_g2s(smem_u32(smem + L.off_w + ws * kGroupBytes),
+                             wg + ((size_t)tw.ft * KC + 2 * gw) * kChunkBytes, kGroupBytes, wfull_bar(ws));
+                    ++wq;
+                    if (++ws == SW) { ws = 0; wpar ^= 1; }
+                    if (++gw == min(n_groups, (tw.slice + 1) * a.gps)) {
+                        idw += gridDim.x;
+                        w_more = tc_tile(a, tab_tiles, tab_rows, idw, tw);
+                        if (w_more) gw = tw.slice * a.gps;
+                    }
+                    progressed = true;
+                }
+                if (progressed) {
+                    t_progress = global_timer_ns();
+                } else {
+                    if (*abort_flag) break;
+                    if (global_timer_ns() - t_progress > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        atomicOr(a.err, kErrWaitTimeout);
+                        break;
+                    }
                 }
             }
-        producer_done:
             if (*abort_flag) {
-                for (int u = q > S ? q - S : 0; u < q; ++u) drain_wait_tc(full_bar(u % S), (u / S) & 1);
+                for (int u = xq > SX ? xq - SX : 0; u < xq; ++u) drain_wait_tc(xfull_bar(u % SX), (u / SX) & 1);
+                for (int u = wq > SW ? wq - SW : 0; u < wq; ++u) drain_wait_tc(wfull_bar(u % SW), (u / SW) & 1);
             }
         }
     } else if (warp == kTcMmaWarp) {
         if (lane == 0) {
             int st = 0, q = 0, sa = 0, qa = 0, tiles = 0;
+            const int S = SX;
             TileInfo ti;
             for (int id = blockIdx.x; tc_tile(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
                 if (tiles > 0 && !mbar_wait(dempty_bar, (tiles - 1) & 1, abort_flag, a.err)) break;
@@ -268,7 +320,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 const int g1 = min(n_groups, (ti.slice + 1) * a.gps);
                 bool ok = true;
                 for (int grp = g0; grp < g1; ++grp) {
-                    if (!mbar_wait(full_bar(st), (q / S) & 1, abort_flag, a.err) ||
+                    if (!mbar_wait(xfull_bar(st), (q / S) & 1, abort_flag, a.err) ||
                         !mbar_wait(afull_bar(sa), (qa / SA) & 1, abort_flag, a.err)) {
                         ok = false;
                         break;
@@ -284,7 +336,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                             tc_mma_ts(tmem_base + kTcDCol, acol + 32u * h + 8u * j, bdesc + 2u * j,
                                       idesc, (grp > g0 || h > 0 || j > 0) ? 1u : 0u);
                     }
-                    tc_commit(empty_bar(st));
+                    tc_commit(xempty_bar(st));
                     tc_commit(aempty_bar(sa));
                     ++q;
                     st = (st + 1 == S) ? 0 : st + 1;
@@ -308,6 +360,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         const uint32_t lane_base = uint32_t(32 * sub + 16 * half) << 16;
         unsigned char *epi = smem + L.off_epi + warp * kEpiBytesPerWarp;
         int st = 0, q = 0, sa = 0, qa = 0, tiles = 0;
+        const int S = SW;
         // Scales of the next group (possibly in the next tile), loaded one group
         // ahead so the dequantisers never wait on them.
         uint32_t n0 = 0, n1 = 0;
@@ -335,32 +388,37 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             const uint16_t *sg = a.S + (unsigned long long)ti.group * a.s_group_stride;
             bool ok = true;
             for (int grp = g0; grp < g1; ++grp) {
-                uint32_t s0, s1;
+                uint32_t s0, s1;                    // raw; paired after the stage wait
                 if (have_next) {
                     s0 = n0;
                     s1 = n1;
                 } else {
-                    s0 = scale_pair(sg, r0, a.N, size_t(r0) * n_groups + grp);
-                    s1 = scale_pair(sg, r0 + 8, a.N, size_t(r0 + 8) * n_groups + grp);
+                    s0 = scale_raw(sg, r0, a.N, size_t(r0) * n_groups + grp);
+                    s1 = scale_raw(sg, r0 + 8, a.N, size_t(r0 + 8) * n_groups + grp);
                 }
                 have_next = false;
                 if (grp + 1 < g1) {
-                    n0 = scale_pair(sg, r0, a.N, size_t(r0) * n_groups + grp + 1);
-                    n1 = scale_pair(sg, r0 + 8, a.N, size_t(r0 + 8) * n_groups + grp + 1);
+                    n0 = scale_raw(sg, r0, a.N, size_t(r0) * n_groups + grp + 1);
+                    n1 = scale_raw(sg, r0 + 8, a.N, size_t(r0 + 8) * n_groups + grp + 1);
                     have_next = true;
                 } else if (nx_ok) {
                     const int rn = nx.ft * kTileRows + 16 * block + g;
                     const int gn = nx.slice * a.gps;
                     const uint16_t *sn = a.S + (unsigned long long)nx.group * a.s_group_stride;
-                    n0 = scale_pair(sn, rn, a.N, size_t(rn) * n_groups + gn);
-                    n1 = scale_pair(sn, rn + 8, a.N, size_t(rn + 8) * n_groups + gn);
+                    n0 = scale_raw(sn, rn, a.N, size_t(rn) * n_groups + gn);
+                    n1 = scale_raw(sn, rn + 8, a.N, size_t(rn + 8) * n_groups + gn);
                     have_next = true;
                 }
-                if (!mbar_wait(full_bar(st), (q / S) & 1, abort_flag, a.err)) { ok = false; break; }
+                if (!mbar_wait(wfull_bar(st), (q / S) & 1, abort_flag, a.err)) { ok = false; break; }
                 const unsigned char *wsrc = smem + L.off_w + st * kGroupBytes + block * kBlockBytes + lane * 16;
                 const uint4 wa = *reinterpret_cast<const uint4 *>(wsrc);
                 const uint4 wb = *reinterpret_cast<const uint4 *>(wsrc + kChunkBytes);
                 const uint32_t wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+                // The stage's bytes are in registers: hand it back to the producer.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(wempty_bar(st));
+                s0 = scale_pair2(s0);
+                s1 = scale_pair2(s1);
                 uint32_t frag[32];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -483,15 +541,17 @@ int tensor_tmem_cols(int bt, int occupancy) {
     return cols;
 }
 
-size_t tensor_smem_bytes(int bt, int stages, int occupancy, int num_groups) {
-    return size_t(tc_smem_layout(bt, stages, tensor_a_stages(bt, occupancy), num_groups).total) +
+size_t tensor_smem_bytes(int bt, int x_stages, int w_stages, int occupancy, int num_groups) {
+    return size_t(tc_smem_layout(bt, x_stages, w_stages, tensor_a_stages(bt, occupancy), num_groups)
+                      .total) +
            1024;  // + alignment slack
 }
 
 cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, const int32_t *m_sizes,
                           int *status, int num_groups, int M_total, int N, int K, cudaStream_t s) {
-    if (p.tile_tokens < 32 || p.tile_tokens > 256 || p.tile_tokens % 32 || p.stages < 2 ||
+    if (p.tile_tokens < 32 || p.tile_tokens > 256 || p.tile_tokens % 32 || p.x_stages < 2 ||
+        p.w_stages < 2 ||
         p.ctas < 1 || num_groups < 1 || num_groups > kMaxGroups || p.occupancy < 1 ||
         p.occupancy > 2 || tensor_a_stages(p.tile_tokens, p.occupancy) < 2)
         return cudaErrorInvalidValue;
@@ -525,7 +585,8 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
     a.n_tiles = p.n_tiles;
     a.split_k = p.split_k;
     a.gps = p.groups_per_slice;
-    a.stages = p.stages;
+    a.x_stages = p.x_stages;
+    a.w_stages = p.w_stages;
     a.a_stages = tensor_a_stages(p.tile_tokens, p.occupancy);
     a.tmem_cols = tensor_tmem_cols(p.tile_tokens, p.occupancy);
     a.vec_store = (N % 8 == 0) && (reinterpret_cast<uintptr_t>(Y) % 16 == 0);
@@ -544,7 +605,7 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
         if (e != cudaSuccess) return e;
         opted[split].fetch_or(bit, std::memory_order_acq_rel);
     }
-    const size_t smem = tensor_smem_bytes(p.tile_tokens, p.stages, p.occupancy, num_groups);
+    const size_t smem = tensor_smem_bytes(p.tile_tokens, p.x_stages, p.w_stages, p.occupancy, num_groups);
     if (smem > size_t(tensor_smem_budget(p.occupancy))) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.ctas);
