@@ -182,7 +182,11 @@ class Shape:
         w4.gemm(self.x, self.w[c], self.s[c], out=self.y, workspace=self.ws)
 
     def partials(self, w4, i):
+        """The main kernel alone: the split-K decode kernel, or the whole call
+        when the plan has one launch."""
         c = i % len(self.w)
+        if self.plan["split_k"] == 1:
+            return self.call(w4, i)
         return w4.gemm_partials(self.x, self.w[c], self.s[c], out=self.y, workspace=self.ws)
 
     def reduce(self, w4):

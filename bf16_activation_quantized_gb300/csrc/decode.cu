@@ -206,6 +206,9 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
     const int rows_alloc = min(8 * MT, M);
     const DecodeSmem L = decode_smem_layout(MT, rows_alloc, GPS);
     const int NS = min(L.stages, ring_stages);
+    // A window deeper than the ring would wait on a slot's next phase before
+    // issuing it: keep it within the ring.
+    const int IF = min(in_flight, NS);
     unsigned char *ring = smem + L.off_ring;
     const uint32_t full0 = smem_u32(smem + L.off_bar);
     const uint32_t empty0 = full0 + 8 * kDecodeMaxStages;
@@ -260,16 +263,16 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         if (lane == 0) {
             const size_t tile_step = size_t(C) * KC * kChunkBytes;
             const uint8_t *src = Wp + (size_t(c0) * KC + size_t(2 * grp0)) * kChunkBytes;
-            // At most in_flight copies are in the air at once (the ring may
+            // At most IF copies are in the air at once (the ring may
             // hold more that have landed): a small burst per CTA lets the
             // first stages land early instead of all of them near the end.
             const int total = n_my * GPS;
             int issued = 0, st = 0, gi = 0, lst = 0;
             uint32_t epar = 1;   // parity of the empty phase to wait for (first lap: none)
-            uint32_t lpar = 0;   // parity of the full phase of copy q - in_flight
+            uint32_t lpar = 0;   // parity of the full phase of copy q - IF
             for (int q = 0; q < total; ++q) {
                 if (q >= NS && !mbar_wait(empty0 + 8 * st, epar, abort_flag, err)) break;
-                if (q >= in_flight) {
+                if (q >= IF) {
                     if (!mbar_wait(full0 + 8 * lst, lpar, abort_flag, err)) break;
                     if (++lst == NS) { lst = 0; lpar ^= 1; }
                 }
@@ -348,13 +351,13 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         // reduction) for the correction table: token r, group gi ->
         // s_corr[(gi * MT + r / 8) * 4 + (r % 8) / 2] = {-1032 S(r), -1032 S(r^1),
         // -1152 S(r), -1152 S(r^1)} (pairs of tokens 2t, 2t + 1), S the scaled sum.
-        const int pairs = 8 * MT * GPS;
+        const int pairs = rows * GPS;       // entries of absent tokens stay unwritten
         const int part = threadIdx.x & 7;
         for (int base = 0; base < pairs; base += kDecodeWarps * 32 / 8) {
             const int pi = base + (threadIdx.x >> 3);
             const int r = pi / GPS, gi = pi - r * GPS;
             float a = 0.f;
-            if (pi < pairs && r < rows) {   // absent tokens: 0 (their rows are never stored)
+            if (pi < pairs) {
                 const float down = pow2f(-slice_shift(s_xmax[r]));
                 // Lane `part` takes 8-element pieces part and 8 + part, so each
                 // access of 8 lanes covers 128 contiguous bytes.
