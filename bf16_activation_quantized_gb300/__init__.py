@@ -61,12 +61,35 @@ def _workspace(device, nbytes: int) -> torch.Tensor:
         return buf
 
 
+# Host-side answers that depend only on the shape, the options and the device
+# (the plan depends on the device's SM count), cached so that a call costs one
+# library call.
+_plan_cache: dict = {}
+_pwb_cache: dict = {}
+
+
+def _workspace_need(M: int, N: int, K: int, o: Options, dev_index: int) -> int:
+    key = (M, N, K, o.arm, o.split_k, o.tile_tokens, dev_index)
+    need = _plan_cache.get(key)
+    if need is None:
+        info = PlanInfo()
+        _lib.check(_lib.lib().w4a16_plan(M, N, K, GROUP, ctypes.byref(o), ctypes.byref(info)),
+                   "w4a16_plan")
+        need = int(info.workspace_bytes)
+        _plan_cache[key] = need
+    return need
+
+
 def layout_version() -> int:
     return int(_lib.lib().w4a16_layout_version())
 
 
 def packed_weight_bytes(N: int, K: int) -> int:
-    return int(_lib.lib().w4a16_packed_weight_bytes(N, K))
+    key = (N, K)
+    nb = _pwb_cache.get(key)
+    if nb is None:
+        nb = _pwb_cache[key] = int(_lib.lib().w4a16_packed_weight_bytes(N, K))
+    return nb
 
 
 def pack(w_canon: torch.Tensor) -> torch.Tensor:
@@ -116,19 +139,26 @@ def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=N
         _need_cuda(out, "out", torch.bfloat16)
     o = _opts(arm, split_k, tile_tokens)
     L = _lib.lib()
-    with torch.cuda.device(x.device):
-        info = PlanInfo()
-        _lib.check(L.w4a16_plan(M, N, K, GROUP, ctypes.byref(o), ctypes.byref(info)), "w4a16_plan")
-        need = int(info.workspace_bytes)
+    dev = x.device
+    switch = dev.index != torch.cuda.current_device()
+    if switch:
+        prev = torch.cuda.current_device()
+        torch.cuda.set_device(dev)
+    try:
+        need = _workspace_need(M, N, K, o, dev.index)
         if workspace is None:
-            ws = _workspace(x.device, need) if need else None
+            ws = _workspace(dev, need) if need else None
         else:
             ws = workspace
         ws_ptr = ws.data_ptr() if ws is not None else None
         ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
         _lib.check(L.w4a16_gemm_ex(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(),
                                    out.data_ptr(), M, N, K, GROUP, ws_ptr, ws_bytes,
-                                   ctypes.byref(o), _stream_ptr(x.device)), "w4a16_gemm_ex")
+                                   ctypes.byref(o), torch.cuda.current_stream(dev).cuda_stream),
+                   "w4a16_gemm_ex")
+    finally:
+        if switch:
+            torch.cuda.set_device(prev)
     return out
 
 

@@ -258,6 +258,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             int idx = blockIdx.x, idw = blockIdx.x;
             bool x_more = tc_tile(a, tab_tiles, tab_rows, idx, tx);
             bool w_more = tc_tile(a, tab_tiles, tab_rows, idw, tw);
+            // Each time the W cursor enters a tile, pull the tile's scales (128
+            // rows x all groups, one contiguous block) into L2, so the
+            // dequantisers' scale loads, issued one group ahead, hit L2.
+            auto prefetch_scales = [&](const TileInfo &ti) {
+                const uint16_t *sg = a.S + (unsigned long long)ti.group * a.s_group_stride;
+                const size_t r0 = size_t(ti.ft) * kTileRows;
+                const size_t r1 = min(size_t(a.N), r0 + kTileRows);
+                // Rounded inwards to 16 bytes: never outside the block.
+                const uintptr_t lo = (reinterpret_cast<uintptr_t>(sg + r0 * n_groups) + 15) & ~uintptr_t(15);
+                const uintptr_t hi = reinterpret_cast<uintptr_t>(sg + r1 * n_groups) & ~uintptr_t(15);
+                if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void *>(lo), uint32_t(hi - lo));
+            };
+            if (w_more) prefetch_scales(tw);
             int gx = x_more ? tx.slice * a.gps : 0, gw = w_more ? tw.slice * a.gps : 0;
             int xq = 0, wq = 0, xs = 0, ws = 0;
             uint32_t xpar = 1, wpar = 1;     // parity of the empty phase to wait for (first lap: none)
@@ -288,7 +301,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     if (++gw == min(n_groups, (tw.slice + 1) * a.gps)) {
                         idw += gridDim.x;
                         w_more = tc_tile(a, tab_tiles, tab_rows, idw, tw);
-                        if (w_more) gw = tw.slice * a.gps;
+                        if (w_more) {
+                            gw = tw.slice * a.gps;
+                            prefetch_scales(tw);
+                        }
                     }
                     progressed = true;
                 }
@@ -310,7 +326,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         }
     } else if (warp == kTcMmaWarp) {
         if (lane == 0) {
-            int st = 0, q = 0, sa = 0, qa = 0, tiles = 0;
+            int st = 0, sa = 0, tiles = 0;
+            uint32_t xph = 0, aph = 0;      // parities of the phases to wait for
             const int S = SX;
             TileInfo ti;
             for (int id = blockIdx.x; tc_tile(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
@@ -320,8 +337,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 const int g1 = min(n_groups, (ti.slice + 1) * a.gps);
                 bool ok = true;
                 for (int grp = g0; grp < g1; ++grp) {
-                    if (!mbar_wait(xfull_bar(st), (q / S) & 1, abort_flag, a.err) ||
-                        !mbar_wait(afull_bar(sa), (qa / SA) & 1, abort_flag, a.err)) {
+                    if (!mbar_wait(xfull_bar(st), xph, abort_flag, a.err) ||
+                        !mbar_wait(afull_bar(sa), aph, abort_flag, a.err)) {
                         ok = false;
                         break;
                     }
@@ -338,10 +355,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     }
                     tc_commit(xempty_bar(st));
                     tc_commit(aempty_bar(sa));
-                    ++q;
-                    st = (st + 1 == S) ? 0 : st + 1;
-                    ++qa;
-                    sa = (sa + 1 == SA) ? 0 : sa + 1;
+                    if (++st == S) { st = 0; xph ^= 1; }
+                    if (++sa == SA) { sa = 0; aph ^= 1; }
                 }
                 if (!ok) break;
                 tc_commit(dfull_bar);
@@ -359,7 +374,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         const int g = lane >> 2;
         const uint32_t lane_base = uint32_t(32 * sub + 16 * half) << 16;
         unsigned char *epi = smem + L.off_epi + warp * kEpiBytesPerWarp;
-        int st = 0, q = 0, sa = 0, qa = 0, tiles = 0;
+        int st = 0, sa = 0, qa = 0, tiles = 0;
+        uint32_t wph = 0;               // parity of the W-ring phase to wait for
+        uint32_t eph = 1;               // parity of the A-ring empty phase (first lap: none)
         const int S = SW;
         // Scales of the next group (possibly in the next tile), loaded one group
         // ahead so the dequantisers never wait on them.
@@ -409,7 +426,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     n1 = scale_raw(sn, rn + 8, a.N, size_t(rn + 8) * n_groups + gn);
                     have_next = true;
                 }
-                if (!mbar_wait(wfull_bar(st), (q / S) & 1, abort_flag, a.err)) { ok = false; break; }
+                if (!mbar_wait(wfull_bar(st), wph, abort_flag, a.err)) { ok = false; break; }
                 const unsigned char *wsrc = smem + L.off_w + st * kGroupBytes + block * kBlockBytes + lane * 16;
                 const uint4 wa = *reinterpret_cast<const uint4 *>(wsrc);
                 const uint4 wb = *reinterpret_cast<const uint4 *>(wsrc + kChunkBytes);
@@ -429,10 +446,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     frag[4 * j + 2] = bf16x2_mul(minus136(magic_pair(wv[j] >> 4)), s1);
                     frag[4 * j + 3] = bf16x2_mul(minus136(magic_pair(wv[j] >> 12)), s1);
                 }
-                ++q;
-                st = (st + 1 == S) ? 0 : st + 1;
+                if (++st == S) { st = 0; wph ^= 1; }
                 flush();
-                if (qa >= SA && !mbar_wait(aempty_bar(sa), ((qa / SA) - 1) & 1, abort_flag, a.err)) {
+                if (qa >= SA && !mbar_wait(aempty_bar(sa), eph, abort_flag, a.err)) {
                     ok = false;
                     break;
                 }
@@ -441,7 +457,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 pending = true;
                 sa_pend = sa;
                 ++qa;
-                sa = (sa + 1 == SA) ? 0 : sa + 1;
+                if (++sa == SA) { sa = 0; eph ^= 1; }
             }
             flush();
             if (!ok) break;
