@@ -104,6 +104,19 @@ __device__ __forceinline__ void consumer_bar() {
     asm volatile("bar.sync 1, %0;" ::"n"(kDecodeWarps * 32) : "memory");
 }
 
+// Pull the scale rows of weight tile `tile` (128 rows x all groups, one
+// contiguous block) into L2, rounded inwards to 16 bytes so nothing outside
+// the block is touched.  Every K slice of the tile asks for the whole block;
+// only the first request goes to DRAM.
+__device__ __forceinline__ void prefetch_tile_scales(const uint16_t *S, int tile, int N, int n_groups) {
+    const size_t r0 = size_t(tile) * kTileRows;
+    const size_t r1 = min(size_t(N), r0 + kTileRows);
+    if (r0 >= r1) return;
+    const uintptr_t lo = (reinterpret_cast<uintptr_t>(S + r0 * n_groups) + 15) & ~uintptr_t(15);
+    const uintptr_t hi = reinterpret_cast<uintptr_t>(S + r1 * n_groups) & ~uintptr_t(15);
+    if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void *>(lo), uint32_t(hi - lo));
+}
+
 // Wait, ignoring the abort flag, for copies still in flight (used only when
 // aborting, so that no copy lands after the CTA has exited).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -238,6 +251,9 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         const int first = min(n_my * GPS, NS);
         for (int q = 0; q < first; ++q)
             bulk_prefetch_l2(src + (q / GPS) * tile_step + (q % GPS) * kStageBytes, kStageBytes);
+        // The scales of the first tiles (the consumers load a tile's scales
+        // two tiles ahead of its use).
+        for (int it = 0; it < min(n_my, 3); ++it) prefetch_tile_scales(S, c0 + it * C, N, n_groups);
     }
     __syncthreads();
     // Read no global memory into the CTA before the previous grid in the
@@ -280,7 +296,14 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
                 bulk_g2s(smem_u32(ring + st * kStageBytes), src + gi * kStageBytes, kStageBytes,
                          full0 + 8 * st);
                 ++issued;
-                if (++gi == GPS) { gi = 0; src += tile_step; }
+                if (++gi == GPS) {
+                    gi = 0;
+                    src += tile_step;
+                    // Entering tile q / GPS: warm L2 with the scales of tile
+                    // q / GPS + 3, which the consumers load about two tiles later.
+                    const int ahead = (q + 1) / GPS + 3;
+                    if (ahead < n_my) prefetch_tile_scales(S, c0 + ahead * C, N, n_groups);
+                }
                 if (++st == NS) { st = 0; epar ^= 1; }
             }
             if (*abort_flag) {
