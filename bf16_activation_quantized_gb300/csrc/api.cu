@@ -159,9 +159,9 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, DecodePlan *d) 
 // or 2 stages that still leaves at least 3 W stages, then as many W stages
 // (8 KB each, up to kTensorMaxWStages) as fit.  Returns false if even 2 + 2
 // does not fit.
-bool tensor_rings(int bt, int num_groups, int occupancy, int *x_stages, int *w_stages) {
+bool tensor_rings(int bt, int num_groups, int occupancy, bool sep, int *x_stages, int *w_stages) {
     const size_t budget = size_t(tensor_smem_budget(occupancy));
-    const size_t fixed = tensor_smem_bytes(bt, 0, 0, occupancy, num_groups);
+    const size_t fixed = tensor_smem_bytes(bt, 0, 0, occupancy, num_groups, sep);
     if (budget <= fixed) return false;
     const size_t avail = budget - fixed;
     const size_t x_stage = 2 * size_t(bt) * 128 + 16;     // + its two barriers
@@ -193,10 +193,13 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
     int found = 0;
     for (int bt = 32; bt <= 256; bt += 32) {
         if (forced_bt > 0 && bt != forced_bt) continue;
-        for (int occ = 1; occ <= 2; ++occ) {
-            if (tensor_a_stages(bt, occ) < 2) continue;       // TMEM share too small
+        for (int variant = 0; variant < 3; ++variant) {
+            // occupancy 2; occupancy 1; occupancy 1 with a separate epilogue
+            const int occ = variant == 0 ? 2 : 1;
+            const bool sep = variant == 2;
+            if (tensor_a_stages(bt, occ, sep) < 2) continue;  // TMEM share too small
             int sx = 0, sw = 0;
-            if (!tensor_rings(bt, num_groups, occ, &sx, &sw)) continue;
+            if (!tensor_rings(bt, num_groups, occ, sep, &sx, &sw)) continue;
             const int max_sk = num_groups > 1 ? 1 : (groups < 16 ? groups : 16);
             for (int sk_req = 1; sk_req <= max_sk; ++sk_req) {
                 int sk = sk_req;
@@ -209,6 +212,12 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                 const long long t_tiles =
                     (long long)num_groups * (long long)ceil_div((long long)(rows_per_unit + 0.999), bt);
                 const long long tiles = (long long)t->n_tiles * t_tiles * sk;
+                // A grid that fits one CTA per SM gains nothing from a second
+                // CTA slot but shallower rings, and the slot lets the block
+                // scheduler put two CTAs of a launch that starts while the
+                // previous one is still resident (programmatic dependent
+                // launch) on the same SM while others stay idle.
+                if (occ == 2 && tiles <= sms) continue;
                 const long long slots = (long long)occ * sms;
                 const long long ctas = tiles < slots ? tiles : slots;
                 const int conc = int(ceil_div(ctas, sms));
@@ -216,7 +225,10 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                                               kChunkBytes / 22.0 + bt * 128.0 / 64.0);
                 const double kb = std::max(kb_tp, kTcChainClk / conc);
                 const double per_cta_tiles = double(ceil_div(tiles, ctas));
-                double time = (per_cta_tiles * conc * 2.0 * gps * kb + per_cta_tiles * 1500.0) / kClockHz;
+                // Per-tile fixed cost: the epilogue, which a separate epilogue
+                // overlaps with the next tile (except the CTA's last one).
+                const double epi = sep ? 1500.0 : per_cta_tiles * 1500.0;
+                double time = (per_cta_tiles * conc * 2.0 * gps * kb + epi) / kClockHz;
                 if (sk > 1) time += 2.0 * sk * double(M) * N * 4.0 / kL2BytesPerS + kReduceSeconds;
                 if (time < best * 0.999) {
                     best = time;
@@ -228,7 +240,8 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                     t->x_stages = sx;
                     t->w_stages = sw;
                     t->occupancy = occ;
-                    t->smem_bytes = tensor_smem_bytes(bt, sx, sw, occ, num_groups);
+                    t->sep_epilogue = sep;
+                    t->smem_bytes = tensor_smem_bytes(bt, sx, sw, occ, num_groups, sep);
                     found = 1;
                 }
                 if (forced_split > 0 || num_groups > 1) break;

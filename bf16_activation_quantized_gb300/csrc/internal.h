@@ -28,6 +28,7 @@ struct TensorPlan {
     int x_stages;         // X ring depth (groups of X in shared memory)
     int w_stages;         // W ring depth (groups of packed weights in shared memory)
     int occupancy;        // CTAs per SM the resources are sized for (1 or 2)
+    bool sep_epilogue;    // two TMEM accumulators drained by dedicated epilogue warps (occupancy 1)
     size_t smem_bytes;
 };
 
@@ -59,9 +60,9 @@ inline int tensor_smem_budget(int occupancy) {
     const int b = kSmemPerSm / occupancy - kSmemReservedPerCta;
     return b < kTensorMaxSmem ? b : kTensorMaxSmem;
 }
-size_t tensor_smem_bytes(int bt, int x_stages, int w_stages, int occupancy, int num_groups);
-int tensor_a_stages(int bt, int occupancy);   // TMEM A ring depth (0: does not fit)
-int tensor_tmem_cols(int bt, int occupancy);  // TMEM columns a CTA allocates
+size_t tensor_smem_bytes(int bt, int x_stages, int w_stages, int occupancy, int num_groups, bool sep);
+int tensor_a_stages(int bt, int occupancy, bool sep);   // TMEM A ring depth (0: does not fit)
+int tensor_tmem_cols(int bt, int occupancy, bool sep);  // TMEM columns a CTA allocates
 cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, const int32_t *m_sizes,
                           int *status, int num_groups, int M_total, int N, int K, cudaStream_t s);

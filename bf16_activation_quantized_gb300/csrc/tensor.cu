@@ -49,6 +49,12 @@ constexpr int kTcDequantWarps = 8;
 constexpr int kTcProducerWarp = 8;
 constexpr int kTcMmaWarp = 9;
 constexpr int kTcThreads = 10 * 32;
+// With a separate epilogue (one CTA per SM): warps 10-13 drain the
+// accumulator while the dequantisers and the MMA go on with the next tile
+// into the other of two TMEM accumulators.
+constexpr int kTcEpiWarp0 = 10;
+constexpr int kTcEpiWarps = 4;
+constexpr int kTcThreadsSep = (kTcEpiWarp0 + kTcEpiWarps) * 32;
 constexpr uint32_t kTcDCol = 0;      // accumulator: columns [0, bt); A stage sa: [bt + 32 sa, bt + 32 sa + 32)
 
 struct TcArgs {
@@ -66,7 +72,8 @@ struct TcArgs {
     int x_stages;             // X ring depth (one 128-column group of X per stage)
     int w_stages;             // W ring depth (8 KB of packed weights per stage)
     int a_stages;             // TMEM A ring depth (one group = 64 columns per stage)
-    int tmem_cols;            // TMEM columns allocated (power of two >= bt + 64 * a_stages)
+    int tmem_cols;            // TMEM columns allocated (power of two >= dcols + 64 * a_stages)
+    int dcols;                // accumulator columns: bt, or 2 bt with a separate epilogue
     int vec_store;            // Y rows are 16-byte aligned: stage the epilogue for 16-byte stores
     unsigned long long w_group_stride;  // bytes between groups' packed weights
     unsigned long long s_group_stride;  // elements between groups' scales
@@ -90,7 +97,7 @@ __host__ __device__ inline TcSmem tc_smem_layout(int bt, int x_stages, int w_sta
     L.off_w = L.off_x + x_stages * L.x_stage;
     L.off_epi = L.off_w + w_stages * kGroupBytes;
     L.off_bar = L.off_epi + kTcDequantWarps * kEpiBytesPerWarp;
-    L.off_misc = L.off_bar + (2 * x_stages + 2 * w_stages + 2 * a_stages + 3) * 8;
+    L.off_misc = L.off_bar + (2 * x_stages + 2 * w_stages + 2 * a_stages + 5) * 8;
     L.off_tab = (L.off_misc + 16 + 15) & ~15;           // group tables: 2 x (G + 1) ints
     L.total = L.off_tab + 2 * (num_groups + 1) * 4;
     return L;
@@ -168,8 +175,54 @@ __device__ __forceinline__ void tc_st_16x256b_x8(uint32_t taddr, const uint32_t 
         : "memory");
 }
 
+// One 32-token column block of a warp's 32 accumulator rows (v[i]: row
+// fb + lane, token ti.x_row0 + 32 cb + i) to Y (bf16) or to the split-K
+// workspace (fp32).  With 16-byte-aligned Y rows the block is transposed
+// through shared memory so that each lane writes 16 bytes (8 rows) of four
+// tokens.
 template <bool kSplit>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__device__ __forceinline__ void tc_store_block(const TcArgs &a, const TileInfo &ti, int fb, int cb,
+                                               const uint32_t (&v)[32], unsigned char *epi,
+                                               int lane) {
+    const int t0 = ti.x_row0 + cb * 32;                // token of v[0]
+    const int nt = min(32, ti.rows - cb * 32);         // valid tokens of the block
+    if (kSplit || !a.vec_store) {
+        const int f = fb + lane;
+        if (f < a.N) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                if (i < nt) {
+                    const size_t off = size_t(t0 + i) * a.N + f;
+                    if (kSplit)
+                        a.ws[size_t(ti.slice) * a.M_total * a.N + off] = __uint_as_float(v[i]);
+                    else
+                        a.Y[off] = f32_to_bf16_rn(__uint_as_float(v[i]));
+                }
+            }
+        }
+    } else {
+        // Transpose through shared memory: [token][32 rows] bf16, then
+        // each lane writes 16 bytes (8 rows) of four tokens.
+        uint16_t *tile = reinterpret_cast<uint16_t *>(epi);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) tile[i * 32 + lane] = f32_to_bf16_rn(__uint_as_float(v[i]));
+        __syncwarp();
+        const int chunk = lane & 3;
+        const int f8 = fb + 8 * chunk;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int i = (lane >> 2) + 8 * c;
+            if (i < nt && f8 < a.N) {
+                const uint4 val = *reinterpret_cast<const uint4 *>(tile + i * 32 + 8 * chunk);
+                *reinterpret_cast<uint4 *>(a.Y + size_t(t0 + i) * a.N + f8) = val;
+            }
+        }
+        __syncwarp();
+    }
+}
+
+template <bool kSplit, bool kSep>
+__global__ void __launch_bounds__(kSep ? kTcThreadsSep : kTcThreads, kSep ? 1 : 2)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled X tiles (the host adds the slack).
@@ -187,9 +240,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     auto wempty_bar = [&](int s) { return bar0 + 8u * (2 * SX + SW + s); };
     auto afull_bar = [&](int s) { return bar0 + 8u * (2 * SX + 2 * SW + s); };
     auto aempty_bar = [&](int s) { return bar0 + 8u * (2 * SX + 2 * SW + SA + s); };
-    const uint32_t dfull_bar = bar0 + 8u * (2 * SX + 2 * SW + 2 * SA);
-    const uint32_t dempty_bar = dfull_bar + 8;
-    const uint32_t done_bar = dfull_bar + 16;
+    // Accumulator b in {0, 1}: dfull[b] (the MMA commit), dempty[b] (its readers).
+    const uint32_t dbar0 = bar0 + 8u * (2 * SX + 2 * SW + 2 * SA);
+    auto dfull_bar = [&](int b) { return dbar0 + 8u * b; };
+    auto dempty_bar = [&](int b) { return dbar0 + 16u + 8u * b; };
+    const uint32_t done_bar = dbar0 + 32;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
     int *tab_tiles = reinterpret_cast<int *>(smem + L.off_tab);
@@ -208,8 +263,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             mbar_init(afull_bar(s), kTcDequantWarps);
             mbar_init(aempty_bar(s), 1);
         }
-        mbar_init(dfull_bar, 1);
-        mbar_init(dempty_bar, kTcDequantWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(dfull_bar(b), 1);
+            mbar_init(dempty_bar(b), kSep ? kTcEpiWarps : kTcDequantWarps);
+        }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -331,8 +388,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             const int S = SX;
             TileInfo ti;
             for (int id = blockIdx.x; tc_tile(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
-                if (tiles > 0 && !mbar_wait(dempty_bar, (tiles - 1) & 1, abort_flag, a.err)) break;
+                // Accumulator of this tile and the wait for its previous readers.
+                const int db = kSep ? (tiles & 1) : 0;
+                const int uses = kSep ? (tiles >> 1) : tiles;     // earlier tiles on this buffer
+                if (uses > 0 && !mbar_wait(dempty_bar(db), (uses - 1) & 1, abort_flag, a.err)) break;
                 tc_fence_after();
+                const uint32_t dcol = tmem_base + kTcDCol + uint32_t(db * a.bt);
                 const int g0 = ti.slice * a.gps;
                 const int g1 = min(n_groups, (ti.slice + 1) * a.gps);
                 bool ok = true;
@@ -344,13 +405,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     }
                     tc_fence_after();
                     const uint32_t xs = smem_u32(smem + L.off_x + st * L.x_stage);
-                    const uint32_t acol = tmem_base + uint32_t(a.bt) + 64u * sa;
+                    const uint32_t acol = tmem_base + uint32_t(a.dcols) + 64u * sa;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const uint64_t bdesc = tc_sdesc_sw128(xs + h * x_bytes);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            tc_mma_ts(tmem_base + kTcDCol, acol + 32u * h + 8u * j, bdesc + 2u * j,
+                            tc_mma_ts(dcol, acol + 32u * h + 8u * j, bdesc + 2u * j,
                                       idesc, (grp > g0 || h > 0 || j > 0) ? 1u : 0u);
                     }
                     tc_commit(xempty_bar(st));
@@ -359,15 +420,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     if (++sa == SA) { sa = 0; aph ^= 1; }
                 }
                 if (!ok) break;
-                tc_commit(dfull_bar);
+                tc_commit(dfull_bar(db));
                 ++tiles;
             }
             // Every MMA this thread issued has completed before TMEM is freed.
             tc_commit(done_bar);
             drain_wait_tc(done_bar, 0);
         }
-    } else {
-        // Dequantisers and epilogue.
+    } else if (warp < kTcDequantWarps) {
+        // Dequantisers (and, without a separate epilogue, the epilogue).
         const int sub = warp & 3;                   // TMEM sub-partition of this warp
         const int half = warp >> 2;                 // which 16 lanes of the sub-partition
         const int block = 2 * sub + half;           // 16-row block of the tile
@@ -453,7 +514,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     break;
                 }
                 tc_fence_after();
-                tc_st_16x256b_x8(tmem_base + lane_base + uint32_t(a.bt) + 64u * sa, frag);
+                tc_st_16x256b_x8(tmem_base + lane_base + uint32_t(a.dcols) + 64u * sa, frag);
                 pending = true;
                 sa_pend = sa;
                 ++qa;
@@ -461,54 +522,47 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             }
             flush();
             if (!ok) break;
+            if (kSep) continue;
             // Epilogue: warp (sub, half) reads lanes 32 sub .. 32 sub + 31 (its
             // weight rows) for every other 32-token column block.
-            if (!mbar_wait(dfull_bar, tiles & 1, abort_flag, a.err)) break;
+            if (!mbar_wait(dfull_bar(0), tiles & 1, abort_flag, a.err)) break;
             tc_fence_after();
             const int fb = ti.ft * kTileRows + 32 * sub;           // first weight row of the warp
             for (int cb = half; cb * 32 < a.bt; cb += 2) {
                 uint32_t v[32];
                 tc_ld_32x32b_x32(tmem_base + (uint32_t(32 * sub) << 16) + kTcDCol + 32u * cb, v);
                 tc_wait_ld();
-                const int t0 = ti.x_row0 + cb * 32;                // token of v[0]
-                const int nt = min(32, ti.rows - cb * 32);         // valid tokens of the block
-                if (kSplit || !a.vec_store) {
-                    const int f = fb + lane;
-                    if (f < a.N) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            if (i < nt) {
-                                const size_t off = size_t(t0 + i) * a.N + f;
-                                if (kSplit)
-                                    a.ws[size_t(ti.slice) * a.M_total * a.N + off] = __uint_as_float(v[i]);
-                                else
-                                    a.Y[off] = f32_to_bf16_rn(__uint_as_float(v[i]));
-                            }
-                        }
-                    }
-                } else {
-                    // Transpose through shared memory: [token][32 rows] bf16, then
-                    // each lane writes 16 bytes (8 rows) of four tokens.
-                    uint16_t *tile = reinterpret_cast<uint16_t *>(epi);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) tile[i * 32 + lane] = f32_to_bf16_rn(__uint_as_float(v[i]));
-                    __syncwarp();
-                    const int chunk = lane & 3;
-                    const int f8 = fb + 8 * chunk;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int i = (lane >> 2) + 8 * c;
-                        if (i < nt && f8 < a.N) {
-                            const uint4 val = *reinterpret_cast<const uint4 *>(tile + i * 32 + 8 * chunk);
-                            *reinterpret_cast<uint4 *>(a.Y + size_t(t0 + i) * a.N + f8) = val;
-                        }
-                    }
-                    __syncwarp();
-                }
+                tc_store_block<kSplit>(a, ti, fb, cb, v, epi, lane);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(dempty_bar);
+            if (lane == 0) mbar_arrive(dempty_bar(0));
+            ++tiles;
+        }
+    } else if (kSep) {
+        // Separate epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (its
+        // 32 weight rows) for every 32-token column block of the tile's
+        // accumulator, alternating between the two accumulators.
+        const int sub = warp & 3;
+        unsigned char *epi = smem + L.off_epi + (warp - kTcEpiWarp0) * kEpiBytesPerWarp;
+        int tiles = 0;
+        TileInfo ti;
+        for (int id = blockIdx.x; tc_tile(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
+            const int db = tiles & 1;
+            if (!mbar_wait(dfull_bar(db), (tiles >> 1) & 1, abort_flag, a.err)) break;
+            tc_fence_after();
+            const int fb = ti.ft * kTileRows + 32 * sub;
+            for (int cb = 0; cb * 32 < a.bt; ++cb) {
+                uint32_t v[32];
+                tc_ld_32x32b_x32(tmem_base + (uint32_t(32 * sub) << 16) + kTcDCol +
+                                     uint32_t(db * a.bt) + 32u * cb,
+                                 v);
+                tc_wait_ld();
+                tc_store_block<kSplit>(a, ti, fb, cb, v, epi, lane);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dempty_bar(db));
             ++tiles;
         }
     }
@@ -544,21 +598,27 @@ EncodeTiledFn encode_tiled() {
 // A ring depth: as many 64-column group stages (at most four) as fit next to
 // the bt accumulator columns in the CTA's share of the SM's 512 TMEM columns
 // (all of them with one CTA per SM, half with two); 0 if none fits.
-int tensor_a_stages(int bt, int occupancy) {
+// A ring depth: as many 64-column group stages (at most four) as fit next to
+// the accumulator columns (bt, or 2 bt with a separate epilogue) in the CTA's
+// share of the SM's 512 TMEM columns (all of them with one CTA per SM, half
+// with two); 0 if none fits.
+int tensor_a_stages(int bt, int occupancy, bool sep) {
     const int share = 512 / occupancy;
-    int sa = (share - bt) / 64;
+    const int dcols = sep ? 2 * bt : bt;
+    int sa = (share - dcols) / 64;
     return sa > 4 ? 4 : (sa < 0 ? 0 : sa);
 }
 
-int tensor_tmem_cols(int bt, int occupancy) {
-    const int need = bt + 64 * tensor_a_stages(bt, occupancy);
+int tensor_tmem_cols(int bt, int occupancy, bool sep) {
+    const int need = (sep ? 2 * bt : bt) + 64 * tensor_a_stages(bt, occupancy, sep);
     int cols = 32;
     while (cols < need) cols <<= 1;
     return cols;
 }
 
-size_t tensor_smem_bytes(int bt, int x_stages, int w_stages, int occupancy, int num_groups) {
-    return size_t(tc_smem_layout(bt, x_stages, w_stages, tensor_a_stages(bt, occupancy), num_groups)
+size_t tensor_smem_bytes(int bt, int x_stages, int w_stages, int occupancy, int num_groups, bool sep) {
+    return size_t(tc_smem_layout(bt, x_stages, w_stages, tensor_a_stages(bt, occupancy, sep),
+                                 num_groups)
                       .total) +
            1024;  // + alignment slack
 }
@@ -569,7 +629,8 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
     if (p.tile_tokens < 32 || p.tile_tokens > 256 || p.tile_tokens % 32 || p.x_stages < 2 ||
         p.w_stages < 2 ||
         p.ctas < 1 || num_groups < 1 || num_groups > kMaxGroups || p.occupancy < 1 ||
-        p.occupancy > 2 || tensor_a_stages(p.tile_tokens, p.occupancy) < 2)
+        p.occupancy > 2 || (p.sep_epilogue && p.occupancy != 1) ||
+        tensor_a_stages(p.tile_tokens, p.occupancy, p.sep_epilogue) < 2)
         return cudaErrorInvalidValue;
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return cudaErrorNotSupported;
@@ -603,29 +664,34 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
     a.gps = p.groups_per_slice;
     a.x_stages = p.x_stages;
     a.w_stages = p.w_stages;
-    a.a_stages = tensor_a_stages(p.tile_tokens, p.occupancy);
-    a.tmem_cols = tensor_tmem_cols(p.tile_tokens, p.occupancy);
+    a.a_stages = tensor_a_stages(p.tile_tokens, p.occupancy, p.sep_epilogue);
+    a.tmem_cols = tensor_tmem_cols(p.tile_tokens, p.occupancy, p.sep_epilogue);
+    a.dcols = p.sep_epilogue ? 2 * p.tile_tokens : p.tile_tokens;
     a.vec_store = (N % 8 == 0) && (reinterpret_cast<uintptr_t>(Y) % 16 == 0);
     a.w_group_stride = packed_bytes(N, K);
     a.s_group_stride = (unsigned long long)N * (K / kGroup);
 
     const bool split = p.split_k > 1;
-    auto kern = split ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
-    static std::atomic<unsigned long long> opted[2];
+    const bool sep = p.sep_epilogue;
+    auto kern = split ? (sep ? tc_gemm_kernel<true, true> : tc_gemm_kernel<true, false>)
+                      : (sep ? tc_gemm_kernel<false, true> : tc_gemm_kernel<false, false>);
+    static std::atomic<unsigned long long> opted[4];
+    const int ki = (split ? 2 : 0) + (sep ? 1 : 0);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
-    if (!(opted[split].load(std::memory_order_acquire) & bit)) {
+    if (!(opted[ki].load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTensorMaxSmem);
         if (e != cudaSuccess) return e;
-        opted[split].fetch_or(bit, std::memory_order_acq_rel);
+        opted[ki].fetch_or(bit, std::memory_order_acq_rel);
     }
-    const size_t smem = tensor_smem_bytes(p.tile_tokens, p.x_stages, p.w_stages, p.occupancy, num_groups);
+    const size_t smem =
+        tensor_smem_bytes(p.tile_tokens, p.x_stages, p.w_stages, p.occupancy, num_groups, sep);
     if (smem > size_t(tensor_smem_budget(p.occupancy))) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.ctas);
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(p.sep_epilogue ? kTcThreadsSep : kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
