@@ -40,10 +40,14 @@ def _need_cuda(t: torch.Tensor, name: str, dtype=None):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _opts(arm, split_k, tile_tokens):
+FLAG_RESIDENT_WEIGHTS = 1
+
+
+def _opts(arm, split_k, tile_tokens, resident_weights=False):
     if arm not in _ARMS:
         raise ValueError(f"arm must be one of {list(_ARMS)}")
-    return Options(_ARMS[arm], int(split_k), int(tile_tokens))
+    return Options(_ARMS[arm], int(split_k), int(tile_tokens),
+                   FLAG_RESIDENT_WEIGHTS if resident_weights else 0)
 
 
 _ws_lock = threading.Lock()
@@ -122,8 +126,12 @@ def plan(M: int, N: int, K: int, arm=None, split_k: int = 0, tile_tokens: int = 
 
 def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=None,
          split_k: int = 0, tile_tokens: int = 0, out: torch.Tensor | None = None,
-         workspace: torch.Tensor | None = None) -> torch.Tensor:
-    """Y = X . dequant(W)^T.  x: bf16 [M, K]; scales: bf16 [N, K/128]; returns bf16 [M, N]."""
+         workspace: torch.Tensor | None = None, resident_weights: bool = False) -> torch.Tensor:
+    """Y = X . dequant(W)^T.  x: bf16 [M, K]; scales: bf16 [N, K/128]; returns bf16 [M, N].
+
+    ``resident_weights=True`` promises that no kernel still running on the
+    current stream writes ``w_packed`` or ``scales`` (W4A16_FLAG_RESIDENT_WEIGHTS):
+    the call may then start streaming them before the previous kernel ends."""
     _need_cuda(x, "x", torch.bfloat16)
     _need_cuda(scales, "scales", torch.bfloat16)
     _need_cuda(w_packed, "w_packed", torch.uint8)
@@ -137,7 +145,7 @@ def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=N
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     else:
         _need_cuda(out, "out", torch.bfloat16)
-    o = _opts(arm, split_k, tile_tokens)
+    o = _opts(arm, split_k, tile_tokens, resident_weights)
     L = _lib.lib()
     dev = x.device
     switch = dev.index != torch.cuda.current_device()
@@ -164,14 +172,14 @@ def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=N
 
 def gemm_partials(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *,
                   out: torch.Tensor, workspace: torch.Tensor, arm=None, split_k: int = 0,
-                  tile_tokens: int = 0) -> int:
+                  tile_tokens: int = 0, resident_weights: bool = False) -> int:
     """First launch of gemm() only (see w4a16_gemm_partials); returns SPLIT_K.
 
     With SPLIT_K > 1 the fp32 partial sums land in ``workspace`` as
     [SPLIT_K, M, N] and ``out`` is untouched; splitk_reduce() finishes the call."""
     M, K = x.shape
     N = scales.shape[0]
-    o = _opts(arm, split_k, tile_tokens)
+    o = _opts(arm, split_k, tile_tokens, resident_weights)
     sk = ctypes.c_int(0)
     with torch.cuda.device(x.device):
         _lib.check(_lib.lib().w4a16_gemm_partials(

@@ -17,7 +17,7 @@ SZ = ctypes.c_size_t
 
 
 class Options(ctypes.Structure):
-    _fields_ = [("arm", I), ("split_k", I), ("tile_tokens", I)]
+    _fields_ = [("arm", I), ("split_k", I), ("tile_tokens", I), ("flags", I)]
 
 
 class PlanInfo(ctypes.Structure):

@@ -253,15 +253,16 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
 
 w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p) {
     std::memset(p, 0, sizeof *p);
-    int sms = 0;
-    if (device_sm_count(&sms) != 0 || sms < 1) return W4A16_ERR_CUDA;
     int arm = opts ? opts->arm : W4A16_ARM_AUTO;
     if (arm != W4A16_ARM_AUTO && arm != W4A16_ARM_DECODE && arm != W4A16_ARM_TENSOR)
         return W4A16_ERR_INVALID_ARG;
     if (opts && opts->split_k < 0) return W4A16_ERR_INVALID_ARG;
+    if (opts && (opts->flags & ~int(W4A16_FLAG_RESIDENT_WEIGHTS))) return W4A16_ERR_INVALID_ARG;
     const int forced_bt = opts ? opts->tile_tokens : 0;
     if (forced_bt != 0 && (forced_bt < 32 || forced_bt > 256 || forced_bt % 32))
         return W4A16_ERR_UNSUPPORTED;
+    int sms = 0;
+    if (device_sm_count(&sms) != 0 || sms < 1) return W4A16_ERR_CUDA;
     if (arm == W4A16_ARM_AUTO) arm = M <= kDecodeMaxM ? W4A16_ARM_DECODE : W4A16_ARM_TENSOR;
     if (arm == W4A16_ARM_DECODE && forced_bt != 0) return W4A16_ERR_INVALID_ARG;
     p->arm = arm;
@@ -367,8 +368,9 @@ static w4a16_status gemm_impl(const w4a16_bf16 *X, const uint8_t *W_packed,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float *ws = static_cast<float *>(workspace);
     cudaError_t e;
+    const bool resident = opts && (opts->flags & W4A16_FLAG_RESIDENT_WEIGHTS);
     if (p.arm == W4A16_ARM_DECODE)
-        e = launch_decode(p.decode, X, W_packed, scales, Y, ws, M, N, K, s);
+        e = launch_decode(p.decode, X, W_packed, scales, Y, ws, resident, M, N, K, s);
     else
         e = launch_tensor(p.tensor, X, W_packed, scales, Y, ws, nullptr, nullptr, 1, M, N, K, s);
     if (e != cudaSuccess) return W4A16_ERR_CUDA;

@@ -84,15 +84,6 @@ __device__ __forceinline__ int slice_shift(int max_abs_bits) {
 }
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
 
-// 16-byte shared load done only when pred != 0; otherwise v keeps its value.
-__device__ __forceinline__ void lds128_if(uint4 &v, const void *p, uint32_t pred) {
-    asm volatile(
-        "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %4, 0;\n\t"
-        "@q ld.shared.v4.u32 {%0,%1,%2,%3}, [%5];\n\t}"
-        : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
-        : "r"(pred), "r"(smem_u32(p)));
-}
-
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -200,7 +191,8 @@ template <int MT, int GPS, bool kSplit>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
               const uint16_t *__restrict__ S, uint16_t *__restrict__ Y, float *__restrict__ ws,
-              int M, int N, int K, int n_tiles, int ring_stages, int in_flight, int s_vec, int *err) {
+              int M, int N, int K, int n_tiles, int ring_stages, int in_flight, int s_vec,
+              int resident, int *err) {
     extern __shared__ __align__(128) unsigned char smem[];
     // Groups between scale applications (register budget): up to 8 for 8
     // tokens, up to 4 for 16.
@@ -245,25 +237,22 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         // While the previous grid finishes, pull this CTA's first weight
         // stages into L2 (a prefetch reads nothing into the CTA and writes
         // nothing, so it needs no dependency wait); the copies after the wait
-        // then hit L2.
-        const uint8_t *src = Wp + (size_t(c0) * KC + size_t(2 * grp0)) * kChunkBytes;
-        const size_t tile_step = size_t(C) * KC * kChunkBytes;
-        const int first = min(n_my * GPS, NS);
-        for (int q = 0; q < first; ++q)
-            bulk_prefetch_l2(src + (q / GPS) * tile_step + (q % GPS) * kStageBytes, kStageBytes);
+        // then hit L2.  Resident weights are copied straight away instead.
+        if (!resident) {
+            const uint8_t *src = Wp + (size_t(c0) * KC + size_t(2 * grp0)) * kChunkBytes;
+            const size_t tile_step = size_t(C) * KC * kChunkBytes;
+            const int first = min(n_my * GPS, NS);
+            for (int q = 0; q < first; ++q)
+                bulk_prefetch_l2(src + (q / GPS) * tile_step + (q % GPS) * kStageBytes, kStageBytes);
+        }
         // The scales of the first tiles (the consumers load a tile's scales
         // two tiles ahead of its use).
         for (int it = 0; it < min(n_my, 3); ++it) prefetch_tile_scales(S, c0 + it * C, N, n_groups);
     }
     __syncthreads();
-    // Read no global memory into the CTA before the previous grid in the
-    // stream has completed (it may have written X, W or the scales).
-    pdl_wait();
 
     const int g = lane >> 2, t = lane & 3;
     const bool vec_scales = s_vec != 0;
-    // Scales of rows g and g+8 of this warp's block for the first tile: issued
-    // before anything else so they are not queued behind the weight stream.
     ScaleRow<GPS> s_cur[2], s_next[2];
     auto load_scales = [&](int tile, ScaleRow<GPS> (&dst)[2]) {
         const int f0 = tile * kTileRows + warp * 16 + g;
@@ -271,11 +260,20 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         dst[0] = load_scale_row<GPS>(p0, f0 < N, vec_scales);
         dst[1] = load_scale_row<GPS>(p0 + 8 * size_t(n_groups), f0 + 8 < N, vec_scales);
     };
+    // Read nothing that the previous grid in the stream may write before it
+    // has completed: X always, and W and the scales unless they are resident
+    // (then only the consumers wait, for X, and they load the first tile's
+    // scales before waiting).
+    if (resident && warp < kDecodeWarps && n_my > 0) load_scales(c0, s_cur);
+    if (!resident || warp < kDecodeWarps) pdl_wait();
+
     if (warp == kDecodeWarps) {
-        // Producer: one lane streams every (tile, group) block of this CTA,
-        // starting once the consumers have issued their X and scale loads so
-        // that those small reads are not queued behind the weight stream.
-        named_bar_sync(2, kDecodeThreads);
+        // Producer: one lane streams every (tile, group) block of this CTA.
+        // Non-resident weights: it starts once the consumers have issued their
+        // X and scale loads, so that those small reads are not queued behind
+        // the weight stream.  Resident weights: it starts at once and fills
+        // the ring while the previous grid finishes.
+        if (!resident) named_bar_sync(2, kDecodeThreads);
         if (lane == 0) {
             const size_t tile_step = size_t(C) * KC * kChunkBytes;
             const uint8_t *src = Wp + (size_t(c0) * KC + size_t(2 * grp0)) * kChunkBytes;
@@ -337,8 +335,12 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
             xval[k] = ldg_nc16(X + size_t(m0 + r) * K + size_t(grp0) * kGroup + v * 8);
         }
     }
-    if (warp < kDecodeWarps && n_my > 0) load_scales(c0, s_cur);
-    named_bar_arrive(2, kDecodeThreads);
+    if (!resident) {
+        // Scales of rows g and g+8 of this warp's block for the first tile,
+        // issued before the weight stream starts.
+        if (n_my > 0) load_scales(c0, s_cur);
+        named_bar_arrive(2, kDecodeThreads);
+    }
 #pragma unroll
     for (int k = 0; k < kVecPerThread; ++k) {
         const int i = threadIdx.x + k * kDecodeWarps * 32;
@@ -434,11 +436,6 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
             fac16[o][e] = 0.0625f * fac[o][e];
         }
 
-    const uint32_t xload = g < rows;
-    uint4 xkeep[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) xkeep[q] = make_uint4(0, 0, 0, 0);
-
     int st = 0;
     uint32_t fpar = 0;
     const unsigned char *wlane = ring + warp * kBlockBytes + lane * 16;
@@ -483,18 +480,11 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
                     float c[4] = {cc.x, cc.y, cc.z, cc.w};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        // Rows of absent tokens hold stale bytes: they reach
-                        // only those tokens' output columns, which are never
-                        // stored.  With one token octet, lanes of absent rows
-                        // skip the load and keep stale registers instead.
-                        uint4 xv;
-                        const uint16_t *xp = xs + xrow[o] + gi * kGroup + 32 * q;
-                        if constexpr (MT == 1) {
-                            lds128_if(xkeep[q], xp, xload);
-                            xv = xkeep[q];
-                        } else {
-                            xv = *reinterpret_cast<const uint4 *>(xp);
-                        }
+                        // Lanes of absent tokens read the last staged row (xrow
+                        // is clamped): those values reach only absent tokens'
+                        // output columns, which are never stored.
+                        const uint4 xv = *reinterpret_cast<const uint4 *>(
+                            xs + xrow[o] + gi * kGroup + 32 * q);
                         float d[4];
                         mma_16816_f16_c(d, af[2 * q], xv.x, xv.y, c);
                         mma_16816_f16_c(c, af[2 * q + 1], xv.z, xv.w, d);
@@ -550,9 +540,9 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
 
 // Split-K reduce: each thread owns VEC consecutive outputs (one VEC-wide load
 // per slice).  VEC shrinks for small outputs so that enough threads run;
-// loads are issued 16 slices at a time so their latencies overlap, and the
-// sum runs over the slices in ascending order, so the result does not depend
-// on VEC or the unrolling.
+// loads are issued a batch of slices at a time so their latencies overlap,
+// and the sum runs over the slices in ascending order, so the result does not
+// depend on VEC, the batch or the unrolling.
 template <int VEC>
 struct FloatVec;
 template <> struct FloatVec<1> { using T = float; };
@@ -570,7 +560,10 @@ __device__ __forceinline__ void vstore(uint16_t *y, float4 a) {
     *reinterpret_cast<uint2 *>(y) = make_uint2(pack_bf16x2_rn(a.x, a.y), pack_bf16x2_rn(a.z, a.w));
 }
 
-template <int VEC>
+// kBatch slices are loaded per round trip: 16, or 64 / VEC for deeper splits
+// (a 64-deep batch also costs registers and instructions, which slows the
+// short splits down when the kernel is chained between two GEMM launches).
+template <int VEC, int kBatch>
 __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float *__restrict__ ws, uint16_t *__restrict__ Y, int splits,
                      long long count) {
@@ -580,14 +573,18 @@ splitk_reduce_kernel(const float *__restrict__ ws, uint16_t *__restrict__ Y, int
     const long long i = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * VEC;
     if (i >= count) return;
     T a;
-    for (int s = 0; s < splits; s += 16) {
-        T b[16];
+    const float *q = ws + i;   // slice s of this thread's outputs: q + s * count
+    for (int s = 0; s < splits; s += kBatch) {
+        const int n = min(kBatch, splits - s);
+        T b[kBatch];
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-            if (s + u < splits) b[u] = *reinterpret_cast<const T *>(ws + size_t(s + u) * count + i);
+        for (int u = 0; u < kBatch; ++u) {
+            if (u < n) b[u] = *reinterpret_cast<const T *>(q);
+            q += count;
+        }
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            if (s + u >= splits) break;
+        for (int u = 0; u < kBatch; ++u) {
+            if (u >= n) break;
             if (s + u == 0) a = b[u];
             else vadd(a, b[u]);
         }
@@ -597,8 +594,8 @@ splitk_reduce_kernel(const float *__restrict__ ws, uint16_t *__restrict__ Y, int
 
 template <int MT, int GPS, bool kSplit>
 cudaError_t launch_decode_t(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
-                            const uint16_t *S, uint16_t *Y, float *ws, int M, int N, int K,
-                            cudaStream_t s) {
+                            const uint16_t *S, uint16_t *Y, float *ws, bool resident, int M, int N,
+                            int K, cudaStream_t s) {
     const int smem = decode_smem_layout(MT, M < 8 * MT ? M : 8 * MT, GPS).total;
     auto kern = decode_kernel<MT, GPS, kSplit>;
     if (smem > 48 * 1024) {
@@ -629,20 +626,20 @@ cudaError_t launch_decode_t(const DecodePlan &p, const uint16_t *X, const uint8_
     if (!err) return cudaErrorUnknown;
     const int s_vec = (reinterpret_cast<uintptr_t>(S) % (2 * GPS)) == 0;
     return cudaLaunchKernelEx(&cfg, kern, X, Wp, S, Y, ws, M, N, K, p.n_tiles, p.ring, p.in_flight,
-                              s_vec, err);
+                              s_vec, int(resident), err);
 }
 
 template <int MT, bool kSplit>
 cudaError_t launch_decode_gps(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
-                              const uint16_t *S, uint16_t *Y, float *ws, int M, int N, int K,
-                              cudaStream_t s) {
+                              const uint16_t *S, uint16_t *Y, float *ws, bool res, int M, int N,
+                              int K, cudaStream_t s) {
     switch (p.groups_per_slice) {
-        case 1: return launch_decode_t<MT, 1, kSplit>(p, X, Wp, S, Y, ws, M, N, K, s);
-        case 2: return launch_decode_t<MT, 2, kSplit>(p, X, Wp, S, Y, ws, M, N, K, s);
-        case 4: return launch_decode_t<MT, 4, kSplit>(p, X, Wp, S, Y, ws, M, N, K, s);
-        case 8: return launch_decode_t<MT, 8, kSplit>(p, X, Wp, S, Y, ws, M, N, K, s);
+        case 1: return launch_decode_t<MT, 1, kSplit>(p, X, Wp, S, Y, ws, res, M, N, K, s);
+        case 2: return launch_decode_t<MT, 2, kSplit>(p, X, Wp, S, Y, ws, res, M, N, K, s);
+        case 4: return launch_decode_t<MT, 4, kSplit>(p, X, Wp, S, Y, ws, res, M, N, K, s);
+        case 8: return launch_decode_t<MT, 8, kSplit>(p, X, Wp, S, Y, ws, res, M, N, K, s);
         case 16:
-            if constexpr (MT == 1) return launch_decode_t<MT, 16, kSplit>(p, X, Wp, S, Y, ws, M, N, K, s);
+            if constexpr (MT == 1) return launch_decode_t<MT, 16, kSplit>(p, X, Wp, S, Y, ws, res, M, N, K, s);
             return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
@@ -655,7 +652,7 @@ int decode_smem_needed(int M, int mt, int groups_per_slice) {
 }
 
 cudaError_t launch_decode(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
-                          const uint16_t *S, uint16_t *Y, float *ws, int M, int N, int K,
+                          const uint16_t *S, uint16_t *Y, float *ws, bool res, int M, int N, int K,
                           cudaStream_t s) {
     if (p.ring < 2 || p.in_flight < 1 || p.in_flight > p.ring) return cudaErrorInvalidValue;
     if (p.groups_per_slice < 1 || p.groups_per_slice > kDecodeMaxGps || p.ctas_per_slice < 1 ||
@@ -664,10 +661,10 @@ cudaError_t launch_decode(const DecodePlan &p, const uint16_t *X, const uint8_t 
     if ((K / kGroup) % p.groups_per_slice != 0) return cudaErrorInvalidValue;
     const bool split = p.split_k > 1;
     if (p.mt == 1)
-        return split ? launch_decode_gps<1, true>(p, X, Wp, S, Y, ws, M, N, K, s)
-                     : launch_decode_gps<1, false>(p, X, Wp, S, Y, ws, M, N, K, s);
-    return split ? launch_decode_gps<2, true>(p, X, Wp, S, Y, ws, M, N, K, s)
-                 : launch_decode_gps<2, false>(p, X, Wp, S, Y, ws, M, N, K, s);
+        return split ? launch_decode_gps<1, true>(p, X, Wp, S, Y, ws, res, M, N, K, s)
+                     : launch_decode_gps<1, false>(p, X, Wp, S, Y, ws, res, M, N, K, s);
+    return split ? launch_decode_gps<2, true>(p, X, Wp, S, Y, ws, res, M, N, K, s)
+                 : launch_decode_gps<2, false>(p, X, Wp, S, Y, ws, res, M, N, K, s);
 }
 
 cudaError_t launch_reduce(const float *ws, uint16_t *Y, int splits, long long count, bool pdl,
@@ -695,9 +692,15 @@ cudaError_t launch_reduce(const float *ws, uint16_t *Y, int splits, long long co
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (vec == 4) return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<4>, ws, Y, splits, count);
-    if (vec == 2) return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<2>, ws, Y, splits, count);
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<1>, ws, Y, splits, count);
+    const bool deep = splits > 16;
+    if (vec == 4)
+        return deep ? cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<4, 16>, ws, Y, splits, count)
+                    : cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<4, 16>, ws, Y, splits, count);
+    if (vec == 2)
+        return deep ? cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<2, 32>, ws, Y, splits, count)
+                    : cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<2, 16>, ws, Y, splits, count);
+    return deep ? cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<1, 64>, ws, Y, splits, count)
+                : cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<1, 16>, ws, Y, splits, count);
 }
 
 }  // namespace w4a16

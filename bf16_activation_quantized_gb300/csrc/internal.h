@@ -47,9 +47,11 @@ size_t packed_bytes(int N, int K);
 cudaError_t launch_pack(const uint8_t *w_canon, uint8_t *w_packed, int N, int K, cudaStream_t s);
 cudaError_t launch_dequant(const uint8_t *w_packed, const uint16_t *scales, void *out,
                            bool bf16_out, int N, int K, cudaStream_t s);
+// resident: the weights and scales are not written by the previous kernel on
+// the stream, so the weight stream may start before that kernel completes.
 cudaError_t launch_decode(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
-                          const uint16_t *S, uint16_t *Y, float *ws, int M, int N, int K,
-                          cudaStream_t s);
+                          const uint16_t *S, uint16_t *Y, float *ws, bool resident, int M, int N,
+                          int K, cudaStream_t s);
 // Tensor arm (tensor.cu).
 constexpr int kTensorMaxSmem = 227 * 1024;     // per-CTA opt-in maximum
 constexpr int kSmemPerSm = 228 * 1024;         // shared memory of one SM

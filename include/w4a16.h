@@ -57,6 +57,20 @@ typedef enum {
     W4A16_ARM_TENSOR = 2    /* TMA + TMEM + tcgen05.mma arm */
 } w4a16_arm;
 
+/* w4a16_options.flags bits. */
+enum {
+    /* W_packed and scales are resident: no kernel still running on the stream
+     * when the call is made writes them (they were written before that kernel
+     * started, e.g. when the model was loaded).  The call's kernel is launched
+     * with programmatic dependent launch and may then start streaming the
+     * weights into shared memory while the previous kernel on the stream is
+     * still running; only X is read after that kernel has completed.  Without
+     * the flag nothing is read before it has completed.  Do not set it when
+     * W_packed or scales alias the output or workspace of a call just before
+     * on the same stream. */
+    W4A16_FLAG_RESIDENT_WEIGHTS = 1
+};
+
 /* Overrides for tests and tuning.  Zero-initialised = automatic. */
 typedef struct {
     int arm;          /* w4a16_arm */
@@ -65,6 +79,7 @@ typedef struct {
                          slices hold 1, 2, 4, 8 or (up to 8 tokens) 16 of the 128-wide
                          groups each. */
     int tile_tokens;  /* tensor arm only: 0 = automatic, else tokens per tile (32..256, multiple of 32) */
+    int flags;        /* W4A16_FLAG_* bits; unknown bits are rejected (W4A16_ERR_INVALID_ARG) */
 } w4a16_options;
 
 /* What the dispatcher chose for a shape on the current device. */

@@ -319,3 +319,55 @@ def test_splitk_reduce_bit_exact(S, M, N):
     ref = oracle.sum_slices(ws)
     expect = np.array([oracle.f64_to_bf16(v) for v in ref.ravel()], dtype=np.uint16).reshape(M, N)
     assert np.array_equal(got, expect)
+
+
+# ------------------------------------------------------------ resident weights
+@pytest.mark.parametrize("M,N,K", [(1, 8192, 8192), (16, 2560, 9728), (3, 300, 640), (8, 19456, 2560)])
+def test_resident_weights_give_the_same_bits(M, N, K):
+    # The flag only moves the weight stream ahead of the dependency wait.
+    p = problem(M, N, K)
+    a = bf16_to_u16(run(p))
+    b = bf16_to_u16(run(p, resident_weights=True))
+    assert np.array_equal(a, b)
+
+
+def test_resident_weights_chain_reads_x_after_the_previous_call():
+    # Y of one call is X of the next (a chain of layers, same stream, inside one
+    # graph): each call streams its weights early but must read X only after the
+    # call before it has completed.
+    K = 2048
+    layers = [DeviceProblem(syn.make_gemm_inputs(1, K, K, seed=50 + i)) for i in range(4)]
+    x0 = layers[0].x.clone()
+
+    def chain(resident):
+        x = x0
+        outs = []
+        for lp in layers:
+            y = w4.gemm(x, lp.w_packed, lp.scales, resident_weights=resident)
+            outs.append(y)
+            x = y
+        return outs
+
+    eager = [bf16_to_u16(y) for y in chain(False)]
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        chain(True)                                    # warm-up on the side stream
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        outs = chain(True)
+    for _ in range(3):
+        for y in outs:
+            y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for y, e in zip(outs, eager):
+            assert np.array_equal(bf16_to_u16(y), e)
+    # and the chain itself is right: the last layer against the oracle, fed the
+    # previous layer's bf16 output
+    xin = bf16_to_u16(outs[-2]).reshape(1, K)
+    last = layers[-1].inp
+    ref = oracle.gemm(xin, last.w_canon, last.scales, 1, K, K)
+    assert_close(bf16_to_f64(outs[-1]), ref, what="chain")
