@@ -78,13 +78,13 @@ struct Plan {
 int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
 
 // Measured on GB300 across the decode workloads (1 to 16 tokens, N 2560 to
-// 19456, K 2560 to 9728): at equal modelled time, 4-group slices run fastest
-// (more tiles per CTA keep its copy ring busy without long unrolled slices),
-// then 8, 2, 16 and 1.  The factor breaks near-ties in that order.
+// 19456, K 2560 to 9728, weights resident): at equal modelled time, 8- and
+// 4-group slices run fastest (8 first: fewer tile epilogues per CTA), then 2,
+// 16 and 1.  The factor breaks near-ties in that order.
 double decode_slice_preference(int gps) {
     switch (gps) {
         case 4: return 1.0;
-        case 8: return 1.04;
+        case 8: return 1.0;
         case 2: return 1.06;
         case 16: return 1.08;
         default: return 1.12;
