@@ -41,13 +41,18 @@ def _need_cuda(t: torch.Tensor, name: str, dtype=None):
 
 
 FLAG_RESIDENT_WEIGHTS = 1
+FLAG_DECODE_WHOLE_K = 2
+FLAG_DECODE_K_SLICES = 4
+_KERNELS = {None: 0, "auto": 0, "whole_k": FLAG_DECODE_WHOLE_K, "k_slices": FLAG_DECODE_K_SLICES}
 
 
-def _opts(arm, split_k, tile_tokens, resident_weights=False):
+def _opts(arm, split_k, tile_tokens, resident_weights=False, decode_kernel=None):
     if arm not in _ARMS:
         raise ValueError(f"arm must be one of {list(_ARMS)}")
-    return Options(_ARMS[arm], int(split_k), int(tile_tokens),
-                   FLAG_RESIDENT_WEIGHTS if resident_weights else 0)
+    if decode_kernel not in _KERNELS:
+        raise ValueError(f"decode_kernel must be one of {list(_KERNELS)}")
+    flags = (FLAG_RESIDENT_WEIGHTS if resident_weights else 0) | _KERNELS[decode_kernel]
+    return Options(_ARMS[arm], int(split_k), int(tile_tokens), flags)
 
 
 _ws_lock = threading.Lock()
@@ -73,7 +78,7 @@ _pwb_cache: dict = {}
 
 
 def _workspace_need(M: int, N: int, K: int, o: Options, dev_index: int) -> int:
-    key = (M, N, K, o.arm, o.split_k, o.tile_tokens, dev_index)
+    key = (M, N, K, o.arm, o.split_k, o.tile_tokens, o.flags, dev_index)
     need = _plan_cache.get(key)
     if need is None:
         info = PlanInfo()
@@ -112,26 +117,28 @@ def pack(w_canon: torch.Tensor) -> torch.Tensor:
 
 
 def plan(M: int, N: int, K: int, arm=None, split_k: int = 0, tile_tokens: int = 0,
-         device=None) -> dict:
+         device=None, decode_kernel=None) -> dict:
     """What the dispatcher picks for this shape on the (current) device."""
     info = PlanInfo()
-    o = _opts(arm, split_k, tile_tokens)
+    o = _opts(arm, split_k, tile_tokens, decode_kernel=decode_kernel)
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         _lib.check(_lib.lib().w4a16_plan(M, N, K, GROUP, ctypes.byref(o), ctypes.byref(info)),
                    "w4a16_plan")
     return {"arm": {1: "decode", 2: "tensor"}.get(info.arm, info.arm), "split_k": info.split_k,
             "tile_tokens": info.tile_tokens, "ctas": info.ctas,
-            "workspace_bytes": int(info.workspace_bytes)}
+            "workspace_bytes": int(info.workspace_bytes), "whole_k": bool(info.whole_k)}
 
 
 def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=None,
          split_k: int = 0, tile_tokens: int = 0, out: torch.Tensor | None = None,
-         workspace: torch.Tensor | None = None, resident_weights: bool = False) -> torch.Tensor:
+         workspace: torch.Tensor | None = None, resident_weights: bool = False,
+         decode_kernel=None) -> torch.Tensor:
     """Y = X . dequant(W)^T.  x: bf16 [M, K]; scales: bf16 [N, K/128]; returns bf16 [M, N].
 
     ``resident_weights=True`` promises that no kernel still running on the
     current stream writes ``w_packed`` or ``scales`` (W4A16_FLAG_RESIDENT_WEIGHTS):
-    the call may then start streaming them before the previous kernel ends."""
+    the call may then start streaming them before the previous kernel ends.
+    ``decode_kernel`` ("whole_k" or "k_slices") forces the decode arm's kernel."""
     _need_cuda(x, "x", torch.bfloat16)
     _need_cuda(scales, "scales", torch.bfloat16)
     _need_cuda(w_packed, "w_packed", torch.uint8)
@@ -145,7 +152,7 @@ def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=N
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     else:
         _need_cuda(out, "out", torch.bfloat16)
-    o = _opts(arm, split_k, tile_tokens, resident_weights)
+    o = _opts(arm, split_k, tile_tokens, resident_weights, decode_kernel)
     L = _lib.lib()
     dev = x.device
     switch = dev.index != torch.cuda.current_device()

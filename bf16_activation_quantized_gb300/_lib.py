@@ -22,7 +22,7 @@ class Options(ctypes.Structure):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("arm", I), ("split_k", I), ("tile_tokens", I), ("ctas", I),
-                ("workspace_bytes", SZ)]
+                ("workspace_bytes", SZ), ("whole_k", I)]
 
 
 # name -> (restype, argtypes); mirrors include/w4a16.h one to one.

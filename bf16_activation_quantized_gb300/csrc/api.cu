@@ -49,7 +49,13 @@ constexpr int kDecodeInFlight = 3;            // bulk copies in the air per deco
 constexpr double kHbmBytesPerS = 6.5e12;      // planning figures, not measurements
 constexpr double kCtaBytesPerS = 25e9;        // one CTA's streaming rate (32 KB in flight)
 constexpr double kL2BytesPerS = 20e12;
-constexpr double kReduceSeconds = 0.5e-6;
+constexpr double kReduceSeconds = 1.0e-6;        // reduce kernel and its launch boundary (measured)
+constexpr double kTensorReduceSeconds = 0.5e-6;  // the tensor arm's plans were tuned with this
+constexpr double kWholeKSeconds = 0.2e-6;        // whole-K kernel: part sums
+// Whole-K kernel: every CTA stages all of X at the start; measured on GB300
+// the CTAs together draw X from L2 at about this rate (the same lines, half
+// of the CTAs on the other die).
+constexpr double kXBroadcastBytesPerS = 2.8e12;
 constexpr double kReducePerSliceSeconds = 0.01e-6;  // reduce latency per extra slice
 constexpr int kDecodeMaxM = 16;               // auto dispatch: M <= 16 -> decode arm
 constexpr double kClockHz = 1.9e9;            // planning clock
@@ -96,7 +102,10 @@ double decode_slice_preference(int gps) {
 // the busiest CTA's bytes at one CTA's streaming rate) + the split-K
 // workspace round trip; at most kDecodeCtasPerSm CTAs per SM are launched so
 // that all of them are resident at once.
-void plan_decode(int M, int N, int K, int sms, int forced_split, DecodePlan *d) {
+// Whole-K plans (no split-K) compete with the sliced ones: each CTA owns
+// B 16-row blocks over all of K, 8 / B K-parts per CTA; one CTA per B blocks,
+// all resident at once.  wk: 0 = either kernel, 1 = whole-K only, 2 = slices only.
+void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, DecodePlan *d) {
     const int groups = K / kGroup;
     d->mt = M <= 8 ? 1 : 2;
     d->token_blocks = ceil_div(M, 8 * d->mt);
@@ -109,6 +118,27 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, DecodePlan *d) 
     d->ctas_per_slice = 1;
     d->ring = kDecodeRing;
     d->in_flight = kDecodeInFlight;
+    d->wk_blocks = 0;
+    if (wk != 2 && forced_split <= 1) {
+        // (one block per CTA would leave each K-part a single ring slot)
+        for (int B : {8, 4, 2}) {
+            if (!decode_wk_fits(M, K, B)) continue;
+            const long long ctas = (long long)d->n_tiles * (kTileRows / 16) / B;
+            if (ctas > slots) continue;
+            const double cta_bytes = double(B) * 16.0 * double(K) / 2.0;
+            double t = w_bytes / kHbmBytesPerS;
+            if (cta_bytes / kCtaBytesPerS > t) t = cta_bytes / kCtaBytesPerS;
+            t += kWholeKSeconds + double(ctas) * M * K * 2.0 / kXBroadcastBytesPerS;
+            if (t < best * 0.999) {
+                best = t;
+                d->wk_blocks = B;
+                d->split_k = 1;
+                d->groups_per_slice = groups;
+                d->ctas_per_slice = int(ctas);
+            }
+        }
+        if (wk == 1) return;
+    }
     // Slices hold 1, 2, 4, 8 or 16 groups and divide K exactly (the kernel
     // unrolls a slice at compile time).  A forced split picks the feasible slice count
     // closest to the request from above.
@@ -145,6 +175,7 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, DecodePlan *d) 
                 d->split_k = sk;
                 d->groups_per_slice = gps;
                 d->ctas_per_slice = C;
+                d->wk_blocks = 0;
             }
         }
     }
@@ -229,7 +260,7 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                 // overlaps with the next tile (except the CTA's last one).
                 const double epi = sep ? 1500.0 : per_cta_tiles * 1500.0;
                 double time = (per_cta_tiles * conc * 2.0 * gps * kb + epi) / kClockHz;
-                if (sk > 1) time += 2.0 * sk * double(M) * N * 4.0 / kL2BytesPerS + kReduceSeconds;
+                if (sk > 1) time += 2.0 * sk * double(M) * N * 4.0 / kL2BytesPerS + kTensorReduceSeconds;
                 if (time < best * 0.999) {
                     best = time;
                     t->tile_tokens = bt;
@@ -257,7 +288,12 @@ w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p) 
     if (arm != W4A16_ARM_AUTO && arm != W4A16_ARM_DECODE && arm != W4A16_ARM_TENSOR)
         return W4A16_ERR_INVALID_ARG;
     if (opts && opts->split_k < 0) return W4A16_ERR_INVALID_ARG;
-    if (opts && (opts->flags & ~int(W4A16_FLAG_RESIDENT_WEIGHTS))) return W4A16_ERR_INVALID_ARG;
+    const int flags = opts ? opts->flags : 0;
+    if (flags & ~int(W4A16_FLAG_RESIDENT_WEIGHTS | W4A16_FLAG_DECODE_WHOLE_K | W4A16_FLAG_DECODE_K_SLICES))
+        return W4A16_ERR_INVALID_ARG;
+    if ((flags & W4A16_FLAG_DECODE_WHOLE_K) && (flags & W4A16_FLAG_DECODE_K_SLICES))
+        return W4A16_ERR_INVALID_ARG;
+    const int wk = (flags & W4A16_FLAG_DECODE_WHOLE_K) ? 1 : (flags & W4A16_FLAG_DECODE_K_SLICES) ? 2 : 0;
     const int forced_bt = opts ? opts->tile_tokens : 0;
     if (forced_bt != 0 && (forced_bt < 32 || forced_bt > 256 || forced_bt % 32))
         return W4A16_ERR_UNSUPPORTED;
@@ -268,11 +304,13 @@ w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p) 
     p->arm = arm;
     if (arm == W4A16_ARM_DECODE) {
         DecodePlan &d = p->decode;
-        plan_decode(M, N, K, sms, opts ? opts->split_k : 0, &d);
+        plan_decode(M, N, K, sms, opts ? opts->split_k : 0, wk, &d);
+        if (wk == 1 && d.wk_blocks == 0) return W4A16_ERR_UNSUPPORTED;
         p->split_k = d.split_k;
-        p->ctas = d.ctas_per_slice * d.split_k * d.token_blocks;
+        p->ctas = d.wk_blocks ? d.ctas_per_slice : d.ctas_per_slice * d.split_k * d.token_blocks;
         p->tile_tokens = 8 * d.mt;
     } else {
+        if (wk == 1) return W4A16_ERR_UNSUPPORTED;
         TensorPlan &t = p->tensor;
         w4a16_status st = plan_tensor(M, N, K, sms, opts ? opts->split_k : 0, forced_bt, 1, &t);
         if (st != W4A16_OK) return st;
@@ -330,6 +368,7 @@ w4a16_status w4a16_plan(int M, int N, int K, int group_size, const w4a16_options
         info->tile_tokens = p.tile_tokens;
         info->ctas = p.ctas;
         info->workspace_bytes = M == 0 ? 0 : p.ws_bytes;
+        info->whole_k = p.arm == W4A16_ARM_DECODE && p.decode.wk_blocks > 0;
     }
     return W4A16_OK;
 }
@@ -369,7 +408,10 @@ static w4a16_status gemm_impl(const w4a16_bf16 *X, const uint8_t *W_packed,
     float *ws = static_cast<float *>(workspace);
     cudaError_t e;
     const bool resident = opts && (opts->flags & W4A16_FLAG_RESIDENT_WEIGHTS);
-    if (p.arm == W4A16_ARM_DECODE)
+    if (p.arm == W4A16_ARM_DECODE && p.decode.wk_blocks > 0)
+        e = launch_decode_wk(p.decode.wk_blocks, p.decode.ctas_per_slice, X, W_packed, scales, Y,
+                             resident, M, N, K, s);
+    else if (p.arm == W4A16_ARM_DECODE)
         e = launch_decode(p.decode, X, W_packed, scales, Y, ws, resident, M, N, K, s);
     else
         e = launch_tensor(p.tensor, X, W_packed, scales, Y, ws, nullptr, nullptr, 1, M, N, K, s);

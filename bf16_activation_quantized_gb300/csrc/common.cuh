@@ -145,6 +145,15 @@ __device__ __forceinline__ void mma_16816_f16_c(float (&d)[4], const uint32_t (&
           "f"(c[2]), "f"(c[3]));
 }
 
+// In place: c += A.B.
+__device__ __forceinline__ void mma_16816_f16_acc(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                  uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ uint4 ldg_nc16(const void *p) {
     uint4 r;
     asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -16,6 +16,8 @@ struct DecodePlan {
     int groups_per_slice; // 128-wide K groups per slice (<= kDecodeMaxGps)
     int ring;             // weight-ring stages to use (capped by shared memory)
     int in_flight;        // bulk copies a CTA keeps in the air (<= ring)
+    int wk_blocks;        // > 0: whole-K kernel, each CTA owns this many 16-row blocks over all
+                          // of K (split_k is 1, ctas_per_slice the grid); 0: the slice kernel
 };
 
 struct TensorPlan {
@@ -41,6 +43,11 @@ int *device_error_word();        // device address of the error word (nullptr on
 constexpr int kDecodeMaxGps = 16;
 constexpr int kDecodeMaxSmem = 113 * 1024;
 int decode_smem_needed(int M, int mt, int groups_per_slice);
+// Whole-K decode kernel: whether M tokens of K fit its staging, and its launch.
+bool decode_wk_fits(int M, int K, int blocks_per_cta);
+cudaError_t launch_decode_wk(int blocks_per_cta, int ctas, const uint16_t *X, const uint8_t *Wp,
+                             const uint16_t *S, uint16_t *Y, bool resident, int M, int N, int K,
+                             cudaStream_t s);
 
 size_t packed_bytes(int N, int K);
 

@@ -68,7 +68,17 @@ enum {
      * the flag nothing is read before it has completed.  Do not set it when
      * W_packed or scales alias the output or workspace of a call just before
      * on the same stream. */
-    W4A16_FLAG_RESIDENT_WEIGHTS = 1
+    W4A16_FLAG_RESIDENT_WEIGHTS = 1,
+    /* Decode-arm kernel choice (for tests and tuning; by default the
+     * dispatcher chooses).  WHOLE_K: the kernel in which every CTA covers all
+     * of K for a few 16-row blocks of W, its warps split K among themselves
+     * and add their partial sums in shared memory, so K is never split across
+     * CTAs (no workspace, no reduce kernel); it takes up to 8 tokens whose X
+     * rows fit its shared-memory staging (M * K <= 16384), otherwise the call
+     * returns W4A16_ERR_UNSUPPORTED.  K_SLICES: never that kernel.  Setting
+     * both is W4A16_ERR_INVALID_ARG. */
+    W4A16_FLAG_DECODE_WHOLE_K = 2,
+    W4A16_FLAG_DECODE_K_SLICES = 4
 };
 
 /* Overrides for tests and tuning.  Zero-initialised = automatic. */
@@ -89,6 +99,7 @@ typedef struct {
     int tile_tokens;      /* tokens per tile (decode arm: 8 or 16 per pass) */
     int ctas;             /* CTAs in the main launch */
     size_t workspace_bytes;
+    int whole_k;          /* 1: the decode arm's whole-K kernel (see W4A16_FLAG_DECODE_WHOLE_K) */
 } w4a16_plan_info;
 
 /* Human-readable name of a status code (static string, never NULL). */

@@ -129,7 +129,8 @@ def test_plan_without_a_gpu_reports_cuda_error(L):
 def test_options_are_checked_before_the_device_is_queried(L):
     # Unknown flag bits, bad arms and bad tile sizes are host-side errors.
     info = _lib.PlanInfo()
-    for o, want in ((_lib.Options(0, 0, 0, 2), INVALID), (_lib.Options(0, 0, 0, 1 << 30), INVALID),
+    for o, want in ((_lib.Options(0, 0, 0, 8), INVALID), (_lib.Options(0, 0, 0, 1 << 30), INVALID),
+                    (_lib.Options(0, 0, 0, 2 | 4), INVALID),
                     (_lib.Options(7, 0, 0, 0), INVALID), (_lib.Options(0, -1, 0, 0), INVALID),
                     (_lib.Options(2, 0, 48, 0), UNSUPPORTED)):
         assert L.w4a16_plan(1, 256, 512, 128, ctypes.byref(o), ctypes.byref(info)) == want
@@ -138,5 +139,6 @@ def test_options_are_checked_before_the_device_is_queried(L):
 def test_header_flag_values_match_the_binding():
     import bf16_activation_quantized_gb300 as w4
     text = open(HEADER).read()
-    assert re.search(r"W4A16_FLAG_RESIDENT_WEIGHTS\s*=\s*1\b", text)
-    assert w4.FLAG_RESIDENT_WEIGHTS == 1
+    for name, value in (("RESIDENT_WEIGHTS", 1), ("DECODE_WHOLE_K", 2), ("DECODE_K_SLICES", 4)):
+        assert re.search(rf"W4A16_FLAG_{name}\s*=\s*{value}\b", text)
+        assert getattr(w4, f"FLAG_{name}") == value

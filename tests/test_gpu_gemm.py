@@ -94,8 +94,8 @@ def test_prefill_sampled_features(M, N, K):
 def test_decode_arm_every_split(M, split_k):
     N, K = 300, 640        # 3 tiles with a ragged last tile, 5 groups
     p = problem(M, N, K, seed=M)
-    y = run(p, arm="decode", split_k=split_k)
-    plan = w4.plan(M, N, K, arm="decode", split_k=split_k)
+    y = run(p, arm="decode", split_k=split_k, decode_kernel="k_slices")
+    plan = w4.plan(M, N, K, arm="decode", split_k=split_k, decode_kernel="k_slices")
     # 5 groups: every slice holds one group, whatever split is requested
     assert plan["split_k"] == 5
     assert_close(bf16_to_f64(y), reference(p), what=f"decode M{M} SK{split_k}")
@@ -106,8 +106,8 @@ def test_decode_arm_every_split(M, split_k):
 def test_decode_arm_slice_sizes(M, split_k):
     N, K = 300, 1024       # 8 groups: slices of 8, 4, 2 and 1 groups
     p = problem(M, N, K, seed=M + 100)
-    y = run(p, arm="decode", split_k=split_k)
-    assert w4.plan(M, N, K, arm="decode", split_k=split_k)["split_k"] == split_k
+    y = run(p, arm="decode", split_k=split_k, decode_kernel="k_slices")
+    assert w4.plan(M, N, K, arm="decode", split_k=split_k, decode_kernel="k_slices")["split_k"] == split_k
     assert_close(bf16_to_f64(y), reference(p), what=f"decode M{M} SK{split_k}")
 
 
@@ -115,8 +115,8 @@ def test_decode_arm_slice_sizes(M, split_k):
 def test_decode_arm_sixteen_group_slices(M):
     N, K = 300, 2048       # 16 groups: one 16-group slice for up to 8 tokens, else two of 8
     p = problem(M, N, K, seed=M + 200)
-    y = run(p, arm="decode", split_k=1)
-    assert w4.plan(M, N, K, arm="decode", split_k=1)["split_k"] == (1 if M <= 8 else 2)
+    y = run(p, arm="decode", split_k=1, decode_kernel="k_slices")
+    assert w4.plan(M, N, K, arm="decode", split_k=1, decode_kernel="k_slices")["split_k"] == (1 if M <= 8 else 2)
     assert_close(bf16_to_f64(y), reference(p), what=f"decode M{M} one slice")
 
 
@@ -124,7 +124,7 @@ def test_decode_arm_sixteen_group_slices(M):
 @pytest.mark.parametrize("split_k", [1, 4, 16])
 def test_decode_arm_splits_on_workload_shapes(M, N, K, split_k):
     p = problem(M, N, K)
-    y = run(p, arm="decode", split_k=split_k)
+    y = run(p, arm="decode", split_k=split_k, decode_kernel="k_slices")
     assert_close(bf16_to_f64(y), reference(p), what=f"decode M{M} N{N} K{K} SK{split_k}")
 
 
@@ -270,7 +270,7 @@ def test_cuda_graph_replay_matches_eager(M, N, K):
 
 
 def test_workspace_too_small_is_rejected_before_launch():
-    M, N, K = 1, 8192, 8192
+    M, N, K = 16, 2560, 9728         # a split-K plan: it needs a workspace
     p = problem(M, N, K)
     need = w4.plan(M, N, K)["workspace_bytes"]
     assert need > 0
@@ -371,3 +371,63 @@ def test_resident_weights_chain_reads_x_after_the_previous_call():
     last = layers[-1].inp
     ref = oracle.gemm(xin, last.w_canon, last.scales, 1, K, K)
     assert_close(bf16_to_f64(outs[-1]), ref, what="chain")
+
+
+# ------------------------------------------------------ whole-K decode kernel
+WHOLE_K = [(1, 8192, 8192), (1, 17408, 5120), (1, 19456, 2560), (1, 2560, 9728), (2, 8192, 8192),
+           (4, 4096, 4096), (8, 2048, 2048), (3, 300, 640), (1, 7, 256), (5, 129, 384), (1, 256, 128)]
+
+
+@pytest.mark.parametrize("M,N,K", WHOLE_K)
+def test_whole_k_kernel_full_output(M, N, K):
+    # Every CTA covers all of K for a few 16-row blocks; its warps split K and
+    # add their parts in shared memory.
+    p = problem(M, N, K)
+    pl = w4.plan(M, N, K, arm="decode", decode_kernel="whole_k")
+    assert pl["whole_k"] and pl["split_k"] == 1 and pl["workspace_bytes"] == 0
+    y = run(p, arm="decode", decode_kernel="whole_k")
+    assert_close(bf16_to_f64(y), reference(p), what=f"whole-K M{M} N{N} K{K} {pl}")
+    again = run(p, arm="decode", decode_kernel="whole_k", resident_weights=True)
+    assert np.array_equal(bf16_to_u16(again), bf16_to_u16(y))
+
+
+def test_whole_k_kernel_refuses_what_it_cannot_stage():
+    # 16 tokens, or X rows beyond its staging (M * K > 16384), are refused when forced.
+    for M, N, K in ((16, 2560, 9728), (3, 8192, 8192)):
+        with pytest.raises(w4.W4A16Error):
+            w4.plan(M, N, K, arm="decode", decode_kernel="whole_k")
+    assert not w4.plan(1, 8192, 8192, decode_kernel="k_slices")["whole_k"]
+
+
+def test_whole_k_kernel_in_a_graph_replays_exactly():
+    M, N, K = 1, 8192, 8192
+    p = problem(M, N, K)
+    eager = bf16_to_u16(run(p, arm="decode", decode_kernel="whole_k"))
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        w4.gemm(p.x, p.w_packed, p.scales, out=out, arm="decode", decode_kernel="whole_k")
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(3):
+            w4.gemm(p.x, p.w_packed, p.scales, out=out, arm="decode", decode_kernel="whole_k",
+                    resident_weights=True)
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(bf16_to_u16(out), eager)
+
+
+def test_whole_k_all_eights_give_near_zero():
+    # All codes 8: every weight is 0; the fp32 offset cancellation leaves a
+    # residue far below the output scale (as in the sliced kernel).
+    M, N, K = 1, 1024, 4096
+    inp = syn.make_gemm_inputs(M, N, K, seed=3)
+    inp.w_canon[:] = 0x88
+    p = DeviceProblem(inp)
+    y = bf16_to_f64(run(p, arm="decode", decode_kernel="whole_k"))
+    x = np.abs(bf16_to_f64(p.x)).sum()
+    assert np.all(np.abs(y) <= 1152 * x * 0.02 * 2.0 ** -18)
