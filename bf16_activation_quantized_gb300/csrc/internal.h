@@ -25,7 +25,7 @@ struct TensorPlan {
     int split_k;          // K slices
     int groups_per_slice;
     int n_tiles;          // 128-row feature tiles
-    int t_tiles;          // token tiles (per group for the grouped op: an upper bound)
+    int t_tiles;          // token tiles (grouped op: the planning estimate; the kernel counts them)
     int ctas;             // persistent CTAs launched
     int x_stages;         // X ring depth (groups of X in shared memory)
     int w_stages;         // W ring depth (groups of packed weights in shared memory)
