@@ -62,6 +62,7 @@ constexpr int kDecodeMaxM = 16;               // auto dispatch: M <= 16 -> decod
 constexpr double kClockHz = 1.9e9;            // planning clock
 constexpr int kTensorMaxWStages = 8;
 constexpr double kTcChainClk = 500.0;         // one CTA's per-K-block dependency chain
+constexpr double kTcSmallTileKbClk = 800.0;   // per-SM cycles per K block, tiles <= 128 tokens
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -261,7 +262,15 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                 const int conc = int(ceil_div(ctas, sms));
                 const double kb_tp = std::max(std::max(2.0 * bt, 150.0),
                                               kChunkBytes / 22.0 + bt * 128.0 / 64.0);
-                const double kb = std::max(kb_tp, kTcChainClk / conc);
+                // A grid that fills the SMs without a split, with tiles of up to
+                // 128 tokens or few tokens in all: measured on GB300, an SM then
+                // spends about kTcSmallTileKbClk per K block whatever the tile
+                // width and whether one or two CTAs share it, so wider tiles
+                // buy nothing and splitting K only adds the reduce.  (Wide
+                // tiles of many tokens, the prefill case, keep the model above.)
+                const bool full = (long long)t->n_tiles * t_tiles >= sms;
+                const double floor_kb = (full && (bt <= 128 || M <= 256)) ? kTcSmallTileKbClk : 0.0;
+                const double kb = std::max(std::max(kb_tp, kTcChainClk / conc), floor_kb);
                 const double per_cta_tiles = double(ceil_div(tiles, ctas));
                 // Per-tile fixed cost: the epilogue, which a separate epilogue
                 // overlaps with the next tile (except the CTA's last one).
