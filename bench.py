@@ -452,7 +452,41 @@ def per_shape_table(torch, w4, syn, metrics, device, peaks, only=None):
         torch.cuda.empty_cache()
     if only is None:
         rows.append(grouped_row(torch, w4, syn, metrics, device, peaks))
+        for B, M, N, K in BATCHED_SHAPES:
+            rows.append(batched_row(torch, w4, syn, metrics, device, peaks, B, M, N, K))
     return rows
+
+
+# The batched op's report rows: the shapes of the pages' batched table (B
+# independent products of one shape, one launch).
+BATCHED_SHAPES = [(4, 128, 8192, 3584), (2, 2048, 7168, 8192)]
+
+
+def batched_row(torch, w4, syn, metrics, device, peaks, B, M, N, K):
+    inps = [syn.make_gemm_inputs(M, N, K, seed=b) for b in range(B)]
+    bits = lambda a: torch.from_numpy(a.view("int16").copy()).view(torch.bfloat16).to(device)
+    x = torch.stack([bits(i.x) for i in inps])
+    s = torch.stack([bits(i.scales) for i in inps])
+    w = torch.stack([w4.pack(torch.from_numpy(i.w_canon.copy()).to(device)) for i in inps])
+    y = torch.empty((B, M, N), dtype=torch.bfloat16, device=device)
+    C = copies_for(torch, device, B * metrics.weight_bytes(N, K))
+    ws = [w] + [w.clone() for _ in range(C - 1)]
+    plan = w4.plan_batched(B, M, N, K)
+    R = max(C, (20 // C) * C)
+    g = capture(torch, lambda i: w4.gemm_batched(x, ws[i % C], s, out=y, resident_weights=True), R)
+    g.replay()
+    t = statistics.median(time_graph(torch, g) for _ in range(3)) / R
+    nbytes = B * metrics.algorithmic_bytes(M, N, K)
+    fl = B * metrics.flops(M, N, K)
+    t_roof = metrics.roofline_seconds(fl, nbytes, peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
+    row = {"workload": "batched", "batch": B, "M": M, "N": N, "K": K,
+           "us": round(t * 1e6, 3), "tflops": round(fl / t / 1e12, 3), "gbs": round(nbytes / t / 1e9, 1),
+           "roofline_frac": round(t_roof / t, 4),
+           "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) >= fl / (peaks["bf16_tflops"] * 1e12) else "tensor",
+           "arm": plan["arm"], "split_k": plan["split_k"], "copies": C}
+    del g, ws
+    torch.cuda.empty_cache()
+    return row
 
 
 def grouped_row(torch, w4, syn, metrics, device, peaks):

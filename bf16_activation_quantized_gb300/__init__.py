@@ -23,7 +23,7 @@ GROUP = 128
 ARM_AUTO, ARM_DECODE, ARM_TENSOR = 0, 1, 2
 _ARMS = {None: ARM_AUTO, "auto": ARM_AUTO, "decode": ARM_DECODE, "tensor": ARM_TENSOR}
 
-__all__ = ["GROUP", "pack", "gemm", "gemm_partials", "gemm_grouped", "dequant_fp32", "dequant_bf16",
+__all__ = ["GROUP", "pack", "gemm", "gemm_partials", "gemm_grouped", "gemm_batched", "plan_batched", "dequant_fp32", "dequant_bf16",
            "splitk_reduce", "plan", "packed_weight_bytes", "layout_version", "W4A16Error"]
 
 
@@ -194,6 +194,57 @@ def gemm_partials(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor,
             workspace.data_ptr(), workspace.numel() * workspace.element_size(), ctypes.byref(o),
             ctypes.byref(sk), _stream_ptr(x.device)), "w4a16_gemm_partials")
     return int(sk.value)
+
+
+def plan_batched(batch: int, M: int, N: int, K: int, arm=None, split_k: int = 0,
+                 tile_tokens: int = 0, device=None, decode_kernel=None) -> dict:
+    """What the dispatcher picks for a batch of ``batch`` products of shape (M, N, K)."""
+    info = PlanInfo()
+    o = _opts(arm, split_k, tile_tokens, decode_kernel=decode_kernel)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _lib.check(_lib.lib().w4a16_plan_batched(batch, M, N, K, GROUP, ctypes.byref(o),
+                                                 ctypes.byref(info)), "w4a16_plan_batched")
+    return {"arm": {1: "decode", 2: "tensor"}.get(info.arm, info.arm), "split_k": info.split_k,
+            "tile_tokens": info.tile_tokens, "ctas": info.ctas,
+            "workspace_bytes": int(info.workspace_bytes), "whole_k": bool(info.whole_k)}
+
+
+def gemm_batched(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=None,
+                 split_k: int = 0, tile_tokens: int = 0, out: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None, resident_weights: bool = False,
+                 decode_kernel=None) -> torch.Tensor:
+    """Y[b] = X[b] . dequant(W[b])^T for every b in one launch.
+
+    x: bf16 [B, M, K]; w_packed: uint8 [B, packed_weight_bytes(N, K)] (or the same
+    bytes flat); scales: bf16 [B, N, K/128]; returns bf16 [B, M, N]."""
+    _need_cuda(x, "x", torch.bfloat16)
+    _need_cuda(scales, "scales", torch.bfloat16)
+    _need_cuda(w_packed, "w_packed", torch.uint8)
+    if x.dim() != 3 or scales.dim() != 3:
+        raise ValueError("x must be [B, M, K] and scales [B, N, K/128]")
+    B, M, K = x.shape
+    N = scales.shape[1]
+    if scales.shape[0] != B or scales.shape[2] * GROUP != K:
+        raise ValueError("scales must be [B, N, K/128]")
+    if w_packed.numel() < B * packed_weight_bytes(N, K):
+        raise ValueError("w_packed is smaller than B * packed_weight_bytes(N, K)")
+    if out is None:
+        out = torch.empty((B, M, N), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need_cuda(out, "out", torch.bfloat16)
+    o = _opts(arm, split_k, tile_tokens, resident_weights, decode_kernel)
+    with torch.cuda.device(x.device):
+        info = PlanInfo()
+        _lib.check(_lib.lib().w4a16_plan_batched(B, M, N, K, GROUP, ctypes.byref(o), ctypes.byref(info)),
+                   "w4a16_plan_batched")
+        need = int(info.workspace_bytes)
+        ws = workspace if workspace is not None else (_workspace(x.device, need) if need else None)
+        _lib.check(_lib.lib().w4a16_gemm_batched(
+            x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), out.data_ptr(), B, M, N, K, GROUP,
+            ws.data_ptr() if ws is not None else None,
+            ws.numel() * ws.element_size() if ws is not None else 0, ctypes.byref(o),
+            _stream_ptr(x.device)), "w4a16_gemm_batched")
+    return out
 
 
 def gemm_grouped(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor,

@@ -107,13 +107,17 @@ double decode_slice_preference(int gps) {
 // Whole-K plans (no split-K) compete with the sliced ones: each CTA owns
 // B 16-row blocks over all of K, 8 / B K-parts per CTA; one CTA per B blocks,
 // all resident at once.  wk: 0 = either kernel, 1 = whole-K only, 2 = slices only.
-void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, DecodePlan *d) {
+// batch > 1: that many independent products of this shape share the GPU
+// (each gets its share of the CTA slots; the weight stream is all of theirs).
+void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int batch, DecodePlan *d) {
     const int groups = K / kGroup;
     d->mt = M <= 8 ? 1 : 2;
     d->token_blocks = ceil_div(M, 8 * d->mt);
     d->n_tiles = ceil_div(N, kTileRows);
-    const long long slots = (long long)kDecodeCtasPerSm * sms;
-    const double w_bytes = double(d->n_tiles) * kTileRows * double(K) / 2.0;
+    d->batch = batch;
+    long long slots = (long long)kDecodeCtasPerSm * sms / batch;
+    if (slots < 1) slots = 1;
+    const double w_bytes = double(batch) * d->n_tiles * kTileRows * double(K) / 2.0;
     double best = 1e30;
     d->split_k = groups;
     d->groups_per_slice = 1;
@@ -126,11 +130,11 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, DecodeP
         for (int B : {8, 4, 2}) {
             if (!decode_wk_fits(M, K, B)) continue;
             const long long ctas = (long long)d->n_tiles * (kTileRows / 16) / B;
-            if (ctas > slots) continue;
+            if (ctas > slots) continue;   // per entry
             const double cta_bytes = double(B) * 16.0 * double(K) / 2.0;
             double t = w_bytes / kHbmBytesPerS;
             if (cta_bytes / kCtaBytesPerS > t) t = cta_bytes / kCtaBytesPerS;
-            t += kWholeKSeconds + double(ctas) * M * K * 2.0 / kXBroadcastBytesPerS;
+            t += kWholeKSeconds + double(ctas) * batch * M * K * 2.0 / kXBroadcastBytesPerS;
             if (t < best * 0.999) {
                 best = t;
                 d->wk_blocks = B;
@@ -218,14 +222,19 @@ bool tensor_rings(int bt, int num_groups, int occupancy, bool sep, int *x_stages
 // weight bytes at its HBM share + activation bytes at its L2 share), and a
 // CTA cannot go faster than its dependency chain (kTcChainClk per K block),
 // which a second resident CTA hides.
+// batch_rows > 0: a batched product, num_groups entries of batch_rows rows
+// (M = their total): the plain product per entry, split-K allowed.
 w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int forced_bt,
-                         int num_groups, TensorPlan *t) {
+                         int num_groups, TensorPlan *t, int batch_rows) {
     const int groups = K / kGroup;
+    const bool grouped = num_groups > 1 && batch_rows == 0;
     t->n_tiles = ceil_div(N, kTileRows);
     double best = 1e30;
     int found = 0;
     for (int bt = 32; bt <= 256; bt += 32) {
         if (forced_bt > 0 && bt != forced_bt) continue;
+        // a batched entry's tile wider than the entry is all padding
+        if (forced_bt == 0 && batch_rows > 0 && bt >= batch_rows + 32) continue;
         for (int variant = 0; variant < 3; ++variant) {
             // occupancy 2; occupancy 1; occupancy 1 with a separate epilogue
             const int occ = variant == 0 ? 2 : 1;
@@ -233,11 +242,11 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
             if (tensor_a_stages(bt, occ, sep) < 2) continue;  // TMEM share too small
             int sx = 0, sw = 0;
             if (!tensor_rings(bt, num_groups, occ, sep, &sx, &sw)) continue;
-            const int max_sk = num_groups > 1 ? 1 : (groups < 16 ? groups : 16);
+            const int max_sk = grouped ? 1 : (groups < 16 ? groups : 16);
             for (int sk_req = 1; sk_req <= max_sk; ++sk_req) {
                 int sk = sk_req;
                 if (forced_split > 0) sk = forced_split > groups ? groups : forced_split;
-                if (num_groups > 1) sk = 1;
+                if (grouped) sk = 1;
                 const int gps = ceil_div(groups, sk);
                 sk = ceil_div(groups, gps);
                 // Grouped: the sizes live on the device; plan with the average
@@ -247,9 +256,8 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                 // K=4096): 128-token tiles 63 us, 256-token tiles 87 us.
                 const double rows_per_unit = double(M) / num_groups;
                 const long long t_tiles =
-                    num_groups == 1
-                        ? (long long)ceil_div((long long)M, bt)
-                        : (long long)std::ceil(num_groups * (rows_per_unit / bt + 0.5));
+                    !grouped ? (long long)num_groups * ceil_div((long long)M / num_groups, bt)
+                             : (long long)std::ceil(num_groups * (rows_per_unit / bt + 0.5));
                 const long long tiles = (long long)t->n_tiles * t_tiles * sk;
                 // A grid that fits one CTA per SM gains nothing from a second
                 // CTA slot but shallower rings, and the slot lets the block
@@ -269,7 +277,8 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                 // buy nothing and splitting K only adds the reduce.  (Wide
                 // tiles of many tokens, the prefill case, keep the model above.)
                 const bool full = (long long)t->n_tiles * t_tiles >= sms;
-                const double floor_kb = (full && (bt <= 128 || M <= 256)) ? kTcSmallTileKbClk : 0.0;
+                const int rows_entry = batch_rows > 0 ? batch_rows : M;   // tokens of one product
+                const double floor_kb = (full && (bt <= 128 || rows_entry <= 256)) ? kTcSmallTileKbClk : 0.0;
                 const double kb = std::max(std::max(kb_tp, kTcChainClk / conc), floor_kb);
                 const double per_cta_tiles = double(ceil_div(tiles, ctas));
                 // Per-tile fixed cost: the epilogue, which a separate epilogue
@@ -291,14 +300,15 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                     t->smem_bytes = tensor_smem_bytes(bt, sx, sw, occ, num_groups, sep);
                     found = 1;
                 }
-                if (forced_split > 0 || num_groups > 1) break;
+                if (forced_split > 0 || grouped) break;
             }
         }
     }
     return found ? W4A16_OK : W4A16_ERR_UNSUPPORTED;
 }
 
-w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p) {
+// batch: independent products of this shape in one launch (1: a plain call).
+w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, int batch = 1) {
     std::memset(p, 0, sizeof *p);
     int arm = opts ? opts->arm : W4A16_ARM_AUTO;
     if (arm != W4A16_ARM_AUTO && arm != W4A16_ARM_DECODE && arm != W4A16_ARM_TENSOR)
@@ -320,21 +330,24 @@ w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p) 
     p->arm = arm;
     if (arm == W4A16_ARM_DECODE) {
         DecodePlan &d = p->decode;
-        plan_decode(M, N, K, sms, opts ? opts->split_k : 0, wk, &d);
+        plan_decode(M, N, K, sms, opts ? opts->split_k : 0, wk, batch, &d);
         if (wk == 1 && d.wk_blocks == 0) return W4A16_ERR_UNSUPPORTED;
         p->split_k = d.split_k;
-        p->ctas = d.wk_blocks ? d.ctas_per_slice : d.ctas_per_slice * d.split_k * d.token_blocks;
+        p->ctas = batch * (d.wk_blocks ? d.ctas_per_slice : d.ctas_per_slice * d.split_k * d.token_blocks);
         p->tile_tokens = 8 * d.mt;
     } else {
         if (wk == 1) return W4A16_ERR_UNSUPPORTED;
         TensorPlan &t = p->tensor;
-        w4a16_status st = plan_tensor(M, N, K, sms, opts ? opts->split_k : 0, forced_bt, 1, &t);
+        w4a16_status st = plan_tensor(batch * M, N, K, sms, opts ? opts->split_k : 0, forced_bt,
+                                      batch, &t, batch > 1 ? M : 0);
         if (st != W4A16_OK) return st;
         p->split_k = t.split_k;
         p->ctas = t.ctas;
         p->tile_tokens = t.tile_tokens;
     }
-    p->ws_bytes = p->split_k > 1 ? size_t(p->split_k) * size_t(M) * size_t(N) * sizeof(float) : 0;
+    p->ws_bytes = p->split_k > 1
+                      ? size_t(p->split_k) * size_t(batch) * size_t(M) * size_t(N) * sizeof(float)
+                      : 0;
     return W4A16_OK;
 }
 
@@ -402,9 +415,10 @@ static w4a16_status gemm_impl(const w4a16_bf16 *X, const uint8_t *W_packed,
                               const w4a16_bf16 *scales, w4a16_bf16 *Y, int M, int N, int K,
                               int group_size, void *workspace, size_t workspace_bytes,
                               const w4a16_options *opts, bool with_reduce, int *split_out,
-                              void *stream) {
+                              void *stream, int batch = 1) {
     w4a16_status st = check_shape(M, N, K, group_size);
     if (st != W4A16_OK) return st;
+    if (batch < 1 || batch > kMaxGroups || (long long)batch * M > (1 << 24)) return W4A16_ERR_INVALID_ARG;
     if (M == 0) {
         if (split_out) *split_out = 1;
         return W4A16_OK;
@@ -413,7 +427,7 @@ static w4a16_status gemm_impl(const w4a16_bf16 *X, const uint8_t *W_packed,
     if (!aligned(X, 16) || !aligned(W_packed, 16) || !aligned(scales, 2) || !aligned(Y, 2))
         return W4A16_ERR_INVALID_ARG;
     Plan p;
-    st = plan_call(M, N, K, opts, &p);
+    st = plan_call(M, N, K, opts, &p, batch);
     if (st != W4A16_OK) return st;
     if (split_out) *split_out = p.split_k;
     if (p.ws_bytes > 0) {
@@ -425,15 +439,16 @@ static w4a16_status gemm_impl(const w4a16_bf16 *X, const uint8_t *W_packed,
     cudaError_t e;
     const bool resident = opts && (opts->flags & W4A16_FLAG_RESIDENT_WEIGHTS);
     if (p.arm == W4A16_ARM_DECODE && p.decode.wk_blocks > 0)
-        e = launch_decode_wk(p.decode.wk_blocks, p.decode.ctas_per_slice, X, W_packed, scales, Y,
-                             resident, M, N, K, s);
+        e = launch_decode_wk(p.decode.wk_blocks, p.decode.ctas_per_slice, batch, X, W_packed, scales,
+                             Y, resident, M, N, K, s);
     else if (p.arm == W4A16_ARM_DECODE)
         e = launch_decode(p.decode, X, W_packed, scales, Y, ws, resident, M, N, K, s);
     else
-        e = launch_tensor(p.tensor, X, W_packed, scales, Y, ws, nullptr, nullptr, 1, M, N, K, s);
+        e = launch_tensor(p.tensor, X, W_packed, scales, Y, ws, nullptr, nullptr, batch, batch * M, N,
+                          K, s, batch > 1 ? M : 0);
     if (e != cudaSuccess) return W4A16_ERR_CUDA;
     if (with_reduce && p.split_k > 1) {
-        e = launch_reduce(ws, Y, p.split_k, (long long)M * N, true, s);
+        e = launch_reduce(ws, Y, p.split_k, (long long)batch * M * N, true, s);
         if (e != cudaSuccess) return W4A16_ERR_CUDA;
     }
     return W4A16_OK;
@@ -460,6 +475,33 @@ w4a16_status w4a16_gemm(const w4a16_bf16 *X, const uint8_t *W_packed, const w4a1
                         size_t workspace_bytes, void *stream) {
     return w4a16_gemm_ex(X, W_packed, scales, Y, M, N, K, group_size, workspace, workspace_bytes,
                          nullptr, stream);
+}
+
+w4a16_status w4a16_plan_batched(int batch, int M, int N, int K, int group_size,
+                                const w4a16_options *opts, w4a16_plan_info *info) {
+    w4a16_status st = check_shape(M, N, K, group_size);
+    if (st != W4A16_OK) return st;
+    if (batch < 1 || batch > kMaxGroups || (long long)batch * M > (1 << 24)) return W4A16_ERR_INVALID_ARG;
+    Plan p;
+    st = plan_call(M, N, K, opts, &p, batch);
+    if (st != W4A16_OK) return st;
+    if (info) {
+        info->arm = p.arm;
+        info->split_k = p.split_k;
+        info->tile_tokens = p.tile_tokens;
+        info->ctas = p.ctas;
+        info->workspace_bytes = M == 0 ? 0 : p.ws_bytes;
+        info->whole_k = p.arm == W4A16_ARM_DECODE && p.decode.wk_blocks > 0;
+    }
+    return W4A16_OK;
+}
+
+w4a16_status w4a16_gemm_batched(const w4a16_bf16 *X, const uint8_t *W_packed,
+                                const w4a16_bf16 *scales, w4a16_bf16 *Y, int batch, int M, int N,
+                                int K, int group_size, void *workspace, size_t workspace_bytes,
+                                const w4a16_options *opts, void *stream) {
+    return gemm_impl(X, W_packed, scales, Y, M, N, K, group_size, workspace, workspace_bytes, opts,
+                     true, nullptr, stream, batch);
 }
 
 w4a16_status w4a16_grouped_workspace_bytes(int num_groups, int M_total, int N, int K,
@@ -490,7 +532,7 @@ w4a16_status w4a16_gemm_grouped(const w4a16_bf16 *X, const uint8_t *W_packed,
     int sms = 0;
     if (device_sm_count(&sms) != 0 || sms < 1) return W4A16_ERR_CUDA;
     TensorPlan t;
-    st = plan_tensor(M_total, N, K, sms, 1, 0, num_groups, &t);
+    st = plan_tensor(M_total, N, K, sms, 1, 0, num_groups, &t, 0);
     if (st != W4A16_OK) return st;
     // Enough CTAs for any split of M_total into the groups: the tile count is
     // at most n_tiles * (ceil(M_total / bt) + num_groups).

@@ -193,14 +193,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
               const uint16_t *__restrict__ S, uint16_t *__restrict__ Y, float *__restrict__ ws,
               int M, int N, int K, int n_tiles, int ring_stages, int in_flight, int s_vec,
-              int resident, int *err) {
+              int resident, int token_blocks, int *err) {
     extern __shared__ __align__(128) unsigned char smem[];
+    // Batched products: grid.z = entries x token blocks; entry b's X, W,
+    // scales, Y and partial sums follow each other in memory.
+    const int bz = blockIdx.z / token_blocks;
+    const int zt = blockIdx.z - bz * token_blocks;
+    const int n_entries = gridDim.z / token_blocks;
+    X += size_t(bz) * M * K;
+    Wp += size_t(bz) * n_tiles * kTileRows * (K / 2);
+    S += size_t(bz) * N * (K / kGroup);
+    Y += size_t(bz) * M * N;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n_groups = K / kGroup;
     const int grp0 = blockIdx.y * GPS;
-    const int m0 = blockIdx.z * 8 * MT;
+    const int m0 = zt * 8 * MT;
     const int rows = min(8 * MT, M - m0);
     const int C = gridDim.x;
     const int c0 = blockIdx.x;
@@ -515,7 +524,7 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
                 if (m < M && f < N) {
                     const size_t off = size_t(m) * N + f;
                     if (kSplit)
-                        ws[size_t(blockIdx.y) * size_t(M) * N + off] = acc[o][r];
+                        ws[(size_t(blockIdx.y) * n_entries + bz) * size_t(M) * N + off] = acc[o][r];
                     else
                         Y[off] = f32_to_bf16_rn(acc[o][r]);
                 }
@@ -574,6 +583,16 @@ decode_wk_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
                  const uint16_t *__restrict__ S, uint16_t *__restrict__ Y, int M, int N, int K,
                  int resident, int s_vec, int *err) {
     constexpr int P = kDecodeWarps / B;
+    // Batched products: grid.y = entries; entry b's X, W, scales and Y follow
+    // each other in memory.
+    {
+        const size_t bz = blockIdx.y;
+        const size_t n_tiles = (size_t(N) + kTileRows - 1) / kTileRows;
+        X += bz * M * K;
+        Wp += bz * n_tiles * kTileRows * (K / 2);
+        S += bz * N * (K / kGroup);
+        Y += bz * M * N;
+    }
     constexpr int SG = B == 1 ? 4 : 8 / B;     // groups per stage (B * SG KB <= 8 KB)
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
@@ -973,7 +992,7 @@ cudaError_t launch_decode_t(const DecodePlan &p, const uint16_t *X, const uint8_
         }
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.ctas_per_slice, p.split_k, p.token_blocks);
+    cfg.gridDim = dim3(p.ctas_per_slice, p.split_k, p.token_blocks * p.batch);
     cfg.blockDim = dim3(kDecodeThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -986,7 +1005,7 @@ cudaError_t launch_decode_t(const DecodePlan &p, const uint16_t *X, const uint8_
     if (!err) return cudaErrorUnknown;
     const int s_vec = (reinterpret_cast<uintptr_t>(S) % (2 * GPS)) == 0;
     return cudaLaunchKernelEx(&cfg, kern, X, Wp, S, Y, ws, M, N, K, p.n_tiles, p.ring, p.in_flight,
-                              s_vec, int(resident), err);
+                              s_vec, int(resident), p.token_blocks, err);
 }
 
 template <int MT, bool kSplit>
@@ -1006,7 +1025,7 @@ cudaError_t launch_decode_gps(const DecodePlan &p, const uint16_t *X, const uint
 }
 
 template <int B>
-cudaError_t launch_wk_t(int ctas, const uint16_t *X, const uint8_t *Wp, const uint16_t *S,
+cudaError_t launch_wk_t(int ctas, int batch, const uint16_t *X, const uint8_t *Wp, const uint16_t *S,
                         uint16_t *Y, bool resident, int M, int N, int K, cudaStream_t s) {
     const int smem = wk_smem_layout(B, M, K).total;
     auto kern = decode_wk_kernel<B>;
@@ -1023,7 +1042,7 @@ cudaError_t launch_wk_t(int ctas, const uint16_t *X, const uint8_t *Wp, const ui
         }
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(ctas);
+    cfg.gridDim = dim3(ctas, batch);
     cfg.blockDim = dim3(kDecodeThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -1034,9 +1053,11 @@ cudaError_t launch_wk_t(int ctas, const uint16_t *X, const uint8_t *Wp, const ui
     cfg.numAttrs = 1;
     int *err = device_error_word();
     if (!err) return cudaErrorUnknown;
-    // 16-byte scale vectors: S and the row stride K / 128 * 2 bytes allow them
-    // for every CTA's first row (a multiple of 16 rows).
-    const int s_vec = (reinterpret_cast<uintptr_t>(S) % 16) == 0 && ((K / kGroup) * 16 * 2) % 16 == 0;
+    // 16-byte scale vectors: every CTA's first scale row (a multiple of 16
+    // rows) is 16-byte aligned when S is, and so is every batch entry's block
+    // when N * K / 128 * 2 bytes is a multiple of 16.
+    const int s_vec = (reinterpret_cast<uintptr_t>(S) % 16) == 0 &&
+                      (batch == 1 || (size_t(N) * (K / kGroup) * 2) % 16 == 0);
     return cudaLaunchKernelEx(&cfg, kern, X, Wp, S, Y, M, N, K, int(resident), s_vec, err);
 }
 
@@ -1050,6 +1071,7 @@ cudaError_t launch_decode(const DecodePlan &p, const uint16_t *X, const uint8_t 
                           const uint16_t *S, uint16_t *Y, float *ws, bool res, int M, int N, int K,
                           cudaStream_t s) {
     if (p.ring != kRing || p.in_flight < 1 || p.in_flight > p.ring) return cudaErrorInvalidValue;
+    if (p.batch < 1 || (long long)p.token_blocks * p.batch > 65535) return cudaErrorInvalidValue;
     if (p.groups_per_slice < 1 || p.groups_per_slice > kDecodeMaxGps || p.ctas_per_slice < 1 ||
         decode_smem_needed(M, p.mt, p.groups_per_slice) > kDecodeMaxSmem ||
         decode_smem_layout(p.mt, M < 8 * p.mt ? M : 8 * p.mt, p.groups_per_slice).stages < kRing)
@@ -1070,15 +1092,15 @@ bool decode_wk_fits(int M, int K, int B) {
     return wk_smem_layout(B, M, K).total <= kDecodeMaxSmem;
 }
 
-cudaError_t launch_decode_wk(int B, int ctas, const uint16_t *X, const uint8_t *Wp,
+cudaError_t launch_decode_wk(int B, int ctas, int batch, const uint16_t *X, const uint8_t *Wp,
                              const uint16_t *S, uint16_t *Y, bool resident, int M, int N, int K,
                              cudaStream_t s) {
-    if (!decode_wk_fits(M, K, B) || ctas < 1) return cudaErrorInvalidValue;
+    if (!decode_wk_fits(M, K, B) || ctas < 1 || batch < 1 || batch > 65535) return cudaErrorInvalidValue;
     switch (B) {
-        case 1: return launch_wk_t<1>(ctas, X, Wp, S, Y, resident, M, N, K, s);
-        case 2: return launch_wk_t<2>(ctas, X, Wp, S, Y, resident, M, N, K, s);
-        case 4: return launch_wk_t<4>(ctas, X, Wp, S, Y, resident, M, N, K, s);
-        case 8: return launch_wk_t<8>(ctas, X, Wp, S, Y, resident, M, N, K, s);
+        case 1: return launch_wk_t<1>(ctas, batch, X, Wp, S, Y, resident, M, N, K, s);
+        case 2: return launch_wk_t<2>(ctas, batch, X, Wp, S, Y, resident, M, N, K, s);
+        case 4: return launch_wk_t<4>(ctas, batch, X, Wp, S, Y, resident, M, N, K, s);
+        case 8: return launch_wk_t<8>(ctas, batch, X, Wp, S, Y, resident, M, N, K, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -18,6 +18,7 @@ struct DecodePlan {
     int in_flight;        // bulk copies a CTA keeps in the air (<= ring)
     int wk_blocks;        // > 0: whole-K kernel, each CTA owns this many 16-row blocks over all
                           // of K (split_k is 1, ctas_per_slice the grid); 0: the slice kernel
+    int batch;            // independent products of this shape (batched op; 1 otherwise)
 };
 
 struct TensorPlan {
@@ -45,7 +46,7 @@ constexpr int kDecodeMaxSmem = 113 * 1024;
 int decode_smem_needed(int M, int mt, int groups_per_slice);
 // Whole-K decode kernel: whether M tokens of K fit its staging, and its launch.
 bool decode_wk_fits(int M, int K, int blocks_per_cta);
-cudaError_t launch_decode_wk(int blocks_per_cta, int ctas, const uint16_t *X, const uint8_t *Wp,
+cudaError_t launch_decode_wk(int blocks_per_cta, int ctas, int batch, const uint16_t *X, const uint8_t *Wp,
                              const uint16_t *S, uint16_t *Y, bool resident, int M, int N, int K,
                              cudaStream_t s);
 
@@ -72,9 +73,12 @@ inline int tensor_smem_budget(int occupancy) {
 size_t tensor_smem_bytes(int bt, int x_stages, int w_stages, int occupancy, int num_groups, bool sep);
 int tensor_a_stages(int bt, int occupancy, bool sep);   // TMEM A ring depth (0: does not fit)
 int tensor_tmem_cols(int bt, int occupancy, bool sep);  // TMEM columns a CTA allocates
+// m_sizes != nullptr: grouped product; else num_groups > 1 is a batched
+// product of num_groups entries of batch_rows rows (M_total = their product).
 cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, const int32_t *m_sizes,
-                          int *status, int num_groups, int M_total, int N, int K, cudaStream_t s);
+                          int *status, int num_groups, int M_total, int N, int K, cudaStream_t s,
+                          int batch_rows = 0);
 
 cudaError_t launch_reduce(const float *ws, uint16_t *Y, int splits, long long count, bool pdl,
                           cudaStream_t s);

@@ -66,6 +66,7 @@ struct TcArgs {
     int *status;              // grouped status word (nullptr for the plain product)
     int *err;
     int M_total, N, K, num_groups;
+    int batch_rows;           // > 0: batched product, num_groups problems of batch_rows rows each
     int bt;                   // tokens per tile = MMA N (multiple of 32, <= 256)
     int n_tiles;              // 128-row weight tiles
     int split_k, gps;         // K slices and 128-wide groups per slice
@@ -109,20 +110,27 @@ struct TileInfo {
     int rows;         // valid rows (<= bt)
 };
 
-// Flattened tile order: feature tile fastest, then token tile, then slice
-// (plain) or group (grouped), so CTAs running together share X tiles in L2.
+// Flattened tile order: feature tile fastest, then token tile, then batch
+// entry and slice (plain and batched) or group (grouped), so CTAs running
+// together share X tiles in L2.  A batched product is the plain product of
+// each entry, entry b owning rows [b * batch_rows, (b + 1) * batch_rows) of
+// the stacked X and Y and weight / scale block b.
 __device__ __forceinline__ bool tc_tile(const TcArgs &a, const int *tab_tiles, const int *tab_rows,
                                         int id, TileInfo &ti) {
     if (a.m_sizes == nullptr) {
-        const int t_tiles = (a.M_total + a.bt - 1) / a.bt;
-        const int per_slice = t_tiles * a.n_tiles;
-        ti.group = 0;
+        const bool batched = a.batch_rows > 0;
+        const int rows_b = batched ? a.batch_rows : a.M_total;
+        const int t_tiles = (rows_b + a.bt - 1) / a.bt;
+        const int per_entry = t_tiles * a.n_tiles;
+        const int per_slice = per_entry * (batched ? a.num_groups : 1);
         ti.slice = id / per_slice;
-        const int r = id - ti.slice * per_slice;
+        int r = id - ti.slice * per_slice;
+        ti.group = r / per_entry;
+        r -= ti.group * per_entry;
         ti.tt = r / a.n_tiles;
         ti.ft = r - ti.tt * a.n_tiles;
-        ti.x_row0 = ti.tt * a.bt;
-        ti.rows = min(a.bt, a.M_total - ti.x_row0);
+        ti.x_row0 = ti.group * rows_b + ti.tt * a.bt;
+        ti.rows = min(a.bt, rows_b - ti.tt * a.bt);
         return ti.slice < a.split_k;
     }
     // binary search: largest g with tab_tiles[g] <= id
@@ -625,7 +633,8 @@ size_t tensor_smem_bytes(int bt, int x_stages, int w_stages, int occupancy, int 
 
 cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, const int32_t *m_sizes,
-                          int *status, int num_groups, int M_total, int N, int K, cudaStream_t s) {
+                          int *status, int num_groups, int M_total, int N, int K, cudaStream_t s,
+                          int batch_rows) {
     if (p.tile_tokens < 32 || p.tile_tokens > 256 || p.tile_tokens % 32 || p.x_stages < 2 ||
         p.w_stages < 2 ||
         p.ctas < 1 || num_groups < 1 || num_groups > kMaxGroups || p.occupancy < 1 ||
@@ -658,6 +667,9 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
     a.N = N;
     a.K = K;
     a.num_groups = num_groups;
+    a.batch_rows = m_sizes == nullptr && num_groups > 1 ? batch_rows : 0;
+    if (m_sizes == nullptr && num_groups > 1 && (batch_rows < 1 || (long long)batch_rows * num_groups != M_total))
+        return cudaErrorInvalidValue;
     a.bt = p.tile_tokens;
     a.n_tiles = p.n_tiles;
     a.split_k = p.split_k;

@@ -172,6 +172,28 @@ w4a16_status w4a16_gemm_partials(const w4a16_bf16 *X, const uint8_t *W_packed,
                                  int group_size, void *workspace, size_t workspace_bytes,
                                  const w4a16_options *opts, int *split_k_out, void *stream);
 
+/* Batched product ("Add Triton BF16xINT4 rowwise GEMM for ROCm gfx942/gfx950",
+ * "bf16i4bf16_shuffled_batched": B independent products of one shape in one
+ * launch): for b < batch, Y[b] = X[b] . dequant(W[b])^T.
+ *  X:        device bf16 [batch][M][K].      Y: device bf16 [batch][M][N].
+ *  W_packed: batch consecutive blocks, each w4a16_packed_weight_bytes(N, K).
+ *  scales:   device bf16 [batch][N][K/128].
+ *  workspace/workspace_bytes: at least the workspace_bytes w4a16_plan_batched
+ *            reports (split-K partials [SPLIT_K][batch][M][N]; 0 without a
+ *            split); contents need no initialisation.
+ *  opts:     as for w4a16_gemm_ex (may be NULL).
+ * The dispatcher plans the whole batch at once (the decode arm for M <= 16
+ * with the CTA slots shared among the entries, else the tensor arm walking
+ * every entry's tiles); each entry's result equals the product computed on its
+ * own within the GEMM tolerance.  1 <= batch <= 1024, batch * M <= 2^24;
+ * M == 0 launches nothing. */
+w4a16_status w4a16_plan_batched(int batch, int M, int N, int K, int group_size,
+                                const w4a16_options *opts, w4a16_plan_info *info);
+w4a16_status w4a16_gemm_batched(const w4a16_bf16 *X, const uint8_t *W_packed,
+                                const w4a16_bf16 *scales, w4a16_bf16 *Y, int batch, int M, int N,
+                                int K, int group_size, void *workspace, size_t workspace_bytes,
+                                const w4a16_options *opts, void *stream);
+
 /* Workspace bytes of a grouped call: 16 bytes holding the device status word
  * (see w4a16_gemm_grouped).  Host only. */
 w4a16_status w4a16_grouped_workspace_bytes(int num_groups, int M_total, int N, int K,

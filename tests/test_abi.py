@@ -142,3 +142,18 @@ def test_header_flag_values_match_the_binding():
     for name, value in (("RESIDENT_WEIGHTS", 1), ("DECODE_WHOLE_K", 2), ("DECODE_K_SLICES", 4)):
         assert re.search(rf"W4A16_FLAG_{name}\s*=\s*{value}\b", text)
         assert getattr(w4, f"FLAG_{name}") == value
+
+
+def test_batched_entry_points_check_arguments(L):
+    info = _lib.PlanInfo()
+    for batch in (0, -1, 1025):
+        assert L.w4a16_plan_batched(batch, 4, 256, 512, 128, None, ctypes.byref(info)) == INVALID
+    assert L.w4a16_plan_batched(2, 4, 256, 512, 64, None, ctypes.byref(info)) == UNSUPPORTED
+    assert L.w4a16_plan_batched(2, 4, 256, 500, 128, None, ctypes.byref(info)) == INVALID
+    # batch * M beyond 2^24 rows
+    assert L.w4a16_plan_batched(1024, 1 << 15, 256, 512, 128, None, ctypes.byref(info)) == INVALID
+    FAKE = 1 << 20
+    assert L.w4a16_gemm_batched(None, FAKE, FAKE, FAKE, 2, 4, 256, 512, 128, None, 0, None, None) == INVALID
+    assert L.w4a16_gemm_batched(FAKE, FAKE, FAKE, FAKE, 0, 4, 256, 512, 128, None, 0, None, None) == INVALID
+    # M == 0: nothing to do, nothing launched, no GPU needed
+    assert L.w4a16_gemm_batched(None, None, None, None, 2, 0, 256, 512, 128, None, 0, None, None) == OK
