@@ -66,7 +66,6 @@ struct TcArgs {
     int *status;              // grouped status word (nullptr for the plain product)
     int *err;
     int M_total, N, K, num_groups;
-    int batch_rows;           // > 0: batched product, num_groups problems of batch_rows rows each
     int bt;                   // tokens per tile = MMA N (multiple of 32, <= 256)
     int n_tiles;              // 128-row weight tiles
     int split_k, gps;         // K slices and 128-wide groups per slice
@@ -79,6 +78,10 @@ struct TcArgs {
     unsigned long long w_group_stride;  // bytes between groups' packed weights
     unsigned long long s_group_stride;  // elements between groups' scales
 };
+// Measured on GB300: growing TcArgs past 128 bytes (the kernel's parameters
+// then exceed 256 bytes with the tensor map) slowed the kernel by about 5 %;
+// new per-launch facts should be derived from these fields instead.
+static_assert(sizeof(TcArgs) == 128, "TcArgs size");
 
 // Shared memory: the X ring (per stage two X boxes, one per 64-column K block,
 // 1024-byte aligned, 128-byte swizzle), the W ring (8 KB of packed weights of a
@@ -110,19 +113,21 @@ struct TileInfo {
     int rows;         // valid rows (<= bt)
 };
 
-// Flattened tile order: feature tile fastest, then token tile, then batch
-// entry and slice (plain and batched) or group (grouped), so CTAs running
-// together share X tiles in L2.  A batched product is the plain product of
-// each entry, entry b owning rows [b * batch_rows, (b + 1) * batch_rows) of
-// the stacked X and Y and weight / scale block b.
+// Flattened tile order: feature tile fastest, then token tile, then slice
+// (plain) or group (grouped), so CTAs running together share X tiles in L2.
+// kBatched: a batched product, the plain product of each of num_groups
+// entries of M_total / num_groups rows, entry b owning rows [b * rows,
+// (b + 1) * rows) of the stacked X and Y and weight / scale block b; order:
+// feature tile, token tile, entry, slice.  (A separate instantiation: folding
+// it into the plain walk measurably slowed the plain kernel's loops.)
+template <bool kBatched>
 __device__ __forceinline__ bool tc_tile(const TcArgs &a, const int *tab_tiles, const int *tab_rows,
                                         int id, TileInfo &ti) {
-    if (a.m_sizes == nullptr) {
-        const bool batched = a.batch_rows > 0;
-        const int rows_b = batched ? a.batch_rows : a.M_total;
+    if constexpr (kBatched) {
+        const int rows_b = a.M_total / a.num_groups;
         const int t_tiles = (rows_b + a.bt - 1) / a.bt;
         const int per_entry = t_tiles * a.n_tiles;
-        const int per_slice = per_entry * (batched ? a.num_groups : 1);
+        const int per_slice = per_entry * a.num_groups;
         ti.slice = id / per_slice;
         int r = id - ti.slice * per_slice;
         ti.group = r / per_entry;
@@ -131,6 +136,18 @@ __device__ __forceinline__ bool tc_tile(const TcArgs &a, const int *tab_tiles, c
         ti.ft = r - ti.tt * a.n_tiles;
         ti.x_row0 = ti.group * rows_b + ti.tt * a.bt;
         ti.rows = min(a.bt, rows_b - ti.tt * a.bt);
+        return ti.slice < a.split_k;
+    }
+    if (a.m_sizes == nullptr) {
+        const int t_tiles = (a.M_total + a.bt - 1) / a.bt;
+        const int per_slice = t_tiles * a.n_tiles;
+        ti.group = 0;
+        ti.slice = id / per_slice;
+        const int r = id - ti.slice * per_slice;
+        ti.tt = r / a.n_tiles;
+        ti.ft = r - ti.tt * a.n_tiles;
+        ti.x_row0 = ti.tt * a.bt;
+        ti.rows = min(a.bt, a.M_total - ti.x_row0);
         return ti.slice < a.split_k;
     }
     // binary search: largest g with tab_tiles[g] <= id
@@ -229,7 +246,7 @@ __device__ __forceinline__ void tc_store_block(const TcArgs &a, const TileInfo &
     }
 }
 
-template <bool kSplit, bool kSep>
+template <bool kSplit, bool kSep, bool kBatched>
 __global__ void __launch_bounds__(kSep ? kTcThreadsSep : kTcThreads, kSep ? 1 : 2)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     extern __shared__ unsigned char smem_raw[];
@@ -321,8 +338,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             // either ring for kWaitLimitNs aborts the CTA.
             TileInfo tx, tw;
             int idx = blockIdx.x, idw = blockIdx.x;
-            bool x_more = tc_tile(a, tab_tiles, tab_rows, idx, tx);
-            bool w_more = tc_tile(a, tab_tiles, tab_rows, idw, tw);
+            bool x_more = tc_tile<kBatched>(a, tab_tiles, tab_rows, idx, tx);
+            bool w_more = tc_tile<kBatched>(a, tab_tiles, tab_rows, idw, tw);
             // Each time the W cursor enters a tile, pull the tile's scales (128
             // rows x all groups, one contiguous block) into L2, so the
             // dequantisers' scale loads, issued one group ahead, hit L2.
@@ -351,7 +368,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     if (++xs == SX) { xs = 0; xpar ^= 1; }
                     if (++gx == min(n_groups, (tx.slice + 1) * a.gps)) {
                         idx += gridDim.x;
-                        x_more = tc_tile(a, tab_tiles, tab_rows, idx, tx);
+                        x_more = tc_tile<kBatched>(a, tab_tiles, tab_rows, idx, tx);
                         if (x_more) gx = tx.slice * a.gps;
                     }
                     progressed = true;
@@ -365,7 +382,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     if (++ws == SW) { ws = 0; wpar ^= 1; }
                     if (++gw == min(n_groups, (tw.slice + 1) * a.gps)) {
                         idw += gridDim.x;
-                        w_more = tc_tile(a, tab_tiles, tab_rows, idw, tw);
+                        w_more = tc_tile<kBatched>(a, tab_tiles, tab_rows, idw, tw);
                         if (w_more) {
                             gw = tw.slice * a.gps;
                             prefetch_scales(tw);
@@ -395,7 +412,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             uint32_t xph = 0, aph = 0;      // parities of the phases to wait for
             const int S = SX;
             TileInfo ti;
-            for (int id = blockIdx.x; tc_tile(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
+            for (int id = blockIdx.x; tc_tile<kBatched>(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
                 // Accumulator of this tile and the wait for its previous readers.
                 const int db = kSep ? (tiles & 1) : 0;
                 const int uses = kSep ? (tiles >> 1) : tiles;     // earlier tiles on this buffer
@@ -466,8 +483,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             }
         };
         TileInfo ti, nx;
-        for (int id = blockIdx.x; tc_tile(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
-            const bool nx_ok = tc_tile(a, tab_tiles, tab_rows, id + gridDim.x, nx);
+        for (int id = blockIdx.x; tc_tile<kBatched>(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
+            const bool nx_ok = tc_tile<kBatched>(a, tab_tiles, tab_rows, id + gridDim.x, nx);
             const int g0 = ti.slice * a.gps;
             const int g1 = min(n_groups, (ti.slice + 1) * a.gps);
             const int r0 = ti.ft * kTileRows + 16 * block + g;     // weight rows r0, r0 + 8
@@ -555,7 +572,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         unsigned char *epi = smem + L.off_epi + (warp - kTcEpiWarp0) * kEpiBytesPerWarp;
         int tiles = 0;
         TileInfo ti;
-        for (int id = blockIdx.x; tc_tile(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
+        for (int id = blockIdx.x; tc_tile<kBatched>(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
             const int db = tiles & 1;
             if (!mbar_wait(dfull_bar(db), (tiles >> 1) & 1, abort_flag, a.err)) break;
             tc_fence_after();
@@ -667,8 +684,8 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
     a.N = N;
     a.K = K;
     a.num_groups = num_groups;
-    a.batch_rows = m_sizes == nullptr && num_groups > 1 ? batch_rows : 0;
-    if (m_sizes == nullptr && num_groups > 1 && (batch_rows < 1 || (long long)batch_rows * num_groups != M_total))
+    const bool batched = m_sizes == nullptr && num_groups > 1;
+    if (batched && (batch_rows < 1 || (long long)batch_rows * num_groups != M_total))
         return cudaErrorInvalidValue;
     a.bt = p.tile_tokens;
     a.n_tiles = p.n_tiles;
@@ -685,10 +702,12 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
 
     const bool split = p.split_k > 1;
     const bool sep = p.sep_epilogue;
-    auto kern = split ? (sep ? tc_gemm_kernel<true, true> : tc_gemm_kernel<true, false>)
-                      : (sep ? tc_gemm_kernel<false, true> : tc_gemm_kernel<false, false>);
-    static std::atomic<unsigned long long> opted[4];
-    const int ki = (split ? 2 : 0) + (sep ? 1 : 0);
+    auto kern = batched ? (split ? (sep ? tc_gemm_kernel<true, true, true> : tc_gemm_kernel<true, false, true>)
+                                 : (sep ? tc_gemm_kernel<false, true, true> : tc_gemm_kernel<false, false, true>))
+                        : (split ? (sep ? tc_gemm_kernel<true, true, false> : tc_gemm_kernel<true, false, false>)
+                                 : (sep ? tc_gemm_kernel<false, true, false> : tc_gemm_kernel<false, false, false>));
+    static std::atomic<unsigned long long> opted[8];
+    const int ki = (batched ? 4 : 0) + (split ? 2 : 0) + (sep ? 1 : 0);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
