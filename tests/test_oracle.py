@@ -146,6 +146,63 @@ def test_oracle_matches_numpy_bruteforce(M, N, K, seed):
     assert np.max(np.abs(y - ref)) <= 1e-12 * scale
 
 
+# Group sizes 32 and 64: the gfx1151 page benchmarks group_size=32 ("Benchmark
+# results (per-GEMM)"); the scale of weight (n, k) is scale[n][k / G].
+@pytest.mark.parametrize("G", [32, 64])
+@pytest.mark.parametrize("M,N,K,seed", [(1, 16, 128, 0), (3, 33, 256, 1), (5, 7, 384, 2)])
+def test_oracle_matches_numpy_bruteforce_small_groups(M, N, K, G, seed):
+    inp = syn.make_gemm_inputs(M, N, K, G=G, seed=seed)
+    assert inp.scales.shape == (N, K // G)
+    y = oracle.gemm(inp.x, inp.w_canon, inp.scales, M, N, K, G=G)
+    ref = np_gemm(inp.x, inp.w_canon, inp.scales, K, G)
+    scale = max(np.max(np.abs(ref)), 1e-300)
+    assert np.max(np.abs(y - ref)) <= 1e-12 * scale
+
+
+@pytest.mark.parametrize("G", [32, 64])
+def test_small_groups_with_repeated_scales_equal_128(G):
+    # Every weight keeps its value when each 128-wide group's scale is repeated
+    # over its 128 / G sub-groups, and the k order of the sum is unchanged: the
+    # results agree bit for bit.
+    M, N, K = 3, 24, 384
+    inp = syn.make_gemm_inputs(M, N, K, seed=9)
+    rep = np.repeat(inp.scales, 128 // G, axis=1)
+    a = oracle.gemm(inp.x, inp.w_canon, inp.scales, M, N, K)
+    b = oracle.gemm(inp.x, inp.w_canon, rep, M, N, K, G=G)
+    assert np.array_equal(a, b)
+    assert np.array_equal(oracle.dequant_f64(inp.w_canon, inp.scales, N, K),
+                          oracle.dequant_f64(inp.w_canon, rep, N, K, G=G))
+
+
+@pytest.mark.parametrize("G", [32, 64])
+def test_one_hot_picks_the_sub_group_scale(G):
+    # Distinct power-of-two scales per (row, group), X one-hot at k0:
+    # Y[m][n] = 2^(e(n, k0 / G)) * (code(n, k0) - 8) exactly (closed form).
+    M, N, K = 1, 12, 256
+    inp = syn.make_gemm_inputs(M, N, K, G=G, seed=10)
+    n_g = K // G
+    e = (np.arange(N)[:, None] * 3 + np.arange(n_g)[None, :]) % 11 - 5      # exponents -5..5
+    scales = ((127 + e) << 7).astype(np.uint16)                              # bf16 2^e
+    codes = np_codes(inp.w_canon, K)
+    for k0 in [0, G - 1, G, 2 * G + 5, K - 1]:
+        x = np.zeros((M, K), dtype=np.uint16)
+        x[0, k0] = 0x3F80
+        y = oracle.gemm(x, inp.w_canon, scales, M, N, K, G=G)
+        want = np.ldexp(1.0, e[:, k0 // G]) * (codes[:, k0] - 8)
+        assert np.array_equal(y[0], want)
+
+
+@pytest.mark.parametrize("G", [32, 64])
+def test_grouped_small_groups_is_concatenation_of_plain(G):
+    inp = syn.make_grouped_inputs(3, 40, 24, 256, G=G, seed=11)
+    y = oracle.gemm_grouped(inp.x, inp.w_canon, inp.scales, inp.m_sizes, 40, 24, 256, G=G)
+    starts = np.concatenate([[0], np.cumsum(inp.m_sizes)[:-1]])
+    for g in range(3):
+        r0, r1 = starts[g], starts[g] + inp.m_sizes[g]
+        ref = np_gemm(inp.x[r0:r1], inp.w_canon[g], inp.scales[g], 256, G)
+        assert np.max(np.abs(y[r0:r1] - ref)) <= 1e-12 * max(np.max(np.abs(ref)), 1e-300)
+
+
 def test_oracle_dequant_matches_numpy():
     inp = syn.make_gemm_inputs(1, 40, 384, seed=3)
     d = oracle.dequant_f64(inp.w_canon, inp.scales, 40, 384)
@@ -328,6 +385,7 @@ MUTANTS = {
                      "(k % 2 == 0) ? (byte >> 4) : (byte & 0x0F)"),
     "offset_7": ("oracle_nibble(w_canon, K, n, k) - 8", "oracle_nibble(w_canon, K, n, k) - 7"),
     "group_index": ("scales[n * (K / G) + k / G]", "scales[n * (K / G) + k / (2 * G)]"),
+    "group_fixed_128": ("scales[n * (K / G) + k / G]", "scales[n * (K / G) + k / 128]"),
     "dropped_term": ("for (long k = 0; k < K; ++k)\n                acc += oracle_bf16_to_f64(x[m * K + k])",
                      "for (long k = 1; k < K; ++k)\n                acc += oracle_bf16_to_f64(x[m * K + k])"),
     "sign": ("acc += oracle_bf16_to_f64(x[m * K + k]) *\n                       oracle_weight(w_canon",
@@ -356,10 +414,10 @@ def _build_mutant(tmp_path, name):
 
 
 def _mutant_fails_pins(lib):
-    def gemm(x, w, s, M, N, K):
+    def gemm(x, w, s, M, N, K, G=128):
         y = np.zeros((M, N))
         lib.oracle_gemm_f64(x.ctypes.data_as(ctypes.c_void_p), w.ctypes.data_as(ctypes.c_void_p),
-                            s.ctypes.data_as(ctypes.c_void_p), M, N, K, 128,
+                            s.ctypes.data_as(ctypes.c_void_p), M, N, K, G,
                             y.ctypes.data_as(ctypes.c_void_p), 1)
         return y
     # pin 1: golden nibble order
@@ -368,11 +426,14 @@ def _mutant_fails_pins(lib):
     for j, r in enumerate(rows):
         if lib.oracle_nibble(b.ctypes.data_as(ctypes.c_void_p), 2 * b.shape[1], 0, 2 * j) != int(r[1]):
             return True
-    # pin 2: brute force on a small shape
-    inp = syn.make_gemm_inputs(3, 16, 256, seed=21)
-    y = gemm(inp.x, inp.w_canon, inp.scales, 3, 16, 256)
-    ref = np_gemm(inp.x, inp.w_canon, inp.scales, 256)
-    return not (np.max(np.abs(y - ref)) <= 1e-12 * np.max(np.abs(ref)))
+    # pin 2: brute force on a small shape, at group sizes 128 and 32
+    for G in (128, 32):
+        inp = syn.make_gemm_inputs(3, 16, 256, G=G, seed=21)
+        y = gemm(inp.x, inp.w_canon, inp.scales, 3, 16, 256, G)
+        ref = np_gemm(inp.x, inp.w_canon, inp.scales, 256, G)
+        if not (np.max(np.abs(y - ref)) <= 1e-12 * np.max(np.abs(ref))):
+            return True
+    return False
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
