@@ -64,6 +64,8 @@ def parse_args(argv=None):
     ap.add_argument("--shape", type=str, default=None, metavar="M,N,K",
                     help="time one GEMM shape (graph of back-to-back calls) and print its row "
                          "only; 'grouped' times the grouped workload")
+    ap.add_argument("--group-size", type=int, default=128, choices=[128, 64, 32],
+                    help="scale group size G for --shape")
     return ap.parse_args(argv)
 
 
@@ -165,8 +167,8 @@ def maybe_init_dist(world, local):
 
 # ---------------------------------------------------------------- our arm
 class Shape:
-    def __init__(self, torch, w4, syn, M, N, K, copies, device, seed=0):
-        inp = syn.make_gemm_inputs(M, N, K, seed=seed)
+    def __init__(self, torch, w4, syn, M, N, K, copies, device, seed=0, G=128):
+        inp = syn.make_gemm_inputs(M, N, K, G=G, seed=seed)
         self.torch = torch
         self.inp = inp
         self.M, self.N, self.K = M, N, K
@@ -177,7 +179,7 @@ class Shape:
         self.w = [wp] + [wp.clone() for _ in range(copies - 1)]
         self.s = [s] + [s.clone() for _ in range(copies - 1)]
         self.y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
-        self.plan = w4.plan(M, N, K)
+        self.plan = w4.plan(M, N, K, group_size=G)
         self.ws = torch.empty(max(self.plan["workspace_bytes"], 256), dtype=torch.uint8, device=device)
         self.launches = 1 + (1 if self.plan["split_k"] > 1 else 0)
 
@@ -419,31 +421,38 @@ def end_to_end(torch, w4, shapes, steps, step_bytes):
                     "resident"}
 
 
-def per_shape_table(torch, w4, syn, metrics, device, peaks, only=None):
-    shapes = [("tiny", 4, 256, 512)]
+# Scale groups of 32 columns (the gfx1151 page benchmarks group_size=32) on a
+# decode and a prefill shape; every other row uses groups of 128.
+GROUP32_SHAPES = [("decode_gemv_g32", 1, 8192, 8192), ("decode_gemv_g32", 1, 17408, 5120),
+                  ("prefill_g32", 1322, 19456, 2560), ("prefill_g32", 1322, 2560, 9728)]
+
+
+def per_shape_table(torch, w4, syn, metrics, device, peaks, only=None, group_size=128):
+    shapes = [("tiny", 4, 256, 512, 128)]
     for name, lst in (("decode_gemv", syn.WORKLOADS["decode_gemv"]),
                       ("decode_sweep_gate_up", syn.WORKLOADS["decode_sweep_gate_up"]),
                       ("decode_sweep_down", syn.WORKLOADS["decode_sweep_down"]),
                       ("prefill", syn.WORKLOADS["prefill"])):
-        shapes += [(name, M, N, K) for (M, N, K) in lst]
+        shapes += [(name, M, N, K, 128) for (M, N, K) in lst]
+    shapes += [(name, M, N, K, 32) for (name, M, N, K) in GROUP32_SHAPES]
     if only is not None:
         if len(only) == 4:    # G, M_total, N, K: the grouped workload
             return [grouped_row(torch, w4, syn, metrics, device, peaks)]
-        named = [sh for sh in shapes if sh[1:] == tuple(only)]
-        shapes = named[:1] or [("custom",) + tuple(only)]
+        named = [sh for sh in shapes if sh[1:] == tuple(only) + (group_size,)]
+        shapes = named[:1] or [("custom",) + tuple(only) + (group_size,)]
     rows = []
-    for name, M, N, K in shapes:
-        wb = metrics.weight_bytes(N, K)
+    for name, M, N, K, G in shapes:
+        wb = metrics.weight_bytes(N, K, G)
         C = copies_for(torch, device, wb + 2 * M * K)
-        s = Shape(torch, w4, syn, M, N, K, C, device)
+        s = Shape(torch, w4, syn, M, N, K, C, device, G=G)
         R = max(C, (100 // C) * C) if M < 512 else C
         g = capture(torch, lambda i: s.call(w4, i), R)
         g.replay()
         t = statistics.median(time_graph(torch, g) for _ in range(5)) / R
-        nbytes = metrics.algorithmic_bytes(M, N, K)
+        nbytes = metrics.algorithmic_bytes(M, N, K, G)
         fl = metrics.flops(M, N, K)
         t_roof = metrics.roofline_seconds(fl, nbytes, peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
-        rows.append({"workload": name, "M": M, "N": N, "K": K, "us": round(t * 1e6, 3),
+        rows.append({"workload": name, "M": M, "N": N, "K": K, "group_size": G, "us": round(t * 1e6, 3),
                      "tflops": round(fl / t / 1e12, 3), "gbs": round(nbytes / t / 1e9, 1),
                      "roofline_frac": round(t_roof / t, 4),
                      "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) >= fl / (peaks["bf16_tflops"] * 1e12) else "tensor",
@@ -608,8 +617,8 @@ def main(argv=None):
         only = ([0, 0, 0, 0] if args.shape == "grouped" else
                 [int(v) for v in args.shape.split(",")])
         if rank == 0:
-            print(json.dumps(per_shape_table(torch, w4, syn, metrics, device, peaks, only)[0]),
-                  flush=True)
+            print(json.dumps(per_shape_table(torch, w4, syn, metrics, device, peaks, only,
+                                             args.group_size)[0]), flush=True)
         return 0
     dist = maybe_init_dist(world, local)
     out = our_arm(args, world, rank, local, dist)

@@ -1,7 +1,8 @@
 """W4A16 skinny GEMM for GB300 (sm_103a): Python binding of the C ABI.
 
 ``Y[M, N] = X[M, K] . dequant(W)[N, K]^T`` with bf16 X and Y, int4 W packed two
-codes per byte (low nibble = even k), one bf16 scale per 128 weights along K,
+codes per byte (low nibble = even k), one bf16 scale per G weights along K
+(G = 128, 64 or 32, read off the scales' shape [N, K/G]),
 ``dequant = scale * (code - 8)``, fp32 accumulation.
 
 Every function here only checks tensor metadata, allocates outputs and
@@ -19,7 +20,8 @@ import torch
 from . import _lib
 from ._lib import Options, PlanInfo, W4A16Error
 
-GROUP = 128
+GROUP = 128                  # default scale group size
+GROUP_SIZES = (128, 64, 32)
 ARM_AUTO, ARM_DECODE, ARM_TENSOR = 0, 1, 2
 _ARMS = {None: ARM_AUTO, "auto": ARM_AUTO, "decode": ARM_DECODE, "tensor": ARM_TENSOR}
 
@@ -44,6 +46,14 @@ FLAG_RESIDENT_WEIGHTS = 1
 FLAG_DECODE_WHOLE_K = 2
 FLAG_DECODE_K_SLICES = 4
 _KERNELS = {None: 0, "auto": 0, "whole_k": FLAG_DECODE_WHOLE_K, "k_slices": FLAG_DECODE_K_SLICES}
+
+
+def _group_size(K: int, cols: int, what: str) -> int:
+    """G from K and the scales' last dimension K / G (the library rejects G
+    other than 128, 64 and 32)."""
+    if cols <= 0 or K % cols or (K // cols) not in GROUP_SIZES:
+        raise ValueError(f"{what} must have K/G columns with G in {GROUP_SIZES} (K={K}, got {cols})")
+    return K // cols
 
 
 def _opts(arm, split_k, tile_tokens, resident_weights=False, decode_kernel=None):
@@ -77,12 +87,12 @@ _plan_cache: dict = {}
 _pwb_cache: dict = {}
 
 
-def _workspace_need(M: int, N: int, K: int, o: Options, dev_index: int) -> int:
-    key = (M, N, K, o.arm, o.split_k, o.tile_tokens, o.flags, dev_index)
+def _workspace_need(M: int, N: int, K: int, G: int, o: Options, dev_index: int) -> int:
+    key = (M, N, K, G, o.arm, o.split_k, o.tile_tokens, o.flags, dev_index)
     need = _plan_cache.get(key)
     if need is None:
         info = PlanInfo()
-        _lib.check(_lib.lib().w4a16_plan(M, N, K, GROUP, ctypes.byref(o), ctypes.byref(info)),
+        _lib.check(_lib.lib().w4a16_plan(M, N, K, G, ctypes.byref(o), ctypes.byref(info)),
                    "w4a16_plan")
         need = int(info.workspace_bytes)
         _plan_cache[key] = need
@@ -117,12 +127,12 @@ def pack(w_canon: torch.Tensor) -> torch.Tensor:
 
 
 def plan(M: int, N: int, K: int, arm=None, split_k: int = 0, tile_tokens: int = 0,
-         device=None, decode_kernel=None) -> dict:
+         device=None, decode_kernel=None, group_size: int = GROUP) -> dict:
     """What the dispatcher picks for this shape on the (current) device."""
     info = PlanInfo()
     o = _opts(arm, split_k, tile_tokens, decode_kernel=decode_kernel)
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
-        _lib.check(_lib.lib().w4a16_plan(M, N, K, GROUP, ctypes.byref(o), ctypes.byref(info)),
+        _lib.check(_lib.lib().w4a16_plan(M, N, K, group_size, ctypes.byref(o), ctypes.byref(info)),
                    "w4a16_plan")
     return {"arm": {1: "decode", 2: "tensor"}.get(info.arm, info.arm), "split_k": info.split_k,
             "tile_tokens": info.tile_tokens, "ctas": info.ctas,
@@ -133,7 +143,7 @@ def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=N
          split_k: int = 0, tile_tokens: int = 0, out: torch.Tensor | None = None,
          workspace: torch.Tensor | None = None, resident_weights: bool = False,
          decode_kernel=None) -> torch.Tensor:
-    """Y = X . dequant(W)^T.  x: bf16 [M, K]; scales: bf16 [N, K/128]; returns bf16 [M, N].
+    """Y = X . dequant(W)^T.  x: bf16 [M, K]; scales: bf16 [N, K/G]; returns bf16 [M, N].
 
     ``resident_weights=True`` promises that no kernel still running on the
     current stream writes ``w_packed`` or ``scales`` (W4A16_FLAG_RESIDENT_WEIGHTS):
@@ -144,8 +154,7 @@ def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=N
     _need_cuda(w_packed, "w_packed", torch.uint8)
     M, K = x.shape
     N = scales.shape[0]
-    if scales.shape[1] * GROUP != K:
-        raise ValueError("scales must be [N, K/128]")
+    G = _group_size(K, scales.shape[1], "scales [N, K/G]")
     if w_packed.numel() < packed_weight_bytes(N, K):
         raise ValueError("w_packed is smaller than packed_weight_bytes(N, K)")
     if out is None:
@@ -160,7 +169,7 @@ def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=N
         prev = torch.cuda.current_device()
         torch.cuda.set_device(dev)
     try:
-        need = _workspace_need(M, N, K, o, dev.index)
+        need = _workspace_need(M, N, K, G, o, dev.index)
         if workspace is None:
             ws = _workspace(dev, need) if need else None
         else:
@@ -168,7 +177,7 @@ def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=N
         ws_ptr = ws.data_ptr() if ws is not None else None
         ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
         _lib.check(L.w4a16_gemm_ex(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(),
-                                   out.data_ptr(), M, N, K, GROUP, ws_ptr, ws_bytes,
+                                   out.data_ptr(), M, N, K, G, ws_ptr, ws_bytes,
                                    ctypes.byref(o), torch.cuda.current_stream(dev).cuda_stream),
                    "w4a16_gemm_ex")
     finally:
@@ -186,23 +195,25 @@ def gemm_partials(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor,
     [SPLIT_K, M, N] and ``out`` is untouched; splitk_reduce() finishes the call."""
     M, K = x.shape
     N = scales.shape[0]
+    G = _group_size(K, scales.shape[1], "scales [N, K/G]")
     o = _opts(arm, split_k, tile_tokens, resident_weights)
     sk = ctypes.c_int(0)
     with torch.cuda.device(x.device):
         _lib.check(_lib.lib().w4a16_gemm_partials(
-            x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), out.data_ptr(), M, N, K, GROUP,
+            x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), out.data_ptr(), M, N, K, G,
             workspace.data_ptr(), workspace.numel() * workspace.element_size(), ctypes.byref(o),
             ctypes.byref(sk), _stream_ptr(x.device)), "w4a16_gemm_partials")
     return int(sk.value)
 
 
 def plan_batched(batch: int, M: int, N: int, K: int, arm=None, split_k: int = 0,
-                 tile_tokens: int = 0, device=None, decode_kernel=None) -> dict:
+                 tile_tokens: int = 0, device=None, decode_kernel=None,
+                 group_size: int = GROUP) -> dict:
     """What the dispatcher picks for a batch of ``batch`` products of shape (M, N, K)."""
     info = PlanInfo()
     o = _opts(arm, split_k, tile_tokens, decode_kernel=decode_kernel)
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
-        _lib.check(_lib.lib().w4a16_plan_batched(batch, M, N, K, GROUP, ctypes.byref(o),
+        _lib.check(_lib.lib().w4a16_plan_batched(batch, M, N, K, group_size, ctypes.byref(o),
                                                  ctypes.byref(info)), "w4a16_plan_batched")
     return {"arm": {1: "decode", 2: "tensor"}.get(info.arm, info.arm), "split_k": info.split_k,
             "tile_tokens": info.tile_tokens, "ctas": info.ctas,
@@ -216,16 +227,17 @@ def gemm_batched(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, 
     """Y[b] = X[b] . dequant(W[b])^T for every b in one launch.
 
     x: bf16 [B, M, K]; w_packed: uint8 [B, packed_weight_bytes(N, K)] (or the same
-    bytes flat); scales: bf16 [B, N, K/128]; returns bf16 [B, M, N]."""
+    bytes flat); scales: bf16 [B, N, K/G]; returns bf16 [B, M, N]."""
     _need_cuda(x, "x", torch.bfloat16)
     _need_cuda(scales, "scales", torch.bfloat16)
     _need_cuda(w_packed, "w_packed", torch.uint8)
     if x.dim() != 3 or scales.dim() != 3:
-        raise ValueError("x must be [B, M, K] and scales [B, N, K/128]")
+        raise ValueError("x must be [B, M, K] and scales [B, N, K/G]")
     B, M, K = x.shape
     N = scales.shape[1]
-    if scales.shape[0] != B or scales.shape[2] * GROUP != K:
-        raise ValueError("scales must be [B, N, K/128]")
+    if scales.shape[0] != B:
+        raise ValueError("scales must be [B, N, K/G]")
+    G = _group_size(K, scales.shape[2], "scales [B, N, K/G]")
     if w_packed.numel() < B * packed_weight_bytes(N, K):
         raise ValueError("w_packed is smaller than B * packed_weight_bytes(N, K)")
     if out is None:
@@ -235,12 +247,12 @@ def gemm_batched(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, 
     o = _opts(arm, split_k, tile_tokens, resident_weights, decode_kernel)
     with torch.cuda.device(x.device):
         info = PlanInfo()
-        _lib.check(_lib.lib().w4a16_plan_batched(B, M, N, K, GROUP, ctypes.byref(o), ctypes.byref(info)),
+        _lib.check(_lib.lib().w4a16_plan_batched(B, M, N, K, G, ctypes.byref(o), ctypes.byref(info)),
                    "w4a16_plan_batched")
         need = int(info.workspace_bytes)
         ws = workspace if workspace is not None else (_workspace(x.device, need) if need else None)
         _lib.check(_lib.lib().w4a16_gemm_batched(
-            x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), out.data_ptr(), B, M, N, K, GROUP,
+            x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), out.data_ptr(), B, M, N, K, G,
             ws.data_ptr() if ws is not None else None,
             ws.numel() * ws.element_size() if ws is not None else 0, ctypes.byref(o),
             _stream_ptr(x.device)), "w4a16_gemm_batched")
@@ -253,7 +265,7 @@ def gemm_grouped(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor,
     """Grouped product in one launch.
 
     x: bf16 [M_total, K]; w_packed: num_groups packed blocks; scales: bf16
-    [num_groups, N, K/128]; m_sizes: int32 [num_groups] on the device (never
+    [num_groups, N, K/G]; m_sizes: int32 [num_groups] on the device (never
     read on the host).  Returns (Y bf16 [M_total, N], status int32 tensor
     whose element 0 the kernel sets; 0 = sizes consistent)."""
     _need_cuda(x, "x", torch.bfloat16)
@@ -261,51 +273,56 @@ def gemm_grouped(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor,
     _need_cuda(w_packed, "w_packed", torch.uint8)
     _need_cuda(m_sizes, "m_sizes", torch.int32)
     M_total, K = x.shape
-    G, N, kg = scales.shape
-    if kg * GROUP != K or m_sizes.numel() != G:
-        raise ValueError("scales must be [num_groups, N, K/128] and m_sizes [num_groups]")
-    if w_packed.numel() < G * packed_weight_bytes(N, K):
+    NG, N, kg = scales.shape
+    if m_sizes.numel() != NG:
+        raise ValueError("scales must be [num_groups, N, K/G] and m_sizes [num_groups]")
+    G = _group_size(K, kg, "scales [num_groups, N, K/G]")
+    if w_packed.numel() < NG * packed_weight_bytes(N, K):
         raise ValueError("w_packed is smaller than num_groups * packed_weight_bytes(N, K)")
     if out is None:
         out = torch.empty((M_total, N), dtype=torch.bfloat16, device=x.device)
     L = _lib.lib()
     with torch.cuda.device(x.device):
         nb = ctypes.c_size_t(0)
-        _lib.check(L.w4a16_grouped_workspace_bytes(G, M_total, N, K, GROUP, ctypes.byref(nb)),
+        _lib.check(L.w4a16_grouped_workspace_bytes(NG, M_total, N, K, G, ctypes.byref(nb)),
                    "w4a16_grouped_workspace_bytes")
         if status is None:
             status = torch.empty(max(4, (nb.value + 3) // 4), dtype=torch.int32, device=x.device)
         _lib.check(L.w4a16_gemm_grouped(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(),
-                                        m_sizes.data_ptr(), out.data_ptr(), G, M_total, N, K,
-                                        GROUP, status.data_ptr(), status.numel() * 4,
+                                        m_sizes.data_ptr(), out.data_ptr(), NG, M_total, N, K,
+                                        G, status.data_ptr(), status.numel() * 4,
                                         _stream_ptr(x.device)), "w4a16_gemm_grouped")
     return out, status
 
 
-def dequant_fp32(w_packed: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
-    """fp32 [N, K] = scale * (code - 8), computed by the kernels' bit trick."""
+def dequant_fp32(w_packed: torch.Tensor, scales: torch.Tensor,
+                 group_size: int = GROUP) -> torch.Tensor:
+    """fp32 [N, K] = scale * (code - 8), computed by the kernels' bit trick;
+    scales bf16 [N, K/G] with G = group_size."""
     _need_cuda(w_packed, "w_packed", torch.uint8)
     _need_cuda(scales, "scales", torch.bfloat16)
     N, kg = scales.shape
-    K = kg * GROUP
+    K = kg * group_size
     out = torch.empty((N, K), dtype=torch.float32, device=scales.device)
     with torch.cuda.device(scales.device):
         _lib.check(_lib.lib().w4a16_dequant_fp32(w_packed.data_ptr(), scales.data_ptr(),
-                                                 out.data_ptr(), N, K, GROUP,
+                                                 out.data_ptr(), N, K, group_size,
                                                  _stream_ptr(scales.device)), "w4a16_dequant_fp32")
     return out
 
 
-def dequant_bf16(w_packed: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
-    """bf16 [N, K] = round_nearest_even(scale * (code - 8)): the tensor arm's operand."""
+def dequant_bf16(w_packed: torch.Tensor, scales: torch.Tensor,
+                 group_size: int = GROUP) -> torch.Tensor:
+    """bf16 [N, K] = round_nearest_even(scale * (code - 8)): the tensor arm's
+    operand; scales bf16 [N, K/G] with G = group_size."""
     _need_cuda(w_packed, "w_packed", torch.uint8)
     _need_cuda(scales, "scales", torch.bfloat16)
     N, kg = scales.shape
-    K = kg * GROUP
+    K = kg * group_size
     out = torch.empty((N, K), dtype=torch.bfloat16, device=scales.device)
     with torch.cuda.device(scales.device):
         _lib.check(_lib.lib().w4a16_dequant_bf16(w_packed.data_ptr(), scales.data_ptr(),
-                                                 out.data_ptr(), N, K, GROUP,
+                                                 out.data_ptr(), N, K, group_size,
                                                  _stream_ptr(scales.device)), "w4a16_dequant_bf16")
     return out
 

@@ -66,8 +66,11 @@ constexpr double kTcSmallTileKbClk = 800.0;   // per-SM cycles per K block, tile
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Scale groups of 128, 64 or 32 columns; K stays a multiple of 128 (the
+// packed layout's block), so every 128-wide block holds 128 / group_size
+// whole scale groups.
 w4a16_status check_shape(int M, int N, int K, int group_size) {
-    if (group_size != kGroup) return W4A16_ERR_UNSUPPORTED;
+    if (group_size != 128 && group_size != 64 && group_size != 32) return W4A16_ERR_UNSUPPORTED;
     if (M < 0 || N < 1 || K < kGroup || K % kGroup) return W4A16_ERR_INVALID_ARG;
     if (N > (1 << 24) || K > (1 << 20) || M > (1 << 24)) return W4A16_ERR_INVALID_ARG;
     return W4A16_OK;
@@ -109,15 +112,23 @@ double decode_slice_preference(int gps) {
 // all resident at once.  wk: 0 = either kernel, 1 = whole-K only, 2 = slices only.
 // batch > 1: that many independent products of this shape share the GPU
 // (each gets its share of the CTA slots; the weight stream is all of theirs).
-void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int batch, DecodePlan *d) {
+// sub: scale groups per 128-wide block (1, 2, 4).  Smaller groups keep
+// GPS * sub scales of a row in registers (at most 16, 8 for two token
+// octets) and have only the slice kernel; their scale bytes (2 per group)
+// scale the modelled weight stream relative to 128-wide groups, for which the
+// constants were measured.
+void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int batch, int sub,
+                 DecodePlan *d) {
     const int groups = K / kGroup;
+    const double sbytes = (0.5 + 2.0 * sub / kGroup) / (0.5 + 2.0 / kGroup);
     d->mt = M <= 8 ? 1 : 2;
     d->token_blocks = ceil_div(M, 8 * d->mt);
     d->n_tiles = ceil_div(N, kTileRows);
     d->batch = batch;
+    d->sub = sub;
     long long slots = (long long)kDecodeCtasPerSm * sms / batch;
     if (slots < 1) slots = 1;
-    const double w_bytes = double(batch) * d->n_tiles * kTileRows * double(K) / 2.0;
+    const double w_bytes = double(batch) * d->n_tiles * kTileRows * double(K) / 2.0 * sbytes;
     double best = 1e30;
     d->split_k = groups;
     d->groups_per_slice = 1;
@@ -125,7 +136,7 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int bat
     d->ring = kDecodeRing;
     d->in_flight = kDecodeInFlight;
     d->wk_blocks = 0;
-    if (wk != 2 && forced_split <= 1) {
+    if (wk != 2 && forced_split <= 1 && sub == 1) {
         // (one block per CTA would leave each K-part a single ring slot)
         for (int B : {8, 4, 2}) {
             if (!decode_wk_fits(M, K, B)) continue;
@@ -145,11 +156,12 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int bat
         }
         if (wk == 1) return;
     }
+    if (wk == 1) return;   // (smaller groups: no whole-K kernel)
     // Slices hold 1, 2, 4, 8 or 16 groups and divide K exactly (the kernel
     // unrolls a slice at compile time).  A forced split picks the feasible slice count
     // closest to the request from above.
     // 16-group slices only for one token octet (register budget).
-    const int gps_max = d->mt == 1 ? 16 : 8;
+    const int gps_max = (d->mt == 1 ? 16 : 8) / sub;
     int forced_gps = 0;
     if (forced_split > 0) {
         for (int gps : {16, 8, 4, 2, 1})
@@ -168,7 +180,7 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int bat
         for (int C = cmax; C >= 1; --C) {
             const int tiles_per = ceil_div(d->n_tiles, C);
             if (C < cmax && ceil_div(d->n_tiles, C + 1) == tiles_per) continue;  // same critical path, fewer CTAs
-            const double cta_bytes = double(tiles_per) * 2.0 * gps * kChunkBytes * d->token_blocks;
+            const double cta_bytes = double(tiles_per) * 2.0 * gps * kChunkBytes * d->token_blocks * sbytes;
             double t = w_bytes * d->token_blocks / kHbmBytesPerS;
             const double t_cta = cta_bytes / kCtaBytesPerS;
             if (t_cta > t) t = t_cta;
@@ -224,9 +236,12 @@ bool tensor_rings(int bt, int num_groups, int occupancy, bool sep, int *x_stages
 // which a second resident CTA hides.
 // batch_rows > 0: a batched product, num_groups entries of batch_rows rows
 // (M = their total): the plain product per entry, split-K allowed.
+// sub: scale groups per 128-wide block (1, 2, 4); the dequantisers load
+// sub scales per row and block, which the model does not charge.
 w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int forced_bt,
-                         int num_groups, TensorPlan *t, int batch_rows) {
+                         int num_groups, TensorPlan *t, int batch_rows, int sub) {
     const int groups = K / kGroup;
+    t->sub = sub;
     const bool grouped = num_groups > 1 && batch_rows == 0;
     t->n_tiles = ceil_div(N, kTileRows);
     double best = 1e30;
@@ -308,7 +323,9 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
 }
 
 // batch: independent products of this shape in one launch (1: a plain call).
-w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, int batch = 1) {
+// sub: scale groups per 128-wide block (128 / group_size).
+w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, int batch = 1,
+                       int sub = 1) {
     std::memset(p, 0, sizeof *p);
     int arm = opts ? opts->arm : W4A16_ARM_AUTO;
     if (arm != W4A16_ARM_AUTO && arm != W4A16_ARM_DECODE && arm != W4A16_ARM_TENSOR)
@@ -330,7 +347,7 @@ w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, 
     p->arm = arm;
     if (arm == W4A16_ARM_DECODE) {
         DecodePlan &d = p->decode;
-        plan_decode(M, N, K, sms, opts ? opts->split_k : 0, wk, batch, &d);
+        plan_decode(M, N, K, sms, opts ? opts->split_k : 0, wk, batch, sub, &d);
         if (wk == 1 && d.wk_blocks == 0) return W4A16_ERR_UNSUPPORTED;
         p->split_k = d.split_k;
         p->ctas = batch * (d.wk_blocks ? d.ctas_per_slice : d.ctas_per_slice * d.split_k * d.token_blocks);
@@ -339,7 +356,7 @@ w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, 
         if (wk == 1) return W4A16_ERR_UNSUPPORTED;
         TensorPlan &t = p->tensor;
         w4a16_status st = plan_tensor(batch * M, N, K, sms, opts ? opts->split_k : 0, forced_bt,
-                                      batch, &t, batch > 1 ? M : 0);
+                                      batch, &t, batch > 1 ? M : 0, sub);
         if (st != W4A16_OK) return st;
         p->split_k = t.split_k;
         p->ctas = t.ctas;
@@ -389,7 +406,7 @@ w4a16_status w4a16_plan(int M, int N, int K, int group_size, const w4a16_options
     w4a16_status st = check_shape(M, N, K, group_size);
     if (st != W4A16_OK) return st;
     Plan p;
-    st = plan_call(M, N, K, opts, &p);
+    st = plan_call(M, N, K, opts, &p, 1, kGroup / group_size);
     if (st != W4A16_OK) return st;
     if (info) {
         info->arm = p.arm;
@@ -427,7 +444,7 @@ static w4a16_status gemm_impl(const w4a16_bf16 *X, const uint8_t *W_packed,
     if (!aligned(X, 16) || !aligned(W_packed, 16) || !aligned(scales, 2) || !aligned(Y, 2))
         return W4A16_ERR_INVALID_ARG;
     Plan p;
-    st = plan_call(M, N, K, opts, &p, batch);
+    st = plan_call(M, N, K, opts, &p, batch, kGroup / group_size);
     if (st != W4A16_OK) return st;
     if (split_out) *split_out = p.split_k;
     if (p.ws_bytes > 0) {
@@ -483,7 +500,7 @@ w4a16_status w4a16_plan_batched(int batch, int M, int N, int K, int group_size,
     if (st != W4A16_OK) return st;
     if (batch < 1 || batch > kMaxGroups || (long long)batch * M > (1 << 24)) return W4A16_ERR_INVALID_ARG;
     Plan p;
-    st = plan_call(M, N, K, opts, &p, batch);
+    st = plan_call(M, N, K, opts, &p, batch, kGroup / group_size);
     if (st != W4A16_OK) return st;
     if (info) {
         info->arm = p.arm;
@@ -532,7 +549,7 @@ w4a16_status w4a16_gemm_grouped(const w4a16_bf16 *X, const uint8_t *W_packed,
     int sms = 0;
     if (device_sm_count(&sms) != 0 || sms < 1) return W4A16_ERR_CUDA;
     TensorPlan t;
-    st = plan_tensor(M_total, N, K, sms, 1, 0, num_groups, &t, 0);
+    st = plan_tensor(M_total, N, K, sms, 1, 0, num_groups, &t, 0, kGroup / group_size);
     if (st != W4A16_OK) return st;
     // Enough CTAs for any split of M_total into the groups: the tile count is
     // at most n_tiles * (ceil(M_total / bt) + num_groups).
@@ -552,7 +569,7 @@ w4a16_status w4a16_dequant_fp32(const uint8_t *W_packed, const w4a16_bf16 *scale
     if (!W_packed || !scales || !out) return W4A16_ERR_INVALID_ARG;
     if (!aligned(W_packed, 16) || !aligned(scales, 2) || !aligned(out, 4))
         return W4A16_ERR_INVALID_ARG;
-    return from_cuda(launch_dequant(W_packed, scales, out, false, N, K,
+    return from_cuda(launch_dequant(W_packed, scales, out, false, N, K, group_size,
                                     static_cast<cudaStream_t>(stream)));
 }
 
@@ -563,7 +580,7 @@ w4a16_status w4a16_dequant_bf16(const uint8_t *W_packed, const w4a16_bf16 *scale
     if (!W_packed || !scales || !out) return W4A16_ERR_INVALID_ARG;
     if (!aligned(W_packed, 16) || !aligned(scales, 2) || !aligned(out, 2))
         return W4A16_ERR_INVALID_ARG;
-    return from_cuda(launch_dequant(W_packed, scales, out, true, N, K,
+    return from_cuda(launch_dequant(W_packed, scales, out, true, N, K, group_size,
                                     static_cast<cudaStream_t>(stream)));
 }
 

@@ -19,6 +19,8 @@ struct DecodePlan {
     int wk_blocks;        // > 0: whole-K kernel, each CTA owns this many 16-row blocks over all
                           // of K (split_k is 1, ctas_per_slice the grid); 0: the slice kernel
     int batch;            // independent products of this shape (batched op; 1 otherwise)
+    int sub;              // scale groups per 128-wide block: 1, 2 or 4 (groups of 128, 64, 32
+                          // columns); the whole-K kernel takes 1 only
 };
 
 struct TensorPlan {
@@ -32,6 +34,7 @@ struct TensorPlan {
     int w_stages;         // W ring depth (groups of packed weights in shared memory)
     int occupancy;        // CTAs per SM the resources are sized for (1 or 2)
     bool sep_epilogue;    // two TMEM accumulators drained by dedicated epilogue warps (occupancy 1)
+    int sub;              // scale groups per 128-wide block: 1, 2 or 4 (groups of 128, 64, 32)
     size_t smem_bytes;
 };
 
@@ -43,7 +46,7 @@ int *device_error_word();        // device address of the error word (nullptr on
 // 1 KB per CTA is reserved).
 constexpr int kDecodeMaxGps = 16;
 constexpr int kDecodeMaxSmem = 113 * 1024;
-int decode_smem_needed(int M, int mt, int groups_per_slice);
+int decode_smem_needed(int M, int mt, int groups_per_slice, int sub);
 // Whole-K decode kernel: whether M tokens of K fit its staging, and its launch.
 bool decode_wk_fits(int M, int K, int blocks_per_cta);
 cudaError_t launch_decode_wk(int blocks_per_cta, int ctas, int batch, const uint16_t *X, const uint8_t *Wp,
@@ -53,8 +56,9 @@ cudaError_t launch_decode_wk(int blocks_per_cta, int ctas, int batch, const uint
 size_t packed_bytes(int N, int K);
 
 cudaError_t launch_pack(const uint8_t *w_canon, uint8_t *w_packed, int N, int K, cudaStream_t s);
+// G: scale group size (128, 64 or 32 columns).
 cudaError_t launch_dequant(const uint8_t *w_packed, const uint16_t *scales, void *out,
-                           bool bf16_out, int N, int K, cudaStream_t s);
+                           bool bf16_out, int N, int K, int G, cudaStream_t s);
 // resident: the weights and scales are not written by the previous kernel on
 // the stream, so the weight stream may start before that kernel completes.
 cudaError_t launch_decode(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,

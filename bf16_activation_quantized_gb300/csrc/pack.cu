@@ -62,13 +62,15 @@ __global__ void pack_kernel(const uint8_t *__restrict__ wc, uint32_t *__restrict
 
 template <bool kBf16Out>
 __global__ void dequant_kernel(const uint32_t *__restrict__ wp, const uint16_t *__restrict__ S,
-                               void *__restrict__ out, int N, int K, size_t words) {
+                               void *__restrict__ out, int N, int K, int G, size_t words) {
     const size_t idx = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= words) return;
     const WordCoord c = word_coord(idx, K / kChunkK);
     const uint32_t w = wp[idx];
-    const int groups = K / kGroup;
-    const int grp = c.k / kGroup;
+    // A word's four columns c.k .. c.k + 3 share one scale group (G is a
+    // multiple of 4).
+    const int groups = K / G;
+    const int grp = c.k / G;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
         const int row = c.row0 + 8 * half;
@@ -115,15 +117,15 @@ cudaError_t launch_pack(const uint8_t *w_canon, uint8_t *w_packed, int N, int K,
 }
 
 cudaError_t launch_dequant(const uint8_t *w_packed, const uint16_t *scales, void *out,
-                           bool bf16_out, int N, int K, cudaStream_t s) {
+                           bool bf16_out, int N, int K, int G, cudaStream_t s) {
     const size_t words = packed_bytes(N, K) / 4;
     const int threads = 256;
     const size_t blocks = (words + threads - 1) / threads;
     const uint32_t *wp = reinterpret_cast<const uint32_t *>(w_packed);
     if (bf16_out)
-        dequant_kernel<true><<<dim3(unsigned(blocks)), threads, 0, s>>>(wp, scales, out, N, K, words);
+        dequant_kernel<true><<<dim3(unsigned(blocks)), threads, 0, s>>>(wp, scales, out, N, K, G, words);
     else
-        dequant_kernel<false><<<dim3(unsigned(blocks)), threads, 0, s>>>(wp, scales, out, N, K, words);
+        dequant_kernel<false><<<dim3(unsigned(blocks)), threads, 0, s>>>(wp, scales, out, N, K, G, words);
     return cudaGetLastError();
 }
 

@@ -57,6 +57,10 @@ constexpr int kTcEpiWarps = 4;
 constexpr int kTcThreadsSep = (kTcEpiWarp0 + kTcEpiWarps) * 32;
 constexpr uint32_t kTcDCol = 0;      // accumulator: columns [0, bt); A stage sa: [bt + 32 sa, bt + 32 sa + 32)
 
+// TcArgs::opt_bits.
+constexpr int kTcVecStore = 1;   // Y rows are 16-byte aligned: stage the epilogue for 16-byte stores
+constexpr int kTcScaleVec = 2;   // scales aligned to 2 * sub bytes: one load per row's sub scales
+
 struct TcArgs {
     const uint8_t *Wp;
     const uint16_t *S;
@@ -74,7 +78,7 @@ struct TcArgs {
     int a_stages;             // TMEM A ring depth (one group = 64 columns per stage)
     int tmem_cols;            // TMEM columns allocated (power of two >= dcols + 64 * a_stages)
     int dcols;                // accumulator columns: bt, or 2 bt with a separate epilogue
-    int vec_store;            // Y rows are 16-byte aligned: stage the epilogue for 16-byte stores
+    int opt_bits;             // kTcVecStore | kTcScaleVec
     unsigned long long w_group_stride;  // bytes between groups' packed weights
     unsigned long long s_group_stride;  // elements between groups' scales
 };
@@ -181,6 +185,49 @@ __device__ __forceinline__ uint32_t scale_raw(const uint16_t *S, int row, int N,
 }
 __device__ __forceinline__ uint32_t scale_pair2(uint32_t raw) { return raw | (raw << 16); }
 
+// The kSub scales of one weight row for one 128-wide block (scale groups of
+// 128 / kSub columns), raw, two per 32-bit word (scale i in half i % 2 of word
+// i / 2).  kSub == 1 is scale_raw.
+template <int kSub>
+struct ScaleRaw {
+    uint32_t w[(kSub + 1) / 2];
+};
+// vec: S + idx is aligned to 2 * kSub bytes (a row's kSub scales of one block
+// start at a multiple of kSub elements), so one 4- or 8-byte load fetches them.
+template <int kSub>
+__device__ __forceinline__ ScaleRaw<kSub> scales_raw(const uint16_t *S, int row, int N, size_t idx,
+                                                     bool vec) {
+    ScaleRaw<kSub> r;
+#pragma unroll
+    for (int i = 0; i < (kSub + 1) / 2; ++i) r.w[i] = 0;
+    if constexpr (kSub == 2) {
+        if (vec) {
+            asm volatile("{\n\t.reg .pred p;\n\tsetp.lt.s32 p, %1, %2;\n\t"
+                         "@p ld.global.nc.u32 %0, [%3];\n\t}"
+                         : "+r"(r.w[0])
+                         : "r"(row), "r"(N), "l"(S + idx));
+            return r;
+        }
+    } else if constexpr (kSub == 4) {
+        if (vec) {
+            asm volatile("{\n\t.reg .pred p;\n\tsetp.lt.s32 p, %2, %3;\n\t"
+                         "@p ld.global.nc.v2.u32 {%0, %1}, [%4];\n\t}"
+                         : "+r"(r.w[0]), "+r"(r.w[1])
+                         : "r"(row), "r"(N), "l"(S + idx));
+            return r;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kSub; ++i) r.w[i / 2] |= scale_raw(S, row, N, idx + i) << (16 * (i & 1));
+    return r;
+}
+// bf16x2 pair {scale i, scale i}.
+template <int kSub>
+__device__ __forceinline__ uint32_t scale_pair_of(const ScaleRaw<kSub> &r, int i) {
+    if constexpr (kSub == 1) return scale_pair2(r.w[0]);
+    return __byte_perm(r.w[i / 2], 0, (i & 1) ? 0x3232 : 0x1010);
+}
+
 __device__ __forceinline__ void drain_wait_tc(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity))
@@ -211,7 +258,7 @@ __device__ __forceinline__ void tc_store_block(const TcArgs &a, const TileInfo &
                                                int lane) {
     const int t0 = ti.x_row0 + cb * 32;                // token of v[0]
     const int nt = min(32, ti.rows - cb * 32);         // valid tokens of the block
-    if (kSplit || !a.vec_store) {
+    if (kSplit || !(a.opt_bits & kTcVecStore)) {
         const int f = fb + lane;
         if (f < a.N) {
 #pragma unroll
@@ -246,7 +293,10 @@ __device__ __forceinline__ void tc_store_block(const TcArgs &a, const TileInfo &
     }
 }
 
-template <bool kSplit, bool kSep, bool kBatched>
+// kSub: scale groups per 128-wide block (1, 2, 4: groups of 128, 64, 32
+// columns).  Packed word j of a lane covers columns 16 j .. 16 j + 15 of the
+// block, so its scale group is j * kSub / 8.
+template <bool kSplit, bool kSep, bool kBatched, int kSub>
 __global__ void __launch_bounds__(kSep ? kTcThreadsSep : kTcThreads, kSep ? 1 : 2)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     extern __shared__ unsigned char smem_raw[];
@@ -326,6 +376,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     const uint32_t tmem_base = *tmem_slot;
 
     const int n_groups = a.K / kGroup;
+    const int n_sg = n_groups * kSub;                         // scales per weight row
     const int KC = a.K / kChunkK;
     const uint32_t x_bytes = uint32_t(a.bt) * 128u;          // one X box
     const uint32_t idesc = tc_idesc_bf16(128, a.bt);
@@ -348,8 +399,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 const size_t r0 = size_t(ti.ft) * kTileRows;
                 const size_t r1 = min(size_t(a.N), r0 + kTileRows);
                 // Rounded inwards to 16 bytes: never outside the block.
-                const uintptr_t lo = (reinterpret_cast<uintptr_t>(sg + r0 * n_groups) + 15) & ~uintptr_t(15);
-                const uintptr_t hi = reinterpret_cast<uintptr_t>(sg + r1 * n_groups) & ~uintptr_t(15);
+                const uintptr_t lo = (reinterpret_cast<uintptr_t>(sg + r0 * n_sg) + 15) & ~uintptr_t(15);
+                const uintptr_t hi = reinterpret_cast<uintptr_t>(sg + r1 * n_sg) & ~uintptr_t(15);
                 if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void *>(lo), uint32_t(hi - lo));
             };
             if (w_more) prefetch_scales(tw);
@@ -466,8 +517,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         const int S = SW;
         // Scales of the next group (possibly in the next tile), loaded one group
         // ahead so the dequantisers never wait on them.
-        uint32_t n0 = 0, n1 = 0;
+        ScaleRaw<kSub> n0 = {}, n1 = {};
         bool have_next = false;
+        const bool svec = (a.opt_bits & kTcScaleVec) != 0;
         // An A stage whose TMEM store is still in flight: its completion is
         // waited for only after the next group is dequantised, so the store
         // latency overlaps the ALU work.
@@ -491,25 +543,25 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             const uint16_t *sg = a.S + (unsigned long long)ti.group * a.s_group_stride;
             bool ok = true;
             for (int grp = g0; grp < g1; ++grp) {
-                uint32_t s0, s1;                    // raw; paired after the stage wait
+                ScaleRaw<kSub> s0, s1;              // raw; paired after the stage wait
                 if (have_next) {
                     s0 = n0;
                     s1 = n1;
                 } else {
-                    s0 = scale_raw(sg, r0, a.N, size_t(r0) * n_groups + grp);
-                    s1 = scale_raw(sg, r0 + 8, a.N, size_t(r0 + 8) * n_groups + grp);
+                    s0 = scales_raw<kSub>(sg, r0, a.N, size_t(r0) * n_sg + size_t(grp) * kSub, svec);
+                    s1 = scales_raw<kSub>(sg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(grp) * kSub, svec);
                 }
                 have_next = false;
                 if (grp + 1 < g1) {
-                    n0 = scale_raw(sg, r0, a.N, size_t(r0) * n_groups + grp + 1);
-                    n1 = scale_raw(sg, r0 + 8, a.N, size_t(r0 + 8) * n_groups + grp + 1);
+                    n0 = scales_raw<kSub>(sg, r0, a.N, size_t(r0) * n_sg + size_t(grp + 1) * kSub, svec);
+                    n1 = scales_raw<kSub>(sg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(grp + 1) * kSub, svec);
                     have_next = true;
                 } else if (nx_ok) {
                     const int rn = nx.ft * kTileRows + 16 * block + g;
                     const int gn = nx.slice * a.gps;
                     const uint16_t *sn = a.S + (unsigned long long)nx.group * a.s_group_stride;
-                    n0 = scale_raw(sn, rn, a.N, size_t(rn) * n_groups + gn);
-                    n1 = scale_raw(sn, rn + 8, a.N, size_t(rn + 8) * n_groups + gn);
+                    n0 = scales_raw<kSub>(sn, rn, a.N, size_t(rn) * n_sg + size_t(gn) * kSub, svec);
+                    n1 = scales_raw<kSub>(sn, rn + 8, a.N, size_t(rn + 8) * n_sg + size_t(gn) * kSub, svec);
                     have_next = true;
                 }
                 if (!mbar_wait(wfull_bar(st), wph, abort_flag, a.err)) { ok = false; break; }
@@ -520,17 +572,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 // The stage's bytes are in registers: hand it back to the producer.
                 __syncwarp();
                 if (lane == 0) mbar_arrive(wempty_bar(st));
-                s0 = scale_pair2(s0);
-                s1 = scale_pair2(s1);
+                uint32_t p0[kSub], p1[kSub];
+#pragma unroll
+                for (int i = 0; i < kSub; ++i) {
+                    p0[i] = scale_pair_of<kSub>(s0, i);
+                    p1[i] = scale_pair_of<kSub>(s1, i);
+                }
                 uint32_t frag[32];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     // Repetition j of the 16x256b store: {row g: pair 0, pair 1},
                     // {row g+8: pair 0, pair 1} of columns 16j + 4t of the group.
-                    frag[4 * j + 0] = bf16x2_mul(minus136(magic_pair(wv[j])), s0);
-                    frag[4 * j + 1] = bf16x2_mul(minus136(magic_pair(wv[j] >> 8)), s0);
-                    frag[4 * j + 2] = bf16x2_mul(minus136(magic_pair(wv[j] >> 4)), s1);
-                    frag[4 * j + 3] = bf16x2_mul(minus136(magic_pair(wv[j] >> 12)), s1);
+                    const uint32_t q0 = p0[j * kSub / 8], q1 = p1[j * kSub / 8];
+                    frag[4 * j + 0] = bf16x2_mul(minus136(magic_pair(wv[j])), q0);
+                    frag[4 * j + 1] = bf16x2_mul(minus136(magic_pair(wv[j] >> 8)), q0);
+                    frag[4 * j + 2] = bf16x2_mul(minus136(magic_pair(wv[j] >> 4)), q1);
+                    frag[4 * j + 3] = bf16x2_mul(minus136(magic_pair(wv[j] >> 12)), q1);
                 }
                 if (++st == S) { st = 0; wph ^= 1; }
                 flush();
@@ -648,6 +705,45 @@ size_t tensor_smem_bytes(int bt, int x_stages, int w_stages, int occupancy, int 
            1024;  // + alignment slack
 }
 
+namespace {
+
+// One of the kernel's eight (split, separate epilogue, batched) forms for
+// kSub scale groups per 128-wide block.
+template <int kSub>
+cudaError_t launch_tc_sub(const TensorPlan &p, const CUtensorMap &tmap, const TcArgs &a, bool batched,
+                          size_t smem, cudaStream_t s) {
+    const bool split = p.split_k > 1;
+    const bool sep = p.sep_epilogue;
+    auto kern = batched ? (split ? (sep ? tc_gemm_kernel<true, true, true, kSub> : tc_gemm_kernel<true, false, true, kSub>)
+                                 : (sep ? tc_gemm_kernel<false, true, true, kSub> : tc_gemm_kernel<false, false, true, kSub>))
+                        : (split ? (sep ? tc_gemm_kernel<true, true, false, kSub> : tc_gemm_kernel<true, false, false, kSub>)
+                                 : (sep ? tc_gemm_kernel<false, true, false, kSub> : tc_gemm_kernel<false, false, false, kSub>));
+    static std::atomic<unsigned long long> opted[8];
+    const int ki = (batched ? 4 : 0) + (split ? 2 : 0) + (sep ? 1 : 0);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(opted[ki].load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTensorMaxSmem);
+        if (e != cudaSuccess) return e;
+        opted[ki].fetch_or(bit, std::memory_order_acq_rel);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.ctas);
+    cfg.blockDim = dim3(p.sep_epilogue ? kTcThreadsSep : kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmap, a);
+}
+
+}  // namespace
+
 cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, const int32_t *m_sizes,
                           int *status, int num_groups, int M_total, int N, int K, cudaStream_t s,
@@ -656,6 +752,7 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
         p.w_stages < 2 ||
         p.ctas < 1 || num_groups < 1 || num_groups > kMaxGroups || p.occupancy < 1 ||
         p.occupancy > 2 || (p.sep_epilogue && p.occupancy != 1) ||
+        (p.sub != 1 && p.sub != 2 && p.sub != 4) ||
         tensor_a_stages(p.tile_tokens, p.occupancy, p.sep_epilogue) < 2)
         return cudaErrorInvalidValue;
     EncodeTiledFn enc = encode_tiled();
@@ -696,41 +793,17 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
     a.a_stages = tensor_a_stages(p.tile_tokens, p.occupancy, p.sep_epilogue);
     a.tmem_cols = tensor_tmem_cols(p.tile_tokens, p.occupancy, p.sep_epilogue);
     a.dcols = p.sep_epilogue ? 2 * p.tile_tokens : p.tile_tokens;
-    a.vec_store = (N % 8 == 0) && (reinterpret_cast<uintptr_t>(Y) % 16 == 0);
+    a.opt_bits = ((N % 8 == 0) && (reinterpret_cast<uintptr_t>(Y) % 16 == 0) ? kTcVecStore : 0) |
+                 (reinterpret_cast<uintptr_t>(S) % (2 * p.sub) == 0 ? kTcScaleVec : 0);
     a.w_group_stride = packed_bytes(N, K);
-    a.s_group_stride = (unsigned long long)N * (K / kGroup);
+    a.s_group_stride = (unsigned long long)N * (K / kGroup) * p.sub;
 
-    const bool split = p.split_k > 1;
-    const bool sep = p.sep_epilogue;
-    auto kern = batched ? (split ? (sep ? tc_gemm_kernel<true, true, true> : tc_gemm_kernel<true, false, true>)
-                                 : (sep ? tc_gemm_kernel<false, true, true> : tc_gemm_kernel<false, false, true>))
-                        : (split ? (sep ? tc_gemm_kernel<true, true, false> : tc_gemm_kernel<true, false, false>)
-                                 : (sep ? tc_gemm_kernel<false, true, false> : tc_gemm_kernel<false, false, false>));
-    static std::atomic<unsigned long long> opted[8];
-    const int ki = (batched ? 4 : 0) + (split ? 2 : 0) + (sep ? 1 : 0);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(opted[ki].load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTensorMaxSmem);
-        if (e != cudaSuccess) return e;
-        opted[ki].fetch_or(bit, std::memory_order_acq_rel);
-    }
     const size_t smem =
-        tensor_smem_bytes(p.tile_tokens, p.x_stages, p.w_stages, p.occupancy, num_groups, sep);
+        tensor_smem_bytes(p.tile_tokens, p.x_stages, p.w_stages, p.occupancy, num_groups, p.sep_epilogue);
     if (smem > size_t(tensor_smem_budget(p.occupancy))) return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.ctas);
-    cfg.blockDim = dim3(p.sep_epilogue ? kTcThreadsSep : kTcThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tmap, a);
+    if (p.sub == 2) return launch_tc_sub<2>(p, tmap, a, batched, smem, s);
+    if (p.sub == 4) return launch_tc_sub<4>(p, tmap, a, batched, smem, s);
+    return launch_tc_sub<1>(p, tmap, a, batched, smem, s);
 }
 
 }  // namespace w4a16

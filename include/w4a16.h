@@ -2,7 +2,7 @@
  * w4a16.h -- C ABI of the GB300 (sm_103a) W4A16 skinny GEMM library.
  *
  *   Y[M][N] (bf16) = X[M][K] (bf16) . dequant(W)[N][K]^T,  fp32 accumulation,
- *   dequant(W)[n][k] = scale[n][k / 128] * (code(n, k) - 8).
+ *   dequant(W)[n][k] = scale[n][k / G] * (code(n, k) - 8),  G = group_size.
  *
  * The op: "[ROCm][Kernel] W4A16 skinny GEMM: hand-asm kernel for gfx1151"
  * (opening paragraph: int4 weights, bf16 activations, N x K weight shapes;
@@ -25,8 +25,11 @@
  *  - Arguments are validated on the host before anything is enqueued; a
  *    failed check returns an error status and launches nothing.  A launch
  *    failure returns W4A16_ERR_CUDA.  Kernels never trap.
- *  - group_size must be 128 (W4A16_ERR_UNSUPPORTED otherwise); K must be a
- *    positive multiple of 128; N >= 1; M >= 0 (M == 0 launches nothing).
+ *  - group_size G (columns per scale) is 128, 64 or 32
+ *    (W4A16_ERR_UNSUPPORTED otherwise; the gfx1151 page's "Benchmark results
+ *    (per-GEMM)" use group_size=32); scales are bf16 [N][K/G].  K must be a
+ *    positive multiple of 128 whatever G is; N >= 1; M >= 0 (M == 0 launches
+ *    nothing).
  *  - X, W_packed and workspace must be 16-byte aligned; scales and Y 2-byte
  *    aligned (W4A16_ERR_INVALID_ARG otherwise).
  */
@@ -45,7 +48,7 @@ typedef uint16_t w4a16_bf16; /* raw bf16 bit pattern */
 typedef enum {
     W4A16_OK = 0,
     W4A16_ERR_INVALID_ARG = 1,          /* null pointer, bad shape, misalignment */
-    W4A16_ERR_UNSUPPORTED = 2,          /* group_size != 128, or an option not available */
+    W4A16_ERR_UNSUPPORTED = 2,          /* group_size not 128, 64 or 32, or an option not available */
     W4A16_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below what the call needs */
     W4A16_ERR_CUDA = 4                  /* a CUDA runtime call or launch failed */
 } w4a16_status;
@@ -74,8 +77,9 @@ enum {
      * of K for a few 16-row blocks of W, its warps split K among themselves
      * and add their partial sums in shared memory, so K is never split across
      * CTAs (no workspace, no reduce kernel); it takes up to 8 tokens whose X
-     * rows fit its shared-memory staging (M * K <= 16384), otherwise the call
-     * returns W4A16_ERR_UNSUPPORTED.  K_SLICES: never that kernel.  Setting
+     * rows fit its shared-memory staging (M * K <= 16384), with 128-wide scale
+     * groups; otherwise the call returns W4A16_ERR_UNSUPPORTED.  K_SLICES:
+     * never that kernel.  Setting
      * both is W4A16_ERR_INVALID_ARG. */
     W4A16_FLAG_DECODE_WHOLE_K = 2,
     W4A16_FLAG_DECODE_K_SLICES = 4
@@ -87,7 +91,8 @@ typedef struct {
     int split_k;      /* 0 = automatic, else the requested number of K slices, clamped to
                          K/128.  The decode arm rounds it up to the nearest count whose
                          slices hold 1, 2, 4, 8 or (up to 8 tokens) 16 of the 128-wide
-                         groups each. */
+                         blocks each (with G < 128, at most 16 (8 tokens) or 8 scale
+                         groups per slice). */
     int tile_tokens;  /* tensor arm only: 0 = automatic, else tokens per tile (32..256, multiple of 32) */
     int flags;        /* W4A16_FLAG_* bits; unknown bits are rejected (W4A16_ERR_INVALID_ARG) */
 } w4a16_options;
@@ -120,8 +125,9 @@ size_t w4a16_packed_weight_bytes(int N, int K);
  *            BF16xINT4 ...", "Fused A-operand dot": low nibble <-> even K).
  *  w_packed: device, w4a16_packed_weight_bytes(N, K) bytes, written fully
  *            (padding rows hold code 8, i.e. weight 0).  Must not overlap
- *            w_canon.  The scales need no repacking: every entry point takes
- *            them as bf16 [N][K/128].
+ *            w_canon.  The packed layout does not depend on the group size,
+ *            and the scales need no repacking: every entry point takes them
+ *            as bf16 [N][K/G].
  * The CUTLASS path that page mentions also preshuffles the weights; this
  * layout is this library's own. */
 w4a16_status w4a16_pack_weights(const uint8_t *w_canon, uint8_t *w_packed, int N, int K,
@@ -140,9 +146,9 @@ w4a16_status w4a16_workspace_bytes(int M, int N, int K, int group_size, size_t *
 /* Y = X . dequant(W)^T.
  *  X:        device bf16 [M][K].          Y: device bf16 [M][N].
  *  W_packed: output of w4a16_pack_weights for (N, K).
- *  scales:   device bf16 [N][K/128].
+ *  scales:   device bf16 [N][K/G], G = group_size.
  *  workspace/workspace_bytes: device scratch of at least
- *            w4a16_workspace_bytes(M, N, K, 128) bytes (may be NULL when
+ *            w4a16_workspace_bytes(M, N, K, G) bytes (may be NULL when
  *            that is 0).  Its contents need no initialisation.
  * Split-K calls enqueue two kernels (partial products into the workspace,
  * then a reduce that sums the slices in order 0..SPLIT_K-1 and rounds to
@@ -177,7 +183,7 @@ w4a16_status w4a16_gemm_partials(const w4a16_bf16 *X, const uint8_t *W_packed,
  * launch): for b < batch, Y[b] = X[b] . dequant(W[b])^T.
  *  X:        device bf16 [batch][M][K].      Y: device bf16 [batch][M][N].
  *  W_packed: batch consecutive blocks, each w4a16_packed_weight_bytes(N, K).
- *  scales:   device bf16 [batch][N][K/128].
+ *  scales:   device bf16 [batch][N][K/G].
  *  workspace/workspace_bytes: at least the workspace_bytes w4a16_plan_batched
  *            reports (split-K partials [SPLIT_K][batch][M][N]; 0 without a
  *            split); contents need no initialisation.
@@ -205,7 +211,7 @@ w4a16_status w4a16_grouped_workspace_bytes(int num_groups, int M_total, int N, i
  * scale block g.
  *  X:         device bf16 [M_total][K].   Y: device bf16 [M_total][N].
  *  W_packed:  num_groups consecutive blocks, each w4a16_packed_weight_bytes(N, K).
- *  scales:    device bf16 [num_groups][N][K/128].
+ *  scales:    device bf16 [num_groups][N][K/G].
  *  M_sizes_dev: device int32 [num_groups]; read only by the kernel (the host
  *             never reads it, so the call needs no synchronisation).
  *  workspace: >= w4a16_grouped_workspace_bytes(...) bytes.  The kernel writes
@@ -220,7 +226,7 @@ w4a16_status w4a16_gemm_grouped(const w4a16_bf16 *X, const uint8_t *W_packed,
                                 int group_size, void *workspace, size_t workspace_bytes,
                                 void *stream);
 
-/* Dequantise a packed weight to fp32: out[n][k] = float(scale[n][k/128]) *
+/* Dequantise a packed weight to fp32: out[n][k] = float(scale[n][k/G]) *
  * (code - 8), computed with the same in-register bit trick the GEMM arms use
  * (the code is OR-ed into the bf16 pattern of 128 + n and 136 is subtracted
  * exactly, "[ROCm][Kernel] W4A16 ...", section 1).  Exact: the product of an
@@ -229,7 +235,7 @@ w4a16_status w4a16_dequant_fp32(const uint8_t *W_packed, const w4a16_bf16 *scale
                                 int N, int K, int group_size, void *stream);
 
 /* Dequantise to the bf16 operand the tensor arm feeds its MMAs:
- * out[n][k] = bf16_rne(scale[n][k/128] * (code - 8)).  out: device bf16 [N][K]. */
+ * out[n][k] = bf16_rne(scale[n][k/G] * (code - 8)).  out: device bf16 [N][K]. */
 w4a16_status w4a16_dequant_bf16(const uint8_t *W_packed, const w4a16_bf16 *scales,
                                 w4a16_bf16 *out, int N, int K, int group_size, void *stream);
 

@@ -73,8 +73,11 @@ def gemm(L, X=FAKE, W=FAKE, S=FAKE, Y=FAKE, M=4, N=256, K=512, G=128, ws=None, w
 
 
 def test_gemm_argument_checks(L):
-    assert gemm(L, G=64) == UNSUPPORTED
-    assert gemm(L, G=32) == UNSUPPORTED
+    # group sizes 128, 64 and 32 are served (M == 0 needs no device); others are not
+    for G in (128, 64, 32):
+        assert gemm(L, M=0, G=G) == OK
+    for G in (16, 96, 256, 0, -128):
+        assert gemm(L, G=G) == UNSUPPORTED
     assert gemm(L, K=500) == INVALID
     assert gemm(L, K=0) == INVALID
     assert gemm(L, K=64) == INVALID
@@ -97,7 +100,8 @@ def test_other_entry_points_check_arguments(L):
     assert L.w4a16_pack_weights(FAKE, FAKE, 16, 100, None) == INVALID
     assert L.w4a16_pack_weights(FAKE, FAKE + 8, 16, 128, None) == INVALID
     assert L.w4a16_dequant_fp32(FAKE, FAKE, None, 16, 128, 128, None) == INVALID
-    assert L.w4a16_dequant_fp32(FAKE, FAKE, FAKE, 16, 128, 64, None) == UNSUPPORTED
+    assert L.w4a16_dequant_fp32(FAKE, FAKE, FAKE, 16, 128, 256, None) == UNSUPPORTED
+    assert L.w4a16_dequant_fp32(FAKE, FAKE, FAKE, 16, 128, 48, None) == UNSUPPORTED
     assert L.w4a16_dequant_bf16(None, FAKE, FAKE, 16, 128, 128, None) == INVALID
     assert L.w4a16_splitk_reduce(None, FAKE, 2, 4, 4, None) == INVALID
     assert L.w4a16_splitk_reduce(FAKE, FAKE, 0, 4, 4, None) == INVALID
@@ -107,7 +111,8 @@ def test_other_entry_points_check_arguments(L):
     assert L.w4a16_grouped_workspace_bytes(8, 4096, 2048, 4096, 128, ctypes.byref(nb)) == OK
     assert nb.value >= 4
     assert L.w4a16_grouped_workspace_bytes(0, 4096, 2048, 4096, 128, ctypes.byref(nb)) == INVALID
-    assert L.w4a16_grouped_workspace_bytes(8, 4096, 2048, 4096, 64, ctypes.byref(nb)) == UNSUPPORTED
+    assert L.w4a16_grouped_workspace_bytes(8, 4096, 2048, 4096, 256, ctypes.byref(nb)) == UNSUPPORTED
+    assert L.w4a16_grouped_workspace_bytes(8, 4096, 2048, 4096, 32, ctypes.byref(nb)) == OK
     assert L.w4a16_workspace_bytes(1, 256, 512, 128, None) == INVALID
     assert L.w4a16_gemm_grouped(None, FAKE, FAKE, FAKE, FAKE, 8, 64, 256, 512, 128, FAKE, 16,
                                 None) == INVALID
@@ -148,7 +153,7 @@ def test_batched_entry_points_check_arguments(L):
     info = _lib.PlanInfo()
     for batch in (0, -1, 1025):
         assert L.w4a16_plan_batched(batch, 4, 256, 512, 128, None, ctypes.byref(info)) == INVALID
-    assert L.w4a16_plan_batched(2, 4, 256, 512, 64, None, ctypes.byref(info)) == UNSUPPORTED
+    assert L.w4a16_plan_batched(2, 4, 256, 512, 256, None, ctypes.byref(info)) == UNSUPPORTED
     assert L.w4a16_plan_batched(2, 4, 256, 500, 128, None, ctypes.byref(info)) == INVALID
     # batch * M beyond 2^24 rows
     assert L.w4a16_plan_batched(1024, 1 << 15, 256, 512, 128, None, ctypes.byref(info)) == INVALID
