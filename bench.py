@@ -432,7 +432,8 @@ def per_shape_table(torch, w4, syn, metrics, device, peaks, only=None, group_siz
     for name, lst in (("decode_gemv", syn.WORKLOADS["decode_gemv"]),
                       ("decode_sweep_gate_up", syn.WORKLOADS["decode_sweep_gate_up"]),
                       ("decode_sweep_down", syn.WORKLOADS["decode_sweep_down"]),
-                      ("prefill", syn.WORKLOADS["prefill"])):
+                      ("prefill", syn.WORKLOADS["prefill"]),
+                      ("prefill_long", syn.WORKLOADS["prefill_long"])):
         shapes += [(name, M, N, K, 128) for (M, N, K) in lst]
     shapes += [(name, M, N, K, 32) for (name, M, N, K) in GROUP32_SHAPES]
     if only is not None:

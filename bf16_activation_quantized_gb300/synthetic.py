@@ -123,5 +123,9 @@ WORKLOADS = {
     "decode_sweep_gate_up": [(m, 19456, 2560) for m in (1, 8, 16, 32, 64, 128)],
     "decode_sweep_down": [(m, 2560, 9728) for m in (1, 8, 16, 32, 64, 128)],
     "prefill": [(1322, 19456, 2560), (1322, 2560, 9728)],
+    # Longer prefills on the same projections: the end-to-end prefill of the
+    # gfx1151 page runs about 2858 tokens, the rowwise-GEMM page's prefill rows
+    # use 2048 and 4096.
+    "prefill_long": [(m, n, k) for m in (2048, 2858, 4096) for (n, k) in ((19456, 2560), (2560, 9728))],
 }
 GROUPED_WORKLOAD = dict(num_groups=8, M_total=4096, N=2048, K=4096)
