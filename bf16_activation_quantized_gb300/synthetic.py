@@ -95,6 +95,14 @@ def make_gemm_inputs(M: int, N: int, K: int, G: int = GROUP, seed: int = 0) -> G
     return GemmInputs(x=x, w_canon=w, scales=s, M=M, N=N, K=K, G=G)
 
 
+def make_zeros(N: int, K: int, G: int = GROUP, seed: int = 0) -> np.ndarray:
+    """Zero points for the asymmetric variant: uint8 [N, K/G], uniform integers
+    0..15, from a generator of their own (seed + 7919), so the other inputs of
+    a seed are unchanged."""
+    rng = np.random.default_rng(seed + 7919)
+    return rng.integers(0, 16, size=(N, K // G), dtype=np.uint8)
+
+
 def draw_group_sizes(rng, num_groups: int, M_total: int) -> np.ndarray:
     while True:
         sizes = rng.multinomial(M_total, [1.0 / num_groups] * num_groups)

@@ -72,6 +72,13 @@ def _load():
         lib.oracle_gemm_grouped_f64.restype = None
         lib.oracle_sum_slices_f64.argtypes = [P, L, L, P]
         lib.oracle_sum_slices_f64.restype = None
+        lib.oracle_weight_zp.argtypes = [P, P, P, L, L, L, L]
+        lib.oracle_weight_zp.restype = ctypes.c_double
+        for name in ("oracle_dequant_zp_f32", "oracle_dequant_zp_bf16"):
+            getattr(lib, name).argtypes = [P, P, P, L, L, L, P]
+            getattr(lib, name).restype = None
+        lib.oracle_gemm_zp_f64.argtypes = [P, P, P, P, L, L, L, L, P, I]
+        lib.oracle_gemm_zp_f64.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = I
         _lib = lib
@@ -145,6 +152,30 @@ def gemm_cols(x, w_canon, scales, M, N, K, n_lo, n_hi, G=128, threads: int = 0) 
     _load().oracle_gemm_cols_f64(_ptr(x), _ptr(w), _ptr(s), M, N, K, G, n_lo, n_hi,
                                  _ptr(y), threads)
     return y
+
+
+def gemm_zp(x, w_canon, scales, zeros, M, N, K, G=128, threads: int = 0) -> np.ndarray:
+    """Y[M, N] in fp64 with a zero point per scale group:
+    dequant = scale[n, k // G] * (nib - (zeros[n, k // G] & 15)); zeros uint8 [N, K/G]."""
+    x, w, s, z = _u16(x), _u8(w_canon), _u16(scales), _u8(zeros)
+    y = np.zeros((M, N), dtype=np.float64)
+    _load().oracle_gemm_zp_f64(_ptr(x), _ptr(w), _ptr(s), _ptr(z), M, N, K, G, _ptr(y), threads)
+    return y
+
+
+def dequant_zp_f32(w_canon, scales, zeros, N, K, G=128) -> np.ndarray:
+    w, s, z = _u8(w_canon), _u16(scales), _u8(zeros)
+    out = np.empty((N, K), dtype=np.float32)
+    _load().oracle_dequant_zp_f32(_ptr(w), _ptr(s), _ptr(z), N, K, G, _ptr(out))
+    return out
+
+
+def dequant_zp_bf16(w_canon, scales, zeros, N, K, G=128) -> np.ndarray:
+    """bf16 bit patterns of round-to-nearest-even(scale * (nib - zero))."""
+    w, s, z = _u8(w_canon), _u16(scales), _u8(zeros)
+    out = np.empty((N, K), dtype=np.uint16)
+    _load().oracle_dequant_zp_bf16(_ptr(w), _ptr(s), _ptr(z), N, K, G, _ptr(out))
+    return out
 
 
 def group_starts(m_sizes) -> np.ndarray:

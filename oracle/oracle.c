@@ -166,6 +166,56 @@ void oracle_gemm_cols_f64(const uint16_t *x, const uint8_t *w_canon, const uint1
     }
 }
 
+/* ---- Asymmetric variant (zero points) -------------------------------------
+ * The pages state only the symmetric form, scale * (n - 8).  The variant with
+ * a zero point per scale group is a reading (listed in the design notes): the
+ * usual int4 convention of a 4-bit integer zero z per (row, group),
+ *
+ *   Wd[n][k] = scale[n][k / G] * (nib(n, k) - z[n][k / G]),
+ *
+ * z held in the low four bits of one byte per group (zeros: uint8 [N][K/G]).
+ * With every z = 8 it is the symmetric form. */
+double oracle_weight_zp(const uint8_t *w_canon, const uint16_t *scales, const uint8_t *zeros,
+                        long K, long G, long n, long k)
+{
+    long gi = n * (K / G) + k / G;
+    double s = oracle_bf16_to_f64(scales[gi]);
+    return s * (double)(oracle_nibble(w_canon, K, n, k) - (int)(zeros[gi] & 0x0F));
+}
+
+void oracle_dequant_zp_f32(const uint8_t *w_canon, const uint16_t *scales, const uint8_t *zeros,
+                           long N, long K, long G, float *out)
+{
+    for (long n = 0; n < N; ++n)
+        for (long k = 0; k < K; ++k)
+            out[n * K + k] = (float)oracle_weight_zp(w_canon, scales, zeros, K, G, n, k);
+}
+
+void oracle_dequant_zp_bf16(const uint8_t *w_canon, const uint16_t *scales, const uint8_t *zeros,
+                            long N, long K, long G, uint16_t *out)
+{
+    for (long n = 0; n < N; ++n)
+        for (long k = 0; k < K; ++k)
+            out[n * K + k] = oracle_f64_to_bf16(oracle_weight_zp(w_canon, scales, zeros, K, G, n, k));
+}
+
+void oracle_gemm_zp_f64(const uint16_t *x, const uint8_t *w_canon, const uint16_t *scales,
+                        const uint8_t *zeros, long M, long N, long K, long G, double *y,
+                        int threads)
+{
+    set_threads(threads);
+    #pragma omp parallel for collapse(2) schedule(static)
+    for (long m = 0; m < M; ++m) {
+        for (long n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (long k = 0; k < K; ++k)
+                acc += oracle_bf16_to_f64(x[m * K + k]) *
+                       oracle_weight_zp(w_canon, scales, zeros, K, G, n, k);
+            y[m * N + n] = acc;
+        }
+    }
+}
+
 /* Row starts of each group: the exclusive prefix sum of the (clamped) sizes. */
 void oracle_group_starts(const int32_t *m_sizes, long num_groups, int64_t *starts)
 {

@@ -440,3 +440,100 @@ def _mutant_fails_pins(lib):
 def test_planted_mistake_is_caught(tmp_path, name):
     lib = _build_mutant(tmp_path, name)
     assert _mutant_fails_pins(lib), f"planted mistake {name} slipped through the pins"
+
+
+# ------------------------------------------------------- zero points (variant)
+def np_gemm_zp(x, w_canon, scales, zeros, K, G):
+    s = np.repeat(np_bf16(scales), G, axis=-1)
+    z = np.repeat((zeros & 0x0F).astype(np.int64), G, axis=-1)
+    return np_bf16(x) @ (s * (np_codes(w_canon, K) - z).astype(np.float64)).T
+
+
+@pytest.mark.parametrize("G", [128, 64, 32])
+@pytest.mark.parametrize("M,N,K,seed", [(1, 16, 128, 0), (3, 33, 256, 1), (5, 7, 384, 2)])
+def test_oracle_zp_matches_numpy_bruteforce(M, N, K, G, seed):
+    inp = syn.make_gemm_inputs(M, N, K, G=G, seed=seed)
+    z = syn.make_zeros(N, K, G, seed=seed)
+    y = oracle.gemm_zp(inp.x, inp.w_canon, inp.scales, z, M, N, K, G=G)
+    ref = np_gemm_zp(inp.x, inp.w_canon, inp.scales, z, K, G)
+    assert np.max(np.abs(y - ref)) <= 1e-12 * max(np.max(np.abs(ref)), 1e-300)
+
+
+@pytest.mark.parametrize("G", [128, 32])
+def test_zero_point_eight_is_symmetric(G):
+    inp = syn.make_gemm_inputs(3, 40, 384, G=G, seed=13)
+    eights = np.full((40, 384 // G), 8, dtype=np.uint8)
+    assert np.array_equal(oracle.gemm_zp(inp.x, inp.w_canon, inp.scales, eights, 3, 40, 384, G=G),
+                          oracle.gemm(inp.x, inp.w_canon, inp.scales, 3, 40, 384, G=G))
+
+
+def test_zero_point_one_hot_closed_form():
+    # Unit scales, X one-hot at k0: Y[m][n] = code(n, k0) - z(n, k0 / G) exactly.
+    M, N, K, G = 1, 20, 256, 32
+    inp = syn.make_gemm_inputs(M, N, K, G=G, seed=14)
+    z = syn.make_zeros(N, K, G, seed=14)
+    ones = np.full_like(inp.scales, 0x3F80)
+    codes = np_codes(inp.w_canon, K)
+    for k0 in [0, 31, 32, 100, 255]:
+        x = np.zeros((M, K), dtype=np.uint16)
+        x[0, k0] = 0x3F80
+        y = oracle.gemm_zp(x, inp.w_canon, ones, z, M, N, K, G=G)
+        assert np.array_equal(y[0], (codes[:, k0] - z[:, k0 // G]).astype(np.float64))
+
+
+def test_codes_equal_to_zero_point_give_zero():
+    inp = syn.make_gemm_inputs(2, 24, 256, seed=15)
+    for zval in (0, 3, 15):
+        w = np.full_like(inp.w_canon, zval * 0x11)
+        z = np.full((24, 2), zval, dtype=np.uint8)
+        assert np.all(oracle.gemm_zp(inp.x, w, inp.scales, z, 2, 24, 256) == 0.0)
+
+
+def test_zero_point_high_bits_ignored():
+    inp = syn.make_gemm_inputs(2, 24, 256, G=64, seed=16)
+    z = syn.make_zeros(24, 256, 64, seed=16)
+    a = oracle.gemm_zp(inp.x, inp.w_canon, inp.scales, z, 2, 24, 256, G=64)
+    b = oracle.gemm_zp(inp.x, inp.w_canon, inp.scales, z | 0xF0, 2, 24, 256, G=64)
+    assert np.array_equal(a, b)
+
+
+def test_dequant_zp_matches_numpy():
+    inp = syn.make_gemm_inputs(1, 40, 384, G=32, seed=17)
+    z = syn.make_zeros(40, 384, 32, seed=17)
+    d = oracle.dequant_zp_f32(inp.w_canon, inp.scales, z, 40, 384, G=32)
+    s = np.repeat(np_bf16(inp.scales), 32, axis=-1)
+    ref = s * (np_codes(inp.w_canon, 384) - np.repeat(z.astype(np.int64), 32, axis=-1))
+    assert np.array_equal(d.astype(np.float64), ref)
+    b = oracle.dequant_zp_bf16(inp.w_canon, inp.scales, z, 40, 384, G=32)
+    assert np.array_equal(b, np.vectorize(oracle.f64_to_bf16)(ref).astype(np.uint16))
+
+
+ZP_MUTANTS = {
+    "zero_ignored": ("- (int)(zeros[gi] & 0x0F)", "- 8"),
+    "zero_sign": ("(oracle_nibble(w_canon, K, n, k) - (int)(zeros[gi] & 0x0F))",
+                  "(oracle_nibble(w_canon, K, n, k) + (int)(zeros[gi] & 0x0F))"),
+    "zero_index": ("long gi = n * (K / G) + k / G;", "long gi = n * (K / G) + k / (2 * G);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ZP_MUTANTS))
+def test_planted_zero_point_mistake_is_caught(tmp_path, name):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    old, new = ZP_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not found"
+    c = tmp_path / f"{name}.c"
+    so = tmp_path / f"{name}.so"
+    c.write_text(src.replace(old, new))
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", str(c), "-o", str(so), "-lm"],
+                   check=True)
+    lib = ctypes.CDLL(str(so))
+    P, L, I = ctypes.c_void_p, ctypes.c_long, ctypes.c_int
+    lib.oracle_gemm_zp_f64.argtypes = [P, P, P, P, L, L, L, L, P, I]
+    M, N, K, G = 3, 16, 256, 32
+    inp = syn.make_gemm_inputs(M, N, K, G=G, seed=22)
+    z = syn.make_zeros(N, K, G, seed=22)
+    y = np.zeros((M, N))
+    lib.oracle_gemm_zp_f64(*(a.ctypes.data_as(P) for a in (inp.x, inp.w_canon, inp.scales, z)),
+                           M, N, K, G, y.ctypes.data_as(P), 1)
+    ref = np_gemm_zp(inp.x, inp.w_canon, inp.scales, z, K, G)
+    assert not np.max(np.abs(y - ref)) <= 1e-12 * np.max(np.abs(ref)), f"{name} slipped through"
