@@ -45,6 +45,7 @@ def _need_cuda(t: torch.Tensor, name: str, dtype=None):
 FLAG_RESIDENT_WEIGHTS = 1
 FLAG_DECODE_WHOLE_K = 2
 FLAG_DECODE_K_SLICES = 4
+FLAG_ZERO_POINTS = 8
 _KERNELS = {None: 0, "auto": 0, "whole_k": FLAG_DECODE_WHOLE_K, "k_slices": FLAG_DECODE_K_SLICES}
 
 
@@ -56,12 +57,13 @@ def _group_size(K: int, cols: int, what: str) -> int:
     return K // cols
 
 
-def _opts(arm, split_k, tile_tokens, resident_weights=False, decode_kernel=None):
+def _opts(arm, split_k, tile_tokens, resident_weights=False, decode_kernel=None, zero_points=False):
     if arm not in _ARMS:
         raise ValueError(f"arm must be one of {list(_ARMS)}")
     if decode_kernel not in _KERNELS:
         raise ValueError(f"decode_kernel must be one of {list(_KERNELS)}")
-    flags = (FLAG_RESIDENT_WEIGHTS if resident_weights else 0) | _KERNELS[decode_kernel]
+    flags = ((FLAG_RESIDENT_WEIGHTS if resident_weights else 0) | _KERNELS[decode_kernel]
+             | (FLAG_ZERO_POINTS if zero_points else 0))
     return Options(_ARMS[arm], int(split_k), int(tile_tokens), flags)
 
 
@@ -127,10 +129,11 @@ def pack(w_canon: torch.Tensor) -> torch.Tensor:
 
 
 def plan(M: int, N: int, K: int, arm=None, split_k: int = 0, tile_tokens: int = 0,
-         device=None, decode_kernel=None, group_size: int = GROUP) -> dict:
+         device=None, decode_kernel=None, group_size: int = GROUP,
+         zero_points: bool = False) -> dict:
     """What the dispatcher picks for this shape on the (current) device."""
     info = PlanInfo()
-    o = _opts(arm, split_k, tile_tokens, decode_kernel=decode_kernel)
+    o = _opts(arm, split_k, tile_tokens, decode_kernel=decode_kernel, zero_points=zero_points)
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         _lib.check(_lib.lib().w4a16_plan(M, N, K, group_size, ctypes.byref(o), ctypes.byref(info)),
                    "w4a16_plan")
@@ -142,8 +145,11 @@ def plan(M: int, N: int, K: int, arm=None, split_k: int = 0, tile_tokens: int = 
 def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=None,
          split_k: int = 0, tile_tokens: int = 0, out: torch.Tensor | None = None,
          workspace: torch.Tensor | None = None, resident_weights: bool = False,
-         decode_kernel=None) -> torch.Tensor:
+         decode_kernel=None, zeros: torch.Tensor | None = None) -> torch.Tensor:
     """Y = X . dequant(W)^T.  x: bf16 [M, K]; scales: bf16 [N, K/G]; returns bf16 [M, N].
+
+    ``zeros`` (uint8 [N, K/G], low four bits) selects the zero-point variant,
+    dequant = scale * (code - z) (w4a16_gemm_zp); without it z is 8.
 
     ``resident_weights=True`` promises that no kernel still running on the
     current stream writes ``w_packed`` or ``scales`` (W4A16_FLAG_RESIDENT_WEIGHTS):
@@ -157,11 +163,15 @@ def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=N
     G = _group_size(K, scales.shape[1], "scales [N, K/G]")
     if w_packed.numel() < packed_weight_bytes(N, K):
         raise ValueError("w_packed is smaller than packed_weight_bytes(N, K)")
+    if zeros is not None:
+        _need_cuda(zeros, "zeros", torch.uint8)
+        if tuple(zeros.shape) != tuple(scales.shape):
+            raise ValueError("zeros must be uint8 [N, K/G], the shape of scales")
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     else:
         _need_cuda(out, "out", torch.bfloat16)
-    o = _opts(arm, split_k, tile_tokens, resident_weights, decode_kernel)
+    o = _opts(arm, split_k, tile_tokens, resident_weights, decode_kernel, zeros is not None)
     L = _lib.lib()
     dev = x.device
     switch = dev.index != torch.cuda.current_device()
@@ -176,10 +186,15 @@ def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=N
             ws = workspace
         ws_ptr = ws.data_ptr() if ws is not None else None
         ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
-        _lib.check(L.w4a16_gemm_ex(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(),
-                                   out.data_ptr(), M, N, K, G, ws_ptr, ws_bytes,
-                                   ctypes.byref(o), torch.cuda.current_stream(dev).cuda_stream),
-                   "w4a16_gemm_ex")
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        if zeros is None:
+            _lib.check(L.w4a16_gemm_ex(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(),
+                                       out.data_ptr(), M, N, K, G, ws_ptr, ws_bytes,
+                                       ctypes.byref(o), stream), "w4a16_gemm_ex")
+        else:
+            _lib.check(L.w4a16_gemm_zp(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(),
+                                       zeros.data_ptr(), out.data_ptr(), M, N, K, G, ws_ptr,
+                                       ws_bytes, ctypes.byref(o), stream), "w4a16_gemm_zp")
     finally:
         if switch:
             torch.cuda.set_device(prev)
@@ -296,34 +311,50 @@ def gemm_grouped(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor,
 
 
 def dequant_fp32(w_packed: torch.Tensor, scales: torch.Tensor,
-                 group_size: int = GROUP) -> torch.Tensor:
+                 group_size: int = GROUP, zeros: torch.Tensor | None = None) -> torch.Tensor:
     """fp32 [N, K] = scale * (code - 8), computed by the kernels' bit trick;
-    scales bf16 [N, K/G] with G = group_size."""
+    scales bf16 [N, K/G] with G = group_size; with ``zeros`` (uint8 [N, K/G])
+    scale * (code - z)."""
     _need_cuda(w_packed, "w_packed", torch.uint8)
     _need_cuda(scales, "scales", torch.bfloat16)
     N, kg = scales.shape
     K = kg * group_size
     out = torch.empty((N, K), dtype=torch.float32, device=scales.device)
     with torch.cuda.device(scales.device):
-        _lib.check(_lib.lib().w4a16_dequant_fp32(w_packed.data_ptr(), scales.data_ptr(),
-                                                 out.data_ptr(), N, K, group_size,
-                                                 _stream_ptr(scales.device)), "w4a16_dequant_fp32")
+        if zeros is None:
+            _lib.check(_lib.lib().w4a16_dequant_fp32(w_packed.data_ptr(), scales.data_ptr(),
+                                                     out.data_ptr(), N, K, group_size,
+                                                     _stream_ptr(scales.device)), "w4a16_dequant_fp32")
+        else:
+            _need_cuda(zeros, "zeros", torch.uint8)
+            _lib.check(_lib.lib().w4a16_dequant_zp_fp32(w_packed.data_ptr(), scales.data_ptr(),
+                                                        zeros.data_ptr(), out.data_ptr(), N, K,
+                                                        group_size, _stream_ptr(scales.device)),
+                       "w4a16_dequant_zp_fp32")
     return out
 
 
 def dequant_bf16(w_packed: torch.Tensor, scales: torch.Tensor,
-                 group_size: int = GROUP) -> torch.Tensor:
+                 group_size: int = GROUP, zeros: torch.Tensor | None = None) -> torch.Tensor:
     """bf16 [N, K] = round_nearest_even(scale * (code - 8)): the tensor arm's
-    operand; scales bf16 [N, K/G] with G = group_size."""
+    operand; scales bf16 [N, K/G] with G = group_size; with ``zeros``
+    scale * (code - z)."""
     _need_cuda(w_packed, "w_packed", torch.uint8)
     _need_cuda(scales, "scales", torch.bfloat16)
     N, kg = scales.shape
     K = kg * group_size
     out = torch.empty((N, K), dtype=torch.bfloat16, device=scales.device)
     with torch.cuda.device(scales.device):
-        _lib.check(_lib.lib().w4a16_dequant_bf16(w_packed.data_ptr(), scales.data_ptr(),
-                                                 out.data_ptr(), N, K, group_size,
-                                                 _stream_ptr(scales.device)), "w4a16_dequant_bf16")
+        if zeros is None:
+            _lib.check(_lib.lib().w4a16_dequant_bf16(w_packed.data_ptr(), scales.data_ptr(),
+                                                     out.data_ptr(), N, K, group_size,
+                                                     _stream_ptr(scales.device)), "w4a16_dequant_bf16")
+        else:
+            _need_cuda(zeros, "zeros", torch.uint8)
+            _lib.check(_lib.lib().w4a16_dequant_zp_bf16(w_packed.data_ptr(), scales.data_ptr(),
+                                                        zeros.data_ptr(), out.data_ptr(), N, K,
+                                                        group_size, _stream_ptr(scales.device)),
+                       "w4a16_dequant_zp_bf16")
     return out
 
 

@@ -39,10 +39,13 @@ SIGNATURES = {
                                 ctypes.POINTER(I), P]),
     "w4a16_plan_batched": (I, [I, I, I, I, I, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]),
     "w4a16_gemm_batched": (I, [P, P, P, P, I, I, I, I, I, P, SZ, ctypes.POINTER(Options), P]),
+    "w4a16_gemm_zp": (I, [P, P, P, P, P, I, I, I, I, P, SZ, ctypes.POINTER(Options), P]),
     "w4a16_grouped_workspace_bytes": (I, [I, I, I, I, I, ctypes.POINTER(SZ)]),
     "w4a16_gemm_grouped": (I, [P, P, P, P, P, I, I, I, I, I, P, SZ, P]),
     "w4a16_dequant_fp32": (I, [P, P, P, I, I, I, P]),
     "w4a16_dequant_bf16": (I, [P, P, P, I, I, I, P]),
+    "w4a16_dequant_zp_fp32": (I, [P, P, P, P, I, I, I, P]),
+    "w4a16_dequant_zp_bf16": (I, [P, P, P, P, I, I, I, P]),
     "w4a16_splitk_reduce": (I, [P, P, I, I, I, P]),
     "w4a16_gemm_noalloc": (I, [P, P, P, P, I, I, I, I, P]),
 }

@@ -117,8 +117,10 @@ double decode_slice_preference(int gps) {
 // octets) and have only the slice kernel; their scale bytes (2 per group)
 // scale the modelled weight stream relative to 128-wide groups, for which the
 // constants were measured.
+// zp: the zero-point kernels, which hold half as many scale groups of a row
+// per slice (their zero points sit in registers too).
 void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int batch, int sub,
-                 DecodePlan *d) {
+                 bool zp, DecodePlan *d) {
     const int groups = K / kGroup;
     const double sbytes = (0.5 + 2.0 * sub / kGroup) / (0.5 + 2.0 / kGroup);
     d->mt = M <= 8 ? 1 : 2;
@@ -136,7 +138,7 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int bat
     d->ring = kDecodeRing;
     d->in_flight = kDecodeInFlight;
     d->wk_blocks = 0;
-    if (wk != 2 && forced_split <= 1 && sub == 1) {
+    if (wk != 2 && forced_split <= 1 && sub == 1 && !zp) {
         // (one block per CTA would leave each K-part a single ring slot)
         for (int B : {8, 4, 2}) {
             if (!decode_wk_fits(M, K, B)) continue;
@@ -156,12 +158,12 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int bat
         }
         if (wk == 1) return;
     }
-    if (wk == 1) return;   // (smaller groups: no whole-K kernel)
+    if (wk == 1) return;   // (smaller groups, zero points: no whole-K kernel)
     // Slices hold 1, 2, 4, 8 or 16 groups and divide K exactly (the kernel
     // unrolls a slice at compile time).  A forced split picks the feasible slice count
     // closest to the request from above.
     // 16-group slices only for one token octet (register budget).
-    const int gps_max = (d->mt == 1 ? 16 : 8) / sub;
+    const int gps_max = (d->mt == 1 ? 16 : 8) / sub / (zp ? 2 : 1);
     int forced_gps = 0;
     if (forced_split > 0) {
         for (int gps : {16, 8, 4, 2, 1})
@@ -326,14 +328,18 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
 // sub: scale groups per 128-wide block (128 / group_size).
 w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, int batch = 1,
                        int sub = 1) {
+    // (W4A16_FLAG_ZERO_POINTS: plan the zero-point kernels)
     std::memset(p, 0, sizeof *p);
     int arm = opts ? opts->arm : W4A16_ARM_AUTO;
     if (arm != W4A16_ARM_AUTO && arm != W4A16_ARM_DECODE && arm != W4A16_ARM_TENSOR)
         return W4A16_ERR_INVALID_ARG;
     if (opts && opts->split_k < 0) return W4A16_ERR_INVALID_ARG;
     const int flags = opts ? opts->flags : 0;
-    if (flags & ~int(W4A16_FLAG_RESIDENT_WEIGHTS | W4A16_FLAG_DECODE_WHOLE_K | W4A16_FLAG_DECODE_K_SLICES))
+    if (flags & ~int(W4A16_FLAG_RESIDENT_WEIGHTS | W4A16_FLAG_DECODE_WHOLE_K | W4A16_FLAG_DECODE_K_SLICES |
+                     W4A16_FLAG_ZERO_POINTS))
         return W4A16_ERR_INVALID_ARG;
+    const bool zp = (flags & W4A16_FLAG_ZERO_POINTS) != 0;
+    if (zp && batch > 1) return W4A16_ERR_UNSUPPORTED;
     if ((flags & W4A16_FLAG_DECODE_WHOLE_K) && (flags & W4A16_FLAG_DECODE_K_SLICES))
         return W4A16_ERR_INVALID_ARG;
     const int wk = (flags & W4A16_FLAG_DECODE_WHOLE_K) ? 1 : (flags & W4A16_FLAG_DECODE_K_SLICES) ? 2 : 0;
@@ -347,7 +353,7 @@ w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, 
     p->arm = arm;
     if (arm == W4A16_ARM_DECODE) {
         DecodePlan &d = p->decode;
-        plan_decode(M, N, K, sms, opts ? opts->split_k : 0, wk, batch, sub, &d);
+        plan_decode(M, N, K, sms, opts ? opts->split_k : 0, wk, batch, sub, zp, &d);
         if (wk == 1 && d.wk_blocks == 0) return W4A16_ERR_UNSUPPORTED;
         p->split_k = d.split_k;
         p->ctas = batch * (d.wk_blocks ? d.ctas_per_slice : d.ctas_per_slice * d.split_k * d.token_blocks);
@@ -428,11 +434,13 @@ w4a16_status w4a16_workspace_bytes(int M, int N, int K, int group_size, size_t *
     return W4A16_OK;
 }
 
+// zeros != nullptr: the zero-point variant (opts must then carry
+// W4A16_FLAG_ZERO_POINTS, which w4a16_gemm_zp adds).
 static w4a16_status gemm_impl(const w4a16_bf16 *X, const uint8_t *W_packed,
                               const w4a16_bf16 *scales, w4a16_bf16 *Y, int M, int N, int K,
                               int group_size, void *workspace, size_t workspace_bytes,
                               const w4a16_options *opts, bool with_reduce, int *split_out,
-                              void *stream, int batch = 1) {
+                              void *stream, int batch = 1, const uint8_t *zeros = nullptr) {
     w4a16_status st = check_shape(M, N, K, group_size);
     if (st != W4A16_OK) return st;
     if (batch < 1 || batch > kMaxGroups || (long long)batch * M > (1 << 24)) return W4A16_ERR_INVALID_ARG;
@@ -440,6 +448,8 @@ static w4a16_status gemm_impl(const w4a16_bf16 *X, const uint8_t *W_packed,
         if (split_out) *split_out = 1;
         return W4A16_OK;
     }
+    const bool zp_flag = opts && (opts->flags & W4A16_FLAG_ZERO_POINTS);
+    if (zp_flag != (zeros != nullptr)) return W4A16_ERR_INVALID_ARG;
     if (!X || !W_packed || !scales || !Y) return W4A16_ERR_INVALID_ARG;
     if (!aligned(X, 16) || !aligned(W_packed, 16) || !aligned(scales, 2) || !aligned(Y, 2))
         return W4A16_ERR_INVALID_ARG;
@@ -459,10 +469,10 @@ static w4a16_status gemm_impl(const w4a16_bf16 *X, const uint8_t *W_packed,
         e = launch_decode_wk(p.decode.wk_blocks, p.decode.ctas_per_slice, batch, X, W_packed, scales,
                              Y, resident, M, N, K, s);
     else if (p.arm == W4A16_ARM_DECODE)
-        e = launch_decode(p.decode, X, W_packed, scales, Y, ws, resident, M, N, K, s);
+        e = launch_decode(p.decode, X, W_packed, scales, Y, ws, resident, M, N, K, s, zeros);
     else
         e = launch_tensor(p.tensor, X, W_packed, scales, Y, ws, nullptr, nullptr, batch, batch * M, N,
-                          K, s, batch > 1 ? M : 0);
+                          K, s, batch > 1 ? M : 0, zeros);
     if (e != cudaSuccess) return W4A16_ERR_CUDA;
     if (with_reduce && p.split_k > 1) {
         e = launch_reduce(ws, Y, p.split_k, (long long)batch * M * N, true, s);
@@ -519,6 +529,18 @@ w4a16_status w4a16_gemm_batched(const w4a16_bf16 *X, const uint8_t *W_packed,
                                 const w4a16_options *opts, void *stream) {
     return gemm_impl(X, W_packed, scales, Y, M, N, K, group_size, workspace, workspace_bytes, opts,
                      true, nullptr, stream, batch);
+}
+
+w4a16_status w4a16_gemm_zp(const w4a16_bf16 *X, const uint8_t *W_packed, const w4a16_bf16 *scales,
+                           const uint8_t *zeros, w4a16_bf16 *Y, int M, int N, int K,
+                           int group_size, void *workspace, size_t workspace_bytes,
+                           const w4a16_options *opts, void *stream) {
+    if (M > 0 && !zeros) return W4A16_ERR_INVALID_ARG;
+    w4a16_options o = {};
+    if (opts) o = *opts;
+    o.flags |= W4A16_FLAG_ZERO_POINTS;
+    return gemm_impl(X, W_packed, scales, Y, M, N, K, group_size, workspace, workspace_bytes, &o,
+                     true, nullptr, stream, 1, zeros);
 }
 
 w4a16_status w4a16_grouped_workspace_bytes(int num_groups, int M_total, int N, int K,
@@ -582,6 +604,28 @@ w4a16_status w4a16_dequant_bf16(const uint8_t *W_packed, const w4a16_bf16 *scale
         return W4A16_ERR_INVALID_ARG;
     return from_cuda(launch_dequant(W_packed, scales, out, true, N, K, group_size,
                                     static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_dequant_zp_fp32(const uint8_t *W_packed, const w4a16_bf16 *scales,
+                                   const uint8_t *zeros, float *out, int N, int K, int group_size,
+                                   void *stream) {
+    w4a16_status st = check_shape(0, N, K, group_size);
+    if (st != W4A16_OK) return st;
+    if (!W_packed || !scales || !zeros || !out) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(W_packed, 16) || !aligned(scales, 2) || !aligned(out, 4)) return W4A16_ERR_INVALID_ARG;
+    return from_cuda(launch_dequant(W_packed, scales, out, false, N, K, group_size,
+                                    static_cast<cudaStream_t>(stream), zeros));
+}
+
+w4a16_status w4a16_dequant_zp_bf16(const uint8_t *W_packed, const w4a16_bf16 *scales,
+                                   const uint8_t *zeros, w4a16_bf16 *out, int N, int K,
+                                   int group_size, void *stream) {
+    w4a16_status st = check_shape(0, N, K, group_size);
+    if (st != W4A16_OK) return st;
+    if (!W_packed || !scales || !zeros || !out) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(W_packed, 16) || !aligned(scales, 2) || !aligned(out, 2)) return W4A16_ERR_INVALID_ARG;
+    return from_cuda(launch_dequant(W_packed, scales, out, true, N, K, group_size,
+                                    static_cast<cudaStream_t>(stream), zeros));
 }
 
 w4a16_status w4a16_splitk_reduce(const float *ws, w4a16_bf16 *Y, int splits, int M, int N,

@@ -490,19 +490,20 @@ int decode_smem_needed(int M, int mt, int groups_per_slice, int sub) {
 
 cudaError_t launch_decode(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, bool res, int M, int N, int K,
-                          cudaStream_t s) {
+                          cudaStream_t s, const uint8_t *Z) {
     if (p.ring != kRing || p.in_flight < 1 || p.in_flight > p.ring) return cudaErrorInvalidValue;
     if (p.batch < 1 || (long long)p.token_blocks * p.batch > 65535) return cudaErrorInvalidValue;
     if (p.sub != 1 && p.sub != 2 && p.sub != 4) return cudaErrorInvalidValue;
     if (p.groups_per_slice < 1 || p.groups_per_slice > kDecodeMaxGps || p.ctas_per_slice < 1 ||
-        p.groups_per_slice * p.sub > (p.mt == 1 ? 16 : 8) ||
+        p.groups_per_slice * p.sub > (p.mt == 1 ? 16 : 8) / (Z ? 2 : 1) ||
         decode_smem_needed(M, p.mt, p.groups_per_slice, p.sub) > kDecodeMaxSmem ||
         decode_smem_layout(p.mt, M < 8 * p.mt ? M : 8 * p.mt, p.groups_per_slice, p.sub).stages < kRing)
         return cudaErrorInvalidValue;
     if ((K / kGroup) % p.groups_per_slice != 0) return cudaErrorInvalidValue;
+    if (Z) return launch_decode_zp(p, X, Wp, S, Z, Y, ws, res, M, N, K, s);
     if (p.sub == 2) return launch_decode_sub2(p, X, Wp, S, Y, ws, res, M, N, K, s);
     if (p.sub == 4) return launch_decode_sub4(p, X, Wp, S, Y, ws, res, M, N, K, s);
-    return launch_decode_sub<1>(p, X, Wp, S, Y, ws, res, M, N, K, s);
+    return launch_decode_sub<1>(p, X, Wp, S, nullptr, Y, ws, res, M, N, K, s);
 }
 
 bool decode_wk_fits(int M, int K, int B) {

@@ -8,7 +8,7 @@ namespace w4a16 {
 cudaError_t launch_decode_sub4(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
                                const uint16_t *S, uint16_t *Y, float *ws, bool res, int M, int N,
                                int K, cudaStream_t s) {
-    return launch_decode_sub<4>(p, X, Wp, S, Y, ws, res, M, N, K, s);
+    return launch_decode_sub<4>(p, X, Wp, S, nullptr, Y, ws, res, M, N, K, s);
 }
 
 }  // namespace w4a16

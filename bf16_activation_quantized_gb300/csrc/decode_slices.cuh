@@ -171,6 +171,56 @@ __device__ __forceinline__ float scale_of(const ScaleRow<GPS> &r, int gi) {
     return (gi & 1) ? __uint_as_float(r.w[gi / 2] & 0xFFFF0000u) : __uint_as_float(r.w[gi / 2] << 16);
 }
 
+// One weight row's NS zero points of a slice (zero-point variant), one byte
+// each, four to a word (byte i % 4 of word i / 4).  vec: the first byte is
+// aligned to NS bytes (NS <= 8), so one load fetches them.
+template <int NS>
+struct ZeroRow {
+    uint32_t w[(NS + 3) / 4];
+};
+
+template <int NS>
+__device__ __forceinline__ ZeroRow<NS> load_zero_row(const uint8_t *p, bool ok, bool vec) {
+    ZeroRow<NS> r;
+#pragma unroll
+    for (int i = 0; i < (NS + 3) / 4; ++i) r.w[i] = 0;
+    if (!ok) return r;
+    if constexpr (NS == 8) {
+        if (vec) {
+            asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.w[0]), "=r"(r.w[1]) : "l"(p));
+            return r;
+        }
+    } else if constexpr (NS == 4) {
+        if (vec) {
+            asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r.w[0]) : "l"(p));
+            return r;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+        uint32_t v;
+        asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p + i));
+        r.w[i / 4] |= v << (8 * (i & 3));
+    }
+    return r;
+}
+
+// The zero point (low four bits) of scale group i of a row.
+template <int NS>
+__device__ __forceinline__ float zero_of(const ZeroRow<NS> &r, int i) {
+    return float((r.w[i / 4] >> (8 * (i & 3))) & 0xFu);
+}
+
+// Zero points of the rows of weight tile `tile` into L2 (as prefetch_tile_scales).
+__device__ __forceinline__ void prefetch_tile_zeros(const uint8_t *Z, int tile, int N, int n_sg) {
+    const size_t r0 = size_t(tile) * kTileRows;
+    const size_t r1 = min(size_t(N), r0 + kTileRows);
+    if (r0 >= r1) return;
+    const uintptr_t lo = (reinterpret_cast<uintptr_t>(Z + r0 * n_sg) + 15) & ~uintptr_t(15);
+    const uintptr_t hi = reinterpret_cast<uintptr_t>(Z + r1 * n_sg) & ~uintptr_t(15);
+    if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void *>(lo), uint32_t(hi - lo));
+}
+
 // CTA (c, slice, token block): tiles c, c + C, c + 2C, ... of one K slice of
 // GPS groups (GPS divides K/128, so every slice is full).  A producer warp
 // streams the 8 KB (tile, group) blocks, in order, through a ring that holds
@@ -196,12 +246,18 @@ __device__ __forceinline__ float scale_of(const ScaleRow<GPS> &r, int gi) {
 // chain (both the weight words and the staged X are permuted only inside a
 // quarter), so the chain is cut into SUB chains of 4 / SUB steps, each
 // started from its own scale group's correction and scaled by its own scale.
-template <int MT, int GPS, bool kSplit, int SUB>
-__global__ void __launch_bounds__(kDecodeThreads, 2)
-decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
-              const uint16_t *__restrict__ S, uint16_t *__restrict__ Y, float *__restrict__ ws,
-              int M, int N, int K, int n_tiles, int ring_stages, int in_flight, int s_vec,
-              int resident, int token_blocks, int *err) {
+//
+// kZp (zero-point variant, Z = uint8 zero points [N][K/G]): the correction
+// table holds the plain scaled sums S and a chain starts from -(1024 + z) S
+// (rows g) or -(1024 + 16 z) S (rows g + 8), z the row's zero point of the
+// chain's scale group, so it yields sum_k (code_k - z) x_k (times 16).
+// decode_kernel and decode_zp_kernel below are the entry points.
+template <int MT, int GPS, bool kSplit, int SUB, bool kZp>
+__device__ __forceinline__ void
+decode_body(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
+            const uint16_t *__restrict__ S, const uint8_t *__restrict__ Z, uint16_t *__restrict__ Y,
+            float *__restrict__ ws, int M, int N, int K, int n_tiles, int ring_stages, int in_flight,
+            int s_vec, int z_vec, int resident, int token_blocks, int *err) {
     extern __shared__ __align__(128) unsigned char smem[];
     // Batched products: grid.z = entries x token blocks; entry b's X, W,
     // scales, Y and partial sums follow each other in memory.
@@ -211,6 +267,7 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
     X += size_t(bz) * M * K;
     Wp += size_t(bz) * n_tiles * kTileRows * (K / 2);
     S += size_t(bz) * N * (K / kGroup) * SUB;
+    if (kZp) Z += size_t(bz) * N * (K / kGroup) * SUB;
     Y += size_t(bz) * M * N;
 
     const int warp = threadIdx.x >> 5;
@@ -265,7 +322,10 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         }
         // The scales of the first tiles (the consumers load a tile's scales
         // two tiles ahead of its use).
-        for (int it = 0; it < min(n_my, 3); ++it) prefetch_tile_scales(S, c0 + it * C, N, n_sg);
+        for (int it = 0; it < min(n_my, 3); ++it) {
+            prefetch_tile_scales(S, c0 + it * C, N, n_sg);
+            if (kZp) prefetch_tile_zeros(Z, c0 + it * C, N, n_sg);
+        }
         // This CTA's slice of X (a prefetch only warms L2; where the previous
         // kernel writes X, the loads after the dependency wait see its data).
         for (int r = 0; r < rows; ++r)
@@ -276,17 +336,23 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
     const int g = lane >> 2, t = lane & 3;
     const bool vec_scales = s_vec != 0;
     ScaleRow<NSC> s_cur[2], s_next[2];
-    auto load_scales = [&](int tile, ScaleRow<NSC> (&dst)[2]) {
+    ZeroRow<NSC> z_cur[2], z_next[2];     // kZp only
+    auto load_scales = [&](int tile, ScaleRow<NSC> (&dst)[2], ZeroRow<NSC> (&zdst)[2]) {
         const int f0 = tile * kTileRows + warp * 16 + g;
         const uint16_t *p0 = S + size_t(f0) * n_sg + grp0 * SUB;
         dst[0] = load_scale_row<NSC>(p0, f0 < N, vec_scales);
         dst[1] = load_scale_row<NSC>(p0 + 8 * size_t(n_sg), f0 + 8 < N, vec_scales);
+        if constexpr (kZp) {
+            const uint8_t *q0 = Z + size_t(f0) * n_sg + grp0 * SUB;
+            zdst[0] = load_zero_row<NSC>(q0, f0 < N, z_vec != 0);
+            zdst[1] = load_zero_row<NSC>(q0 + 8 * size_t(n_sg), f0 + 8 < N, z_vec != 0);
+        }
     };
     // Read nothing that the previous grid in the stream may write before it
     // has completed: X always, and W and the scales unless they are resident
     // (then only the consumers wait, for X, and they load the first tile's
     // scales before waiting).
-    if (resident && warp < kDecodeWarps && n_my > 0) load_scales(c0, s_cur);
+    if (resident && warp < kDecodeWarps && n_my > 0) load_scales(c0, s_cur, z_cur);
     if (!resident || warp < kDecodeWarps) pdl_wait();
 
     if (warp == kDecodeWarps) {
@@ -322,7 +388,10 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
                     // Entering tile q / GPS: warm L2 with the scales of tile
                     // q / GPS + 3, which the consumers load about two tiles later.
                     const int ahead = (q + 1) / GPS + 3;
-                    if (ahead < n_my) prefetch_tile_scales(S, c0 + ahead * C, N, n_sg);
+                    if (ahead < n_my) {
+                        prefetch_tile_scales(S, c0 + ahead * C, N, n_sg);
+                        if (kZp) prefetch_tile_zeros(Z, c0 + ahead * C, N, n_sg);
+                    }
                 }
                 if (++st == NS) { st = 0; epar ^= 1; }
             }
@@ -360,7 +429,7 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
     if (!resident) {
         // Scales of rows g and g+8 of this warp's block for the first tile,
         // issued before the weight stream starts.
-        if (n_my > 0) load_scales(c0, s_cur);
+        if (n_my > 0) load_scales(c0, s_cur, z_cur);
         named_bar_arrive(2, kDecodeThreads);
     }
 #pragma unroll
@@ -390,7 +459,7 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
             mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         if (i < n_vec && (lane & (lanes_per_row - 1)) == 0) atomicMax(s_xmax + r, int(mx));
     }
-    if (n_my > 1) load_scales(c0 + C, s_next);
+    if (n_my > 1) load_scales(c0 + C, s_next, z_next);
     consumer_bar();
     {
         // Per (token, group): 8 lanes take 16 values each, convert them in
@@ -443,14 +512,16 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
             // SUB == 4: parts 0-3 and 4-7 cover different quarters.
             if (pi < pairs && (part & (SUB == 4 ? 3 : 7)) == 0) {
                 const int ga = gi * SUB + (SUB == 4 ? (part >> 2) : 0);
+                // (kZp: the plain sums; the chains apply their rows' offsets)
+                const float ka = kZp ? 1.f : -1032.f, kb = kZp ? 1.f : -1152.f;
                 float *e = s_corr + ((ga * MT + (r >> 3)) * 4 + ((r & 7) >> 1)) * 4 + (r & 1);
-                e[0] = -1032.f * a;
-                e[2] = -1152.f * a;
+                e[0] = ka * a;
+                e[2] = kb * a;
                 if (SUB > 1) {
                     const int gb = ga + SUB / 2;
                     float *f = s_corr + ((gb * MT + (r >> 3)) * 4 + ((r & 7) >> 1)) * 4 + (r & 1);
-                    f[0] = -1032.f * b;
-                    f[2] = -1152.f * b;
+                    f[0] = ka * b;
+                    f[2] = kb * b;
                 }
             }
         }
@@ -517,10 +588,21 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
                 // scale group gi * SUB + j, loaded a tile ahead.
                 const float s0 = scale_of<NSC>(s_cur[0], gi * SUB + j);
                 const float s1 = scale_of<NSC>(s_cur[1], gi * SUB + j);
+                float kz0 = 0.f, kz1 = 0.f;
+                if constexpr (kZp) {
+                    kz0 = -1024.f - zero_of<NSC>(z_cur[0], gi * SUB + j);
+                    kz1 = fmaf(-16.f, zero_of<NSC>(z_cur[1], gi * SUB + j), -1024.f);
+                }
 #pragma unroll
                 for (int o = 0; o < MT; ++o) {
                     const float4 cc = cs[((gi * SUB + j) * MT + o) * 4];
                     float c[4] = {cc.x, cc.y, cc.z, cc.w};
+                    if constexpr (kZp) {
+                        c[0] *= kz0;
+                        c[1] *= kz0;
+                        c[2] *= kz1;
+                        c[3] *= kz1;
+                    }
 #pragma unroll
                     for (int k16 = j * (4 / SUB); k16 < (j + 1) * (4 / SUB); ++k16) {
                         // Lanes of absent tokens read the last staged row (xrow is
@@ -564,16 +646,45 @@ decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         }
         s_cur[0] = s_next[0];
         s_cur[1] = s_next[1];
-        if (it + 2 < n_my) load_scales(c0 + (it + 2) * C, s_next);
+        if (kZp) {
+            z_cur[0] = z_next[0];
+            z_cur[1] = z_next[1];
+        }
+        if (it + 2 < n_my) load_scales(c0 + (it + 2) * C, s_next, z_next);
     }
 }
 
 template <int MT, int GPS, bool kSplit, int SUB>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
+              const uint16_t *__restrict__ S, uint16_t *__restrict__ Y, float *__restrict__ ws,
+              int M, int N, int K, int n_tiles, int ring_stages, int in_flight, int s_vec,
+              int resident, int token_blocks, int *err) {
+    decode_body<MT, GPS, kSplit, SUB, false>(X, Wp, S, nullptr, Y, ws, M, N, K, n_tiles, ring_stages,
+                                             in_flight, s_vec, 0, resident, token_blocks, err);
+}
+
+template <int MT, int GPS, bool kSplit, int SUB>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+decode_zp_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
+                 const uint16_t *__restrict__ S, const uint8_t *__restrict__ Z,
+                 uint16_t *__restrict__ Y, float *__restrict__ ws, int M, int N, int K, int n_tiles,
+                 int ring_stages, int in_flight, int s_vec, int z_vec, int resident, int token_blocks,
+                 int *err) {
+    decode_body<MT, GPS, kSplit, SUB, true>(X, Wp, S, Z, Y, ws, M, N, K, n_tiles, ring_stages,
+                                            in_flight, s_vec, z_vec, resident, token_blocks, err);
+}
+
+// Z != nullptr: the zero-point kernel (instantiated with kZp).
+template <int MT, int GPS, bool kSplit, int SUB, bool kZp>
 cudaError_t launch_decode_t(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
-                            const uint16_t *S, uint16_t *Y, float *ws, bool resident, int M, int N,
-                            int K, cudaStream_t s) {
+                            const uint16_t *S, const uint8_t *Z, uint16_t *Y, float *ws,
+                            bool resident, int M, int N, int K, cudaStream_t s) {
     const int smem = decode_smem_layout(MT, M < 8 * MT ? M : 8 * MT, GPS, SUB).total;
-    auto kern = decode_kernel<MT, GPS, kSplit, SUB>;
+    auto kern = [] {
+        if constexpr (kZp) return decode_zp_kernel<MT, GPS, kSplit, SUB>;
+        else return decode_kernel<MT, GPS, kSplit, SUB>;
+    }();
     if (smem > 48 * 1024) {
         // Opt in to more than 48 KB of shared memory once per device (not a
         // stream operation, so it is also safe while a graph is being captured).
@@ -603,25 +714,32 @@ cudaError_t launch_decode_t(const DecodePlan &p, const uint16_t *X, const uint8_
     // A slice's scales of one row (GPS * SUB of them) start at a multiple of
     // GPS * SUB elements, in every batch entry.
     const int s_vec = (reinterpret_cast<uintptr_t>(S) % (2 * GPS * SUB)) == 0;
-    return cudaLaunchKernelEx(&cfg, kern, X, Wp, S, Y, ws, M, N, K, p.n_tiles, p.ring, p.in_flight,
-                              s_vec, int(resident), p.token_blocks, err);
+    if constexpr (kZp) {
+        const int z_vec = (reinterpret_cast<uintptr_t>(Z) % (GPS * SUB)) == 0;
+        return cudaLaunchKernelEx(&cfg, kern, X, Wp, S, Z, Y, ws, M, N, K, p.n_tiles, p.ring,
+                                  p.in_flight, s_vec, z_vec, int(resident), p.token_blocks, err);
+    } else {
+        return cudaLaunchKernelEx(&cfg, kern, X, Wp, S, Y, ws, M, N, K, p.n_tiles, p.ring,
+                                  p.in_flight, s_vec, int(resident), p.token_blocks, err);
+    }
 }
 
 // A slice's scales of one row stay in registers (two rows, this tile's and
-// the next one's): at most 16 per row for one token octet, 8 for two.
-template <int MT, int SUB>
+// the next one's): at most 16 per row for one token octet, 8 for two; with
+// zero points (also in registers) half of that.
+template <int MT, int SUB, bool kZp>
 constexpr bool decode_gps_ok(int gps) {
-    return gps * SUB <= (MT == 1 ? 16 : 8);
+    return gps * SUB <= (MT == 1 ? 16 : 8) / (kZp ? 2 : 1);
 }
 
-template <int MT, bool kSplit, int SUB>
+template <int MT, bool kSplit, int SUB, bool kZp>
 cudaError_t launch_decode_gps(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
-                              const uint16_t *S, uint16_t *Y, float *ws, bool res, int M, int N,
-                              int K, cudaStream_t s) {
-#define W4A16_DECODE_GPS_CASE(G)                                                              \
-    case G:                                                                                   \
-        if constexpr (decode_gps_ok<MT, SUB>(G))                                              \
-            return launch_decode_t<MT, G, kSplit, SUB>(p, X, Wp, S, Y, ws, res, M, N, K, s);  \
+                              const uint16_t *S, const uint8_t *Z, uint16_t *Y, float *ws, bool res,
+                              int M, int N, int K, cudaStream_t s) {
+#define W4A16_DECODE_GPS_CASE(G)                                                                  \
+    case G:                                                                                       \
+        if constexpr (decode_gps_ok<MT, SUB, kZp>(G))                                             \
+            return launch_decode_t<MT, G, kSplit, SUB, kZp>(p, X, Wp, S, Z, Y, ws, res, M, N, K, s); \
         return cudaErrorInvalidValue;
     switch (p.groups_per_slice) {
         W4A16_DECODE_GPS_CASE(1)
@@ -634,27 +752,31 @@ cudaError_t launch_decode_gps(const DecodePlan &p, const uint16_t *X, const uint
 #undef W4A16_DECODE_GPS_CASE
 }
 
-template <int SUB>
+template <int SUB, bool kZp = false>
 cudaError_t launch_decode_sub(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
-                              const uint16_t *S, uint16_t *Y, float *ws, bool res, int M, int N,
-                              int K, cudaStream_t s) {
+                              const uint16_t *S, const uint8_t *Z, uint16_t *Y, float *ws, bool res,
+                              int M, int N, int K, cudaStream_t s) {
     const bool split = p.split_k > 1;
     if (p.mt == 1)
-        return split ? launch_decode_gps<1, true, SUB>(p, X, Wp, S, Y, ws, res, M, N, K, s)
-                     : launch_decode_gps<1, false, SUB>(p, X, Wp, S, Y, ws, res, M, N, K, s);
-    return split ? launch_decode_gps<2, true, SUB>(p, X, Wp, S, Y, ws, res, M, N, K, s)
-                 : launch_decode_gps<2, false, SUB>(p, X, Wp, S, Y, ws, res, M, N, K, s);
+        return split ? launch_decode_gps<1, true, SUB, kZp>(p, X, Wp, S, Z, Y, ws, res, M, N, K, s)
+                     : launch_decode_gps<1, false, SUB, kZp>(p, X, Wp, S, Z, Y, ws, res, M, N, K, s);
+    return split ? launch_decode_gps<2, true, SUB, kZp>(p, X, Wp, S, Z, Y, ws, res, M, N, K, s)
+                 : launch_decode_gps<2, false, SUB, kZp>(p, X, Wp, S, Z, Y, ws, res, M, N, K, s);
 }
 
 }  // namespace
 
 // The instantiations for scale groups of 64 (decode_g64.cu) and 32 columns
-// (decode_g32.cu); the plan has been checked by launch_decode.
+// (decode_g32.cu), and the zero-point kernels for every group size
+// (decode_zp.cu); the plan has been checked by launch_decode.
 cudaError_t launch_decode_sub2(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
                                const uint16_t *S, uint16_t *Y, float *ws, bool res, int M, int N,
                                int K, cudaStream_t s);
 cudaError_t launch_decode_sub4(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
                                const uint16_t *S, uint16_t *Y, float *ws, bool res, int M, int N,
                                int K, cudaStream_t s);
+cudaError_t launch_decode_zp(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
+                             const uint16_t *S, const uint8_t *Z, uint16_t *Y, float *ws, bool res,
+                             int M, int N, int K, cudaStream_t s);
 
 }  // namespace w4a16

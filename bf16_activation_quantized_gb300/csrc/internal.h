@@ -56,14 +56,17 @@ cudaError_t launch_decode_wk(int blocks_per_cta, int ctas, int batch, const uint
 size_t packed_bytes(int N, int K);
 
 cudaError_t launch_pack(const uint8_t *w_canon, uint8_t *w_packed, int N, int K, cudaStream_t s);
-// G: scale group size (128, 64 or 32 columns).
+// G: scale group size (128, 64 or 32 columns); Z: zero points uint8 [N][K/G]
+// (nullptr: the symmetric form).
 cudaError_t launch_dequant(const uint8_t *w_packed, const uint16_t *scales, void *out,
-                           bool bf16_out, int N, int K, int G, cudaStream_t s);
+                           bool bf16_out, int N, int K, int G, cudaStream_t s,
+                           const uint8_t *Z = nullptr);
 // resident: the weights and scales are not written by the previous kernel on
 // the stream, so the weight stream may start before that kernel completes.
+// Z: zero points uint8 [N][K/G] (nullptr: the symmetric form, offset 8).
 cudaError_t launch_decode(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, bool resident, int M, int N,
-                          int K, cudaStream_t s);
+                          int K, cudaStream_t s, const uint8_t *Z = nullptr);
 // Tensor arm (tensor.cu).
 constexpr int kTensorMaxSmem = 227 * 1024;     // per-CTA opt-in maximum
 constexpr int kSmemPerSm = 228 * 1024;         // shared memory of one SM
@@ -82,7 +85,7 @@ int tensor_tmem_cols(int bt, int occupancy, bool sep);  // TMEM columns a CTA al
 cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, const int32_t *m_sizes,
                           int *status, int num_groups, int M_total, int N, int K, cudaStream_t s,
-                          int batch_rows = 0);
+                          int batch_rows = 0, const uint8_t *Z = nullptr);   // Z: zero points, plain products
 
 cudaError_t launch_reduce(const float *ws, uint16_t *Y, int splits, long long count, bool pdl,
                           cudaStream_t s);

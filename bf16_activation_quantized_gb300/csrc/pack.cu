@@ -60,9 +60,12 @@ __global__ void pack_kernel(const uint8_t *__restrict__ wc, uint32_t *__restrict
     wp[idx] = w;
 }
 
+// Z (zero-point variant, uint8 [N][K/G], low four bits): weight =
+// scale * (code - z); nullptr: code - 8.
 template <bool kBf16Out>
 __global__ void dequant_kernel(const uint32_t *__restrict__ wp, const uint16_t *__restrict__ S,
-                               void *__restrict__ out, int N, int K, int G, size_t words) {
+                               const uint8_t *__restrict__ Z, void *__restrict__ out, int N, int K,
+                               int G, size_t words) {
     const size_t idx = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= words) return;
     const WordCoord c = word_coord(idx, K / kChunkK);
@@ -77,10 +80,22 @@ __global__ void dequant_kernel(const uint32_t *__restrict__ wp, const uint16_t *
         if (row >= N) continue;
         const uint16_t sbits = S[size_t(row) * groups + grp];
         const size_t o = size_t(row) * K + c.k;
+        const int z = Z ? int(Z[size_t(row) * groups + grp] & 0xF) : 8;
         if (kBf16Out) {
             const uint32_t s2 = uint32_t(sbits) | (uint32_t(sbits) << 16);
             uint32_t p01, p23;
-            dequant_word_row_scaled(w, half, s2, p01, p23);
+            if (Z) {
+                // 128 + code minus 128 + z, exact in bf16, then one rounding.
+                const uint32_t v = w >> (4 * half);
+                const uint32_t off = 0xC300C300u | uint32_t(z) | (uint32_t(z) << 16);
+                uint32_t d01, d23;
+                asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d01) : "r"(magic_pair(v)), "r"(0x3F803F80u), "r"(off));
+                asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d23) : "r"(magic_pair(v >> 8)), "r"(0x3F803F80u), "r"(off));
+                p01 = bf16x2_mul(d01, s2);
+                p23 = bf16x2_mul(d23, s2);
+            } else {
+                dequant_word_row_scaled(w, half, s2, p01, p23);
+            }
             uint16_t *dst = reinterpret_cast<uint16_t *>(out) + o;
             dst[0] = uint16_t(p01 & 0xFFFF);
             dst[1] = uint16_t(p01 >> 16);
@@ -91,11 +106,13 @@ __global__ void dequant_kernel(const uint32_t *__restrict__ wp, const uint16_t *
             dequant_word_frag(w, a);
             const float s = bf16_bits_to_f32(sbits);
             const uint32_t q01 = a[half], q23 = a[2 + half];
+            // (code - 8) + (8 - z) = code - z, exact in fp32
+            const float dz = float(8 - z);
             float *dst = reinterpret_cast<float *>(out) + o;
-            dst[0] = s * bf16_lo_to_f32(q01);
-            dst[1] = s * bf16_hi_to_f32(q01);
-            dst[2] = s * bf16_lo_to_f32(q23);
-            dst[3] = s * bf16_hi_to_f32(q23);
+            dst[0] = s * (bf16_lo_to_f32(q01) + dz);
+            dst[1] = s * (bf16_hi_to_f32(q01) + dz);
+            dst[2] = s * (bf16_lo_to_f32(q23) + dz);
+            dst[3] = s * (bf16_hi_to_f32(q23) + dz);
         }
     }
 }
@@ -117,15 +134,15 @@ cudaError_t launch_pack(const uint8_t *w_canon, uint8_t *w_packed, int N, int K,
 }
 
 cudaError_t launch_dequant(const uint8_t *w_packed, const uint16_t *scales, void *out,
-                           bool bf16_out, int N, int K, int G, cudaStream_t s) {
+                           bool bf16_out, int N, int K, int G, cudaStream_t s, const uint8_t *Z) {
     const size_t words = packed_bytes(N, K) / 4;
     const int threads = 256;
     const size_t blocks = (words + threads - 1) / threads;
     const uint32_t *wp = reinterpret_cast<const uint32_t *>(w_packed);
     if (bf16_out)
-        dequant_kernel<true><<<dim3(unsigned(blocks)), threads, 0, s>>>(wp, scales, out, N, K, G, words);
+        dequant_kernel<true><<<dim3(unsigned(blocks)), threads, 0, s>>>(wp, scales, Z, out, N, K, G, words);
     else
-        dequant_kernel<false><<<dim3(unsigned(blocks)), threads, 0, s>>>(wp, scales, out, N, K, G, words);
+        dequant_kernel<false><<<dim3(unsigned(blocks)), threads, 0, s>>>(wp, scales, Z, out, N, K, G, words);
     return cudaGetLastError();
 }
 

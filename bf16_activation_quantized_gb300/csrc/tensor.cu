@@ -60,6 +60,7 @@ constexpr uint32_t kTcDCol = 0;      // accumulator: columns [0, bt); A stage sa
 // TcArgs::opt_bits.
 constexpr int kTcVecStore = 1;   // Y rows are 16-byte aligned: stage the epilogue for 16-byte stores
 constexpr int kTcScaleVec = 2;   // scales aligned to 2 * sub bytes: one load per row's sub scales
+constexpr int kTcZeroVec = 4;    // zero points aligned to sub bytes: one load per row's sub zeros
 
 struct TcArgs {
     const uint8_t *Wp;
@@ -221,6 +222,52 @@ __device__ __forceinline__ ScaleRaw<kSub> scales_raw(const uint16_t *S, int row,
     for (int i = 0; i < kSub; ++i) r.w[i / 2] |= scale_raw(S, row, N, idx + i) << (16 * (i & 1));
     return r;
 }
+// The kSub zero points (zero-point variant) of one weight row for one
+// 128-wide block, one byte each in a 32-bit word (0 past the last row).
+// vec: Z + idx is aligned to kSub bytes.
+template <int kSub>
+__device__ __forceinline__ uint32_t zeros_raw(const uint8_t *Z, int row, int N, size_t idx, bool vec) {
+    uint32_t r = 0;
+    if constexpr (kSub == 4) {
+        if (vec) {
+            asm volatile("{\n\t.reg .pred p;\n\tsetp.lt.s32 p, %1, %2;\n\t"
+                         "@p ld.global.nc.u32 %0, [%3];\n\t}"
+                         : "+r"(r) : "r"(row), "r"(N), "l"(Z + idx));
+            return r;
+        }
+    } else if constexpr (kSub == 2) {
+        if (vec) {
+            asm volatile("{\n\t.reg .pred p;\n\tsetp.lt.s32 p, %1, %2;\n\t"
+                         "@p ld.global.nc.u16 %0, [%3];\n\t}"
+                         : "+r"(r) : "r"(row), "r"(N), "l"(Z + idx));
+            return r;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kSub; ++i) {
+        uint32_t v = 0;
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.lt.s32 p, %1, %2;\n\t"
+                     "@p ld.global.nc.u8 %0, [%3];\n\t}"
+                     : "+r"(v) : "r"(row), "r"(N), "l"(Z + idx + i));
+        r |= v << (8 * i);
+    }
+    return r;
+}
+
+// bf16x2 pair {-(128 + z), -(128 + z)} of zero point i (low four bits of
+// byte i): 128 + z is bf16 0x4300 | z, exactly.
+__device__ __forceinline__ uint32_t neg_offset_pair(uint32_t zraw, int i) {
+    const uint32_t z = (zraw >> (8 * i)) & 0xFu;
+    return 0xC300C300u | z | (z << 16);
+}
+
+// bf16x2 a * 1 + b: with a = 128 + code and b = -(128 + z), code - z exactly.
+__device__ __forceinline__ uint32_t bf16x2_add_pair(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0x3F803F80u), "r"(b));
+    return d;
+}
+
 // bf16x2 pair {scale i, scale i}.
 template <int kSub>
 __device__ __forceinline__ uint32_t scale_pair_of(const ScaleRaw<kSub> &r, int i) {
@@ -296,9 +343,12 @@ __device__ __forceinline__ void tc_store_block(const TcArgs &a, const TileInfo &
 // kSub: scale groups per 128-wide block (1, 2, 4: groups of 128, 64, 32
 // columns).  Packed word j of a lane covers columns 16 j .. 16 j + 15 of the
 // block, so its scale group is j * kSub / 8.
-template <bool kSplit, bool kSep, bool kBatched, int kSub>
-__global__ void __launch_bounds__(kSep ? kTcThreadsSep : kTcThreads, kSep ? 1 : 2)
-tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
+// kZp: zero points Z (uint8 [N][K/G] per group of the product): the
+// dequantisers subtract 128 + z, exact in bf16, where the symmetric form
+// subtracts 136.  tc_gemm_kernel and tc_gemm_zp_kernel are the entry points.
+template <bool kSplit, bool kSep, bool kBatched, int kSub, bool kZp>
+__device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const TcArgs &a,
+                                             const uint8_t *__restrict__ Z) {
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled X tiles (the host adds the slack).
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -518,8 +568,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         // Scales of the next group (possibly in the next tile), loaded one group
         // ahead so the dequantisers never wait on them.
         ScaleRaw<kSub> n0 = {}, n1 = {};
+        uint32_t nz0 = 0, nz1 = 0;      // zero points of the next block (kZp)
         bool have_next = false;
         const bool svec = (a.opt_bits & kTcScaleVec) != 0;
+        const bool zvec = (a.opt_bits & kTcZeroVec) != 0;
         // An A stage whose TMEM store is still in flight: its completion is
         // waited for only after the next group is dequantised, so the store
         // latency overlaps the ALU work.
@@ -541,20 +593,32 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             const int g1 = min(n_groups, (ti.slice + 1) * a.gps);
             const int r0 = ti.ft * kTileRows + 16 * block + g;     // weight rows r0, r0 + 8
             const uint16_t *sg = a.S + (unsigned long long)ti.group * a.s_group_stride;
+            const uint8_t *zg = kZp ? Z + (unsigned long long)ti.group * a.s_group_stride : nullptr;
             bool ok = true;
             for (int grp = g0; grp < g1; ++grp) {
                 ScaleRaw<kSub> s0, s1;              // raw; paired after the stage wait
+                uint32_t z0 = 0, z1 = 0;
                 if (have_next) {
                     s0 = n0;
                     s1 = n1;
+                    z0 = nz0;
+                    z1 = nz1;
                 } else {
                     s0 = scales_raw<kSub>(sg, r0, a.N, size_t(r0) * n_sg + size_t(grp) * kSub, svec);
                     s1 = scales_raw<kSub>(sg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(grp) * kSub, svec);
+                    if (kZp) {
+                        z0 = zeros_raw<kSub>(zg, r0, a.N, size_t(r0) * n_sg + size_t(grp) * kSub, zvec);
+                        z1 = zeros_raw<kSub>(zg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(grp) * kSub, zvec);
+                    }
                 }
                 have_next = false;
                 if (grp + 1 < g1) {
                     n0 = scales_raw<kSub>(sg, r0, a.N, size_t(r0) * n_sg + size_t(grp + 1) * kSub, svec);
                     n1 = scales_raw<kSub>(sg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(grp + 1) * kSub, svec);
+                    if (kZp) {
+                        nz0 = zeros_raw<kSub>(zg, r0, a.N, size_t(r0) * n_sg + size_t(grp + 1) * kSub, zvec);
+                        nz1 = zeros_raw<kSub>(zg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(grp + 1) * kSub, zvec);
+                    }
                     have_next = true;
                 } else if (nx_ok) {
                     const int rn = nx.ft * kTileRows + 16 * block + g;
@@ -562,6 +626,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     const uint16_t *sn = a.S + (unsigned long long)nx.group * a.s_group_stride;
                     n0 = scales_raw<kSub>(sn, rn, a.N, size_t(rn) * n_sg + size_t(gn) * kSub, svec);
                     n1 = scales_raw<kSub>(sn, rn + 8, a.N, size_t(rn + 8) * n_sg + size_t(gn) * kSub, svec);
+                    if (kZp) {
+                        const uint8_t *zn = Z + (unsigned long long)nx.group * a.s_group_stride;
+                        nz0 = zeros_raw<kSub>(zn, rn, a.N, size_t(rn) * n_sg + size_t(gn) * kSub, zvec);
+                        nz1 = zeros_raw<kSub>(zn, rn + 8, a.N, size_t(rn + 8) * n_sg + size_t(gn) * kSub, zvec);
+                    }
                     have_next = true;
                 }
                 if (!mbar_wait(wfull_bar(st), wph, abort_flag, a.err)) { ok = false; break; }
@@ -584,6 +653,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     // Repetition j of the 16x256b store: {row g: pair 0, pair 1},
                     // {row g+8: pair 0, pair 1} of columns 16j + 4t of the group.
                     const uint32_t q0 = p0[j * kSub / 8], q1 = p1[j * kSub / 8];
+                    if constexpr (kZp) {
+                        const uint32_t o0 = neg_offset_pair(z0, j * kSub / 8);
+                        const uint32_t o1 = neg_offset_pair(z1, j * kSub / 8);
+                        frag[4 * j + 0] = bf16x2_mul(bf16x2_add_pair(magic_pair(wv[j]), o0), q0);
+                        frag[4 * j + 1] = bf16x2_mul(bf16x2_add_pair(magic_pair(wv[j] >> 8), o0), q0);
+                        frag[4 * j + 2] = bf16x2_mul(bf16x2_add_pair(magic_pair(wv[j] >> 4), o1), q1);
+                        frag[4 * j + 3] = bf16x2_mul(bf16x2_add_pair(magic_pair(wv[j] >> 12), o1), q1);
+                        continue;
+                    }
                     frag[4 * j + 0] = bf16x2_mul(minus136(magic_pair(wv[j])), q0);
                     frag[4 * j + 1] = bf16x2_mul(minus136(magic_pair(wv[j] >> 8)), q0);
                     frag[4 * j + 2] = bf16x2_mul(minus136(magic_pair(wv[j] >> 4)), q1);
@@ -655,6 +733,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     if (warp == kTcMmaWarp) tc_dealloc(tmem_base, uint32_t(a.tmem_cols));
 }
 
+template <bool kSplit, bool kSep, bool kBatched, int kSub>
+__global__ void __launch_bounds__(kSep ? kTcThreadsSep : kTcThreads, kSep ? 1 : 2)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
+    tc_gemm_body<kSplit, kSep, kBatched, kSub, false>(tmap_x, a, nullptr);
+}
+
+template <bool kSplit, bool kSep, int kSub>
+__global__ void __launch_bounds__(kSep ? kTcThreadsSep : kTcThreads, kSep ? 1 : 2)
+tc_gemm_zp_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a,
+                  const uint8_t *__restrict__ Z) {
+    tc_gemm_body<kSplit, kSep, false, kSub, true>(tmap_x, a, Z);
+}
+
 using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
 
 EncodeTiledFn encode_tiled() {
@@ -709,23 +800,29 @@ namespace {
 
 // One of the kernel's eight (split, separate epilogue, batched) forms for
 // kSub scale groups per 128-wide block.
+// Z != nullptr: the zero-point kernel (plain products only).
 template <int kSub>
 cudaError_t launch_tc_sub(const TensorPlan &p, const CUtensorMap &tmap, const TcArgs &a, bool batched,
-                          size_t smem, cudaStream_t s) {
+                          size_t smem, cudaStream_t s, const uint8_t *Z) {
     const bool split = p.split_k > 1;
     const bool sep = p.sep_epilogue;
+    if (Z && batched) return cudaErrorInvalidValue;
     auto kern = batched ? (split ? (sep ? tc_gemm_kernel<true, true, true, kSub> : tc_gemm_kernel<true, false, true, kSub>)
                                  : (sep ? tc_gemm_kernel<false, true, true, kSub> : tc_gemm_kernel<false, false, true, kSub>))
                         : (split ? (sep ? tc_gemm_kernel<true, true, false, kSub> : tc_gemm_kernel<true, false, false, kSub>)
                                  : (sep ? tc_gemm_kernel<false, true, false, kSub> : tc_gemm_kernel<false, false, false, kSub>));
-    static std::atomic<unsigned long long> opted[8];
-    const int ki = (batched ? 4 : 0) + (split ? 2 : 0) + (sep ? 1 : 0);
+    auto kern_zp = split ? (sep ? tc_gemm_zp_kernel<true, true, kSub> : tc_gemm_zp_kernel<true, false, kSub>)
+                         : (sep ? tc_gemm_zp_kernel<false, true, kSub> : tc_gemm_zp_kernel<false, false, kSub>);
+    static std::atomic<unsigned long long> opted[12];
+    const int ki = Z ? 8 + (split ? 2 : 0) + (sep ? 1 : 0)
+                     : (batched ? 4 : 0) + (split ? 2 : 0) + (sep ? 1 : 0);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(opted[ki].load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTensorMaxSmem);
+        e = Z ? cudaFuncSetAttribute(kern_zp, cudaFuncAttributeMaxDynamicSharedMemorySize, kTensorMaxSmem)
+              : cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTensorMaxSmem);
         if (e != cudaSuccess) return e;
         opted[ki].fetch_or(bit, std::memory_order_acq_rel);
     }
@@ -739,6 +836,7 @@ cudaError_t launch_tc_sub(const TensorPlan &p, const CUtensorMap &tmap, const Tc
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (Z) return cudaLaunchKernelEx(&cfg, kern_zp, tmap, a, Z);
     return cudaLaunchKernelEx(&cfg, kern, tmap, a);
 }
 
@@ -747,7 +845,7 @@ cudaError_t launch_tc_sub(const TensorPlan &p, const CUtensorMap &tmap, const Tc
 cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, const int32_t *m_sizes,
                           int *status, int num_groups, int M_total, int N, int K, cudaStream_t s,
-                          int batch_rows) {
+                          int batch_rows, const uint8_t *Z) {
     if (p.tile_tokens < 32 || p.tile_tokens > 256 || p.tile_tokens % 32 || p.x_stages < 2 ||
         p.w_stages < 2 ||
         p.ctas < 1 || num_groups < 1 || num_groups > kMaxGroups || p.occupancy < 1 ||
@@ -794,16 +892,18 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
     a.tmem_cols = tensor_tmem_cols(p.tile_tokens, p.occupancy, p.sep_epilogue);
     a.dcols = p.sep_epilogue ? 2 * p.tile_tokens : p.tile_tokens;
     a.opt_bits = ((N % 8 == 0) && (reinterpret_cast<uintptr_t>(Y) % 16 == 0) ? kTcVecStore : 0) |
-                 (reinterpret_cast<uintptr_t>(S) % (2 * p.sub) == 0 ? kTcScaleVec : 0);
+                 (reinterpret_cast<uintptr_t>(S) % (2 * p.sub) == 0 ? kTcScaleVec : 0) |
+                 (reinterpret_cast<uintptr_t>(Z) % p.sub == 0 ? kTcZeroVec : 0);
     a.w_group_stride = packed_bytes(N, K);
     a.s_group_stride = (unsigned long long)N * (K / kGroup) * p.sub;
 
     const size_t smem =
         tensor_smem_bytes(p.tile_tokens, p.x_stages, p.w_stages, p.occupancy, num_groups, p.sep_epilogue);
     if (smem > size_t(tensor_smem_budget(p.occupancy))) return cudaErrorInvalidValue;
-    if (p.sub == 2) return launch_tc_sub<2>(p, tmap, a, batched, smem, s);
-    if (p.sub == 4) return launch_tc_sub<4>(p, tmap, a, batched, smem, s);
-    return launch_tc_sub<1>(p, tmap, a, batched, smem, s);
+    if (Z && (m_sizes != nullptr || batched)) return cudaErrorInvalidValue;
+    if (p.sub == 2) return launch_tc_sub<2>(p, tmap, a, batched, smem, s, Z);
+    if (p.sub == 4) return launch_tc_sub<4>(p, tmap, a, batched, smem, s, Z);
+    return launch_tc_sub<1>(p, tmap, a, batched, smem, s, Z);
 }
 
 }  // namespace w4a16

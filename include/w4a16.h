@@ -82,7 +82,11 @@ enum {
      * never that kernel.  Setting
      * both is W4A16_ERR_INVALID_ARG. */
     W4A16_FLAG_DECODE_WHOLE_K = 2,
-    W4A16_FLAG_DECODE_K_SLICES = 4
+    W4A16_FLAG_DECODE_K_SLICES = 4,
+    /* Plan for the zero-point variant (w4a16_plan / w4a16_workspace_bytes
+     * queries; w4a16_gemm_zp sets it itself).  Passing it to any other call
+     * is W4A16_ERR_INVALID_ARG. */
+    W4A16_FLAG_ZERO_POINTS = 8
 };
 
 /* Overrides for tests and tuning.  Zero-initialised = automatic. */
@@ -200,6 +204,22 @@ w4a16_status w4a16_gemm_batched(const w4a16_bf16 *X, const uint8_t *W_packed,
                                 int K, int group_size, void *workspace, size_t workspace_bytes,
                                 const w4a16_options *opts, void *stream);
 
+/* Zero-point variant: Y = X . dequant(W)^T with
+ *   dequant(W)[n][k] = scale[n][k/G] * (code(n, k) - z[n][k/G]).
+ * The pages describe only the symmetric form (z = 8); this is the usual int4
+ * convention of a 4-bit integer zero point per row and scale group, a reading
+ * for the asymmetric case.
+ *  zeros:    device uint8 [N][K/G]; the low four bits of each byte are z
+ *            (all z = 8 gives the symmetric result).
+ *  Other arguments as for w4a16_gemm_ex; the workspace is what w4a16_plan
+ *  reports with W4A16_FLAG_ZERO_POINTS in opts->flags.  Plain products only
+ *  (no batched or grouped form); the decode arm always uses its K-slice
+ *  kernel. */
+w4a16_status w4a16_gemm_zp(const w4a16_bf16 *X, const uint8_t *W_packed, const w4a16_bf16 *scales,
+                           const uint8_t *zeros, w4a16_bf16 *Y, int M, int N, int K,
+                           int group_size, void *workspace, size_t workspace_bytes,
+                           const w4a16_options *opts, void *stream);
+
 /* Workspace bytes of a grouped call: 16 bytes holding the device status word
  * (see w4a16_gemm_grouped).  Host only. */
 w4a16_status w4a16_grouped_workspace_bytes(int num_groups, int M_total, int N, int K,
@@ -238,6 +258,16 @@ w4a16_status w4a16_dequant_fp32(const uint8_t *W_packed, const w4a16_bf16 *scale
  * out[n][k] = bf16_rne(scale[n][k/G] * (code - 8)).  out: device bf16 [N][K]. */
 w4a16_status w4a16_dequant_bf16(const uint8_t *W_packed, const w4a16_bf16 *scales,
                                 w4a16_bf16 *out, int N, int K, int group_size, void *stream);
+
+/* The same two probes for the zero-point variant: scale * (code - z), z the
+ * low four bits of zeros[n][k/G] (device uint8 [N][K/G]); fp32 exact, bf16
+ * rounded once (the tensor arm's operand). */
+w4a16_status w4a16_dequant_zp_fp32(const uint8_t *W_packed, const w4a16_bf16 *scales,
+                                   const uint8_t *zeros, float *out, int N, int K, int group_size,
+                                   void *stream);
+w4a16_status w4a16_dequant_zp_bf16(const uint8_t *W_packed, const w4a16_bf16 *scales,
+                                   const uint8_t *zeros, w4a16_bf16 *out, int N, int K,
+                                   int group_size, void *stream);
 
 /* The split-K reduce on its own: Y[i] = bf16_rne(sum over s = 0..splits-1 of
  * ws[s][i]) for i < M*N, slices summed in fp32 in ascending order ("Add Triton

@@ -134,7 +134,7 @@ def test_plan_without_a_gpu_reports_cuda_error(L):
 def test_options_are_checked_before_the_device_is_queried(L):
     # Unknown flag bits, bad arms and bad tile sizes are host-side errors.
     info = _lib.PlanInfo()
-    for o, want in ((_lib.Options(0, 0, 0, 8), INVALID), (_lib.Options(0, 0, 0, 1 << 30), INVALID),
+    for o, want in ((_lib.Options(0, 0, 0, 16), INVALID), (_lib.Options(0, 0, 0, 1 << 30), INVALID),
                     (_lib.Options(0, 0, 0, 2 | 4), INVALID),
                     (_lib.Options(7, 0, 0, 0), INVALID), (_lib.Options(0, -1, 0, 0), INVALID),
                     (_lib.Options(2, 0, 48, 0), UNSUPPORTED)):
@@ -144,7 +144,8 @@ def test_options_are_checked_before_the_device_is_queried(L):
 def test_header_flag_values_match_the_binding():
     import bf16_activation_quantized_gb300 as w4
     text = open(HEADER).read()
-    for name, value in (("RESIDENT_WEIGHTS", 1), ("DECODE_WHOLE_K", 2), ("DECODE_K_SLICES", 4)):
+    for name, value in (("RESIDENT_WEIGHTS", 1), ("DECODE_WHOLE_K", 2), ("DECODE_K_SLICES", 4),
+                        ("ZERO_POINTS", 8)):
         assert re.search(rf"W4A16_FLAG_{name}\s*=\s*{value}\b", text)
         assert getattr(w4, f"FLAG_{name}") == value
 
@@ -162,3 +163,20 @@ def test_batched_entry_points_check_arguments(L):
     assert L.w4a16_gemm_batched(FAKE, FAKE, FAKE, FAKE, 0, 4, 256, 512, 128, None, 0, None, None) == INVALID
     # M == 0: nothing to do, nothing launched, no GPU needed
     assert L.w4a16_gemm_batched(None, None, None, None, 2, 0, 256, 512, 128, None, 0, None, None) == OK
+
+
+def test_zero_point_entry_points_check_arguments(L):
+    FAKE = 1 << 20
+    zp = _lib.Options(0, 0, 0, 8)
+    # zeros are required; the flag alone (without a zeros pointer) is refused
+    assert L.w4a16_gemm_zp(FAKE, FAKE, FAKE, None, FAKE, 4, 256, 512, 128, None, 0, None, None) == INVALID
+    assert L.w4a16_gemm_ex(FAKE, FAKE, FAKE, FAKE, 4, 256, 512, 128, None, 0, ctypes.byref(zp),
+                           None) == INVALID
+    assert L.w4a16_gemm_zp(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 512, 256, None, 0, None, None) == UNSUPPORTED
+    assert L.w4a16_gemm_zp(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 500, 128, None, 0, None, None) == INVALID
+    assert L.w4a16_gemm_zp(None, None, None, None, None, 0, 256, 512, 32, None, 0, None, None) == OK
+    # no batched zero-point form
+    info = _lib.PlanInfo()
+    assert L.w4a16_plan_batched(2, 4, 256, 512, 128, ctypes.byref(zp), ctypes.byref(info)) == UNSUPPORTED
+    assert L.w4a16_dequant_zp_fp32(FAKE, FAKE, None, FAKE, 16, 128, 128, None) == INVALID
+    assert L.w4a16_dequant_zp_bf16(FAKE, FAKE, FAKE, FAKE, 16, 128, 48, None) == UNSUPPORTED
