@@ -66,6 +66,8 @@ def parse_args(argv=None):
                          "only; 'grouped' times the grouped workload")
     ap.add_argument("--group-size", type=int, default=128, choices=[128, 64, 32],
                     help="scale group size G for --shape")
+    ap.add_argument("--zero-points", action="store_true",
+                    help="--shape: the zero-point variant (uint8 zero point per row and group)")
     return ap.parse_args(argv)
 
 
@@ -167,7 +169,7 @@ def maybe_init_dist(world, local):
 
 # ---------------------------------------------------------------- our arm
 class Shape:
-    def __init__(self, torch, w4, syn, M, N, K, copies, device, seed=0, G=128):
+    def __init__(self, torch, w4, syn, M, N, K, copies, device, seed=0, G=128, zp=False):
         inp = syn.make_gemm_inputs(M, N, K, G=G, seed=seed)
         self.torch = torch
         self.inp = inp
@@ -179,13 +181,18 @@ class Shape:
         self.w = [wp] + [wp.clone() for _ in range(copies - 1)]
         self.s = [s] + [s.clone() for _ in range(copies - 1)]
         self.y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
-        self.plan = w4.plan(M, N, K, group_size=G)
+        self.z = None
+        if zp:
+            zd = torch.from_numpy(syn.make_zeros(N, K, G, seed=seed)).to(device)
+            self.z = [zd] + [zd.clone() for _ in range(copies - 1)]
+        self.plan = w4.plan(M, N, K, group_size=G, zero_points=zp)
         self.ws = torch.empty(max(self.plan["workspace_bytes"], 256), dtype=torch.uint8, device=device)
         self.launches = 1 + (1 if self.plan["split_k"] > 1 else 0)
 
     def call(self, w4, i):
         c = i % len(self.w)
-        w4.gemm(self.x, self.w[c], self.s[c], out=self.y, workspace=self.ws, resident_weights=True)
+        w4.gemm(self.x, self.w[c], self.s[c], out=self.y, workspace=self.ws, resident_weights=True,
+                zeros=self.z[c] if self.z else None)
 
     def partials(self, w4, i):
         """The main kernel alone: the split-K decode kernel, or the whole call
@@ -425,35 +432,41 @@ def end_to_end(torch, w4, shapes, steps, step_bytes):
 # decode and a prefill shape; every other row uses groups of 128.
 GROUP32_SHAPES = [("decode_gemv_g32", 1, 8192, 8192), ("decode_gemv_g32", 1, 17408, 5120),
                   ("prefill_g32", 1322, 19456, 2560), ("prefill_g32", 1322, 2560, 9728)]
+# The zero-point variant (one uint8 zero point per row and scale group).
+ZP_SHAPES = [("decode_gemv_zp", 1, 8192, 8192, 128), ("decode_gemv_zp", 1, 17408, 5120, 128),
+             ("prefill_zp", 1322, 19456, 2560, 128), ("prefill_zp", 1322, 19456, 2560, 32)]
 
 
-def per_shape_table(torch, w4, syn, metrics, device, peaks, only=None, group_size=128):
-    shapes = [("tiny", 4, 256, 512, 128)]
+def per_shape_table(torch, w4, syn, metrics, device, peaks, only=None, group_size=128, zp=False):
+    shapes = [("tiny", 4, 256, 512, 128, False)]
     for name, lst in (("decode_gemv", syn.WORKLOADS["decode_gemv"]),
                       ("decode_sweep_gate_up", syn.WORKLOADS["decode_sweep_gate_up"]),
                       ("decode_sweep_down", syn.WORKLOADS["decode_sweep_down"]),
                       ("prefill", syn.WORKLOADS["prefill"]),
                       ("prefill_long", syn.WORKLOADS["prefill_long"])):
-        shapes += [(name, M, N, K, 128) for (M, N, K) in lst]
-    shapes += [(name, M, N, K, 32) for (name, M, N, K) in GROUP32_SHAPES]
+        shapes += [(name, M, N, K, 128, False) for (M, N, K) in lst]
+    shapes += [(name, M, N, K, 32, False) for (name, M, N, K) in GROUP32_SHAPES]
+    shapes += [(name, M, N, K, G, True) for (name, M, N, K, G) in ZP_SHAPES]
     if only is not None:
         if len(only) == 4:    # G, M_total, N, K: the grouped workload
             return [grouped_row(torch, w4, syn, metrics, device, peaks)]
-        named = [sh for sh in shapes if sh[1:] == tuple(only) + (group_size,)]
-        shapes = named[:1] or [("custom",) + tuple(only) + (group_size,)]
+        named = [sh for sh in shapes if sh[1:] == tuple(only) + (group_size, zp)]
+        shapes = named[:1] or [("custom",) + tuple(only) + (group_size, zp)]
     rows = []
-    for name, M, N, K, G in shapes:
-        wb = metrics.weight_bytes(N, K, G)
+    for name, M, N, K, G, with_zp in shapes:
+        # (zero points: one more byte per row and scale group)
+        wb = metrics.weight_bytes(N, K, G) + (N * (K // G) if with_zp else 0)
         C = copies_for(torch, device, wb + 2 * M * K)
-        s = Shape(torch, w4, syn, M, N, K, C, device, G=G)
+        s = Shape(torch, w4, syn, M, N, K, C, device, G=G, zp=with_zp)
         R = max(C, (100 // C) * C) if M < 512 else C
         g = capture(torch, lambda i: s.call(w4, i), R)
         g.replay()
         t = statistics.median(time_graph(torch, g) for _ in range(5)) / R
-        nbytes = metrics.algorithmic_bytes(M, N, K, G)
+        nbytes = metrics.algorithmic_bytes(M, N, K, G) + (N * (K // G) if with_zp else 0)
         fl = metrics.flops(M, N, K)
         t_roof = metrics.roofline_seconds(fl, nbytes, peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
-        rows.append({"workload": name, "M": M, "N": N, "K": K, "group_size": G, "us": round(t * 1e6, 3),
+        rows.append({"workload": name, "M": M, "N": N, "K": K, "group_size": G, "zero_points": with_zp,
+                     "us": round(t * 1e6, 3),
                      "tflops": round(fl / t / 1e12, 3), "gbs": round(nbytes / t / 1e9, 1),
                      "roofline_frac": round(t_roof / t, 4),
                      "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) >= fl / (peaks["bf16_tflops"] * 1e12) else "tensor",
@@ -619,7 +632,7 @@ def main(argv=None):
                 [int(v) for v in args.shape.split(",")])
         if rank == 0:
             print(json.dumps(per_shape_table(torch, w4, syn, metrics, device, peaks, only,
-                                             args.group_size)[0]), flush=True)
+                                             args.group_size, args.zero_points)[0]), flush=True)
         return 0
     dist = maybe_init_dist(world, local)
     out = our_arm(args, world, rank, local, dist)
