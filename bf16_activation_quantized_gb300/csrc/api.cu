@@ -300,7 +300,16 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                 const double per_cta_tiles = double(ceil_div(tiles, ctas));
                 // Per-tile fixed cost: the epilogue, which a separate epilogue
                 // overlaps with the next tile (except the CTA's last one).
-                const double epi = sep ? 1500.0 : per_cta_tiles * 1500.0;
+                // A split tile drains fp32 partials through the dequant warps
+                // while the tensor pipe waits; measured on GB300 that stall
+                // grows with the tile width (about (bt / 128)^2 x 1500 cycles
+                // per tile before a CTA's last: 512x7168x8192 split 4 took
+                // 76.3 us, unsplit 51.9 us; 2048x8192x8192 split 2 288 us,
+                // unsplit 199 us).
+                const double e_split = 1500.0 * std::max(1.0, (bt / 128.0) * (bt / 128.0));
+                const double epi = sep ? 1500.0
+                                 : sk > 1 ? 1500.0 + (per_cta_tiles - 1) * e_split
+                                          : per_cta_tiles * 1500.0;
                 double time = (per_cta_tiles * conc * 2.0 * gps * kb + epi) / kClockHz;
                 if (sk > 1) time += 2.0 * sk * double(M) * N * 4.0 / kL2BytesPerS + kTensorReduceSeconds;
                 if (time < best * 0.999) {
