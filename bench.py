@@ -157,6 +157,22 @@ def dist_info():
     return world, rank, local
 
 
+def max_over_ranks(dist, seconds: float, device=None) -> float:
+    """The slowest rank's time, returned on every rank (the whole job ends when
+    its last replica ends).  dist None: one process."""
+    if dist is None:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, step_bytes: int, steps: int, seconds: float) -> float:
+    """Whole-job throughput: every replica moves step_bytes per step."""
+    return world * step_bytes * steps / seconds / 1e9
+
+
 def maybe_init_dist(world, local):
     if world <= 1:
         return None
@@ -295,12 +311,8 @@ def our_arm(args, world, rank, local, dist):
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    elapsed = e0.elapsed_time(e1) / 1e3
-    if dist:
-        t = torch.tensor([elapsed], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
-    value = world * step_bytes * args.steps / elapsed / 1e9
+    elapsed = max_over_ranks(dist, e0.elapsed_time(e1) / 1e3, device)
+    value = whole_job_gbs(world, step_bytes, args.steps, elapsed)
     launches = args.steps * sum(s.launches for s in shapes)
 
     # Dominant kernel alone: graphs of back-to-back decode-kernel launches.
