@@ -254,11 +254,12 @@ __device__ __forceinline__ uint32_t zeros_raw(const uint8_t *Z, int row, int N, 
     return r;
 }
 
-// bf16x2 pair {-(128 + z), -(128 + z)} of zero point i (low four bits of
-// byte i): 128 + z is bf16 0x4300 | z, exactly.
-__device__ __forceinline__ uint32_t neg_offset_pair(uint32_t zraw, int i) {
-    const uint32_t z = (zraw >> (8 * i)) & 0xFu;
-    return 0xC300C300u | z | (z << 16);
+// bf16x2 pair {-(128 + z), -(128 + z)} of zero point i, from the row's
+// zero-point bytes already masked to their low four bits: 128 + z is bf16
+// 0x4300 | z exactly, so the pair's bytes are {z, 0xC3, z, 0xC3}, one byte
+// permute.
+__device__ __forceinline__ uint32_t neg_offset_pair(uint32_t zmasked, int i) {
+    return __byte_perm(zmasked, 0xC3C3C3C3u, 0x4040u + 0x0101u * uint32_t(i));
 }
 
 // bf16x2 a * 1 + b: with a = 128 + code and b = -(128 + z), code - z exactly.
@@ -647,6 +648,15 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                     p0[i] = scale_pair_of<kSub>(s0, i);
                     p1[i] = scale_pair_of<kSub>(s1, i);
                 }
+                uint32_t zo0[kSub], zo1[kSub];      // kZp: offset pairs per scale group
+                if constexpr (kZp) {
+                    const uint32_t m0 = z0 & 0x0F0F0F0Fu, m1 = z1 & 0x0F0F0F0Fu;
+#pragma unroll
+                    for (int i = 0; i < kSub; ++i) {
+                        zo0[i] = neg_offset_pair(m0, i);
+                        zo1[i] = neg_offset_pair(m1, i);
+                    }
+                }
                 uint32_t frag[32];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -654,8 +664,8 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                     // {row g+8: pair 0, pair 1} of columns 16j + 4t of the group.
                     const uint32_t q0 = p0[j * kSub / 8], q1 = p1[j * kSub / 8];
                     if constexpr (kZp) {
-                        const uint32_t o0 = neg_offset_pair(z0, j * kSub / 8);
-                        const uint32_t o1 = neg_offset_pair(z1, j * kSub / 8);
+                        const uint32_t o0 = zo0[j * kSub / 8];
+                        const uint32_t o1 = zo1[j * kSub / 8];
                         frag[4 * j + 0] = bf16x2_mul(bf16x2_add_pair(magic_pair(wv[j]), o0), q0);
                         frag[4 * j + 1] = bf16x2_mul(bf16x2_add_pair(magic_pair(wv[j] >> 8), o0), q0);
                         frag[4 * j + 2] = bf16x2_mul(bf16x2_add_pair(magic_pair(wv[j] >> 4), o1), q1);
