@@ -1,7 +1,8 @@
 // decode.cu -- decode-arm launchers, the whole-K decode kernel and the split-K
 // reduce.  The sliced decode kernel is in decode_slices.cuh; its instantiations
-// for 64- and 32-wide scale groups live in decode_g64.cu and decode_g32.cu so that
-// they compile in parallel.
+// for 64- and 32-wide scale groups live in decode_g64.cu and decode_g32.cu, and
+// its zero-point instantiations in decode_zp.cu, so that they compile in
+// parallel.
 #include <atomic>
 
 #include "decode_slices.cuh"

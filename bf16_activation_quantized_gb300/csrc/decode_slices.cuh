@@ -1,6 +1,6 @@
 // decode_slices.cuh -- the sliced decode kernel (memory-bound arm for few tokens).
 //
-// Decode arm.  A CTA owns one K slice (a run of whole 128-wide scale groups)
+// Decode arm.  A CTA owns one K slice (a run of whole 128-wide blocks of K)
 // and a set of 128-row weight tiles (c, c + C, c + 2C, ...).  One producer warp
 // streams the 8 KB (tile, group) blocks of those tiles, in order, into a ring
 // of up to 16 shared-memory stages with bulk asynchronous copies completed on
@@ -28,6 +28,7 @@
 // plain stores and a separate kernel sums the slices in order ("Add Triton
 // BF16xINT4 rowwise GEMM for ROCm gfx942/gfx950", "Split-K without atomics");
 // that kernel is chained with programmatic dependent launch so its launch
+// overlaps this one.
 #pragma once
 
 #include <atomic>
