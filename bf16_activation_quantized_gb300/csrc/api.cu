@@ -334,10 +334,10 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
 }
 
 // batch: independent products of this shape in one launch (1: a plain call).
-// sub: scale groups per 128-wide block (128 / group_size).
+// sub: scale groups per 128-wide block (128 / group_size).  W4A16_FLAG_ZERO_POINTS
+// in opts plans the zero-point kernels (plain products only).
 w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, int batch = 1,
                        int sub = 1) {
-    // (W4A16_FLAG_ZERO_POINTS: plan the zero-point kernels)
     std::memset(p, 0, sizeof *p);
     int arm = opts ? opts->arm : W4A16_ARM_AUTO;
     if (arm != W4A16_ARM_AUTO && arm != W4A16_ARM_DECODE && arm != W4A16_ARM_TENSOR)
