@@ -38,6 +38,7 @@ SIGNATURES = {
     "w4a16_gemm_partials": (I, [P, P, P, P, I, I, I, I, P, SZ, ctypes.POINTER(Options),
                                 ctypes.POINTER(I), P]),
     "w4a16_plan_batched": (I, [I, I, I, I, I, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]),
+    "w4a16_plan_for_sms": (I, [I, I, I, I, I, I, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]),
     "w4a16_gemm_batched": (I, [P, P, P, P, I, I, I, I, I, P, SZ, ctypes.POINTER(Options), P]),
     "w4a16_gemm_zp": (I, [P, P, P, P, P, I, I, I, I, P, SZ, ctypes.POINTER(Options), P]),
     "w4a16_grouped_workspace_bytes": (I, [I, I, I, I, I, ctypes.POINTER(SZ)]),

@@ -336,8 +336,10 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
 // batch: independent products of this shape in one launch (1: a plain call).
 // sub: scale groups per 128-wide block (128 / group_size).  W4A16_FLAG_ZERO_POINTS
 // in opts plans the zero-point kernels (plain products only).
+// sms > 0: plan for a device with that many SMs instead of querying the
+// current one (host-only planning).
 w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, int batch = 1,
-                       int sub = 1) {
+                       int sub = 1, int sms_given = 0) {
     std::memset(p, 0, sizeof *p);
     int arm = opts ? opts->arm : W4A16_ARM_AUTO;
     if (arm != W4A16_ARM_AUTO && arm != W4A16_ARM_DECODE && arm != W4A16_ARM_TENSOR)
@@ -355,8 +357,8 @@ w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, 
     const int forced_bt = opts ? opts->tile_tokens : 0;
     if (forced_bt != 0 && (forced_bt < 32 || forced_bt > 256 || forced_bt % 32))
         return W4A16_ERR_UNSUPPORTED;
-    int sms = 0;
-    if (device_sm_count(&sms) != 0 || sms < 1) return W4A16_ERR_CUDA;
+    int sms = sms_given;
+    if (sms <= 0 && (device_sm_count(&sms) != 0 || sms < 1)) return W4A16_ERR_CUDA;
     if (arm == W4A16_ARM_AUTO) arm = M <= kDecodeMaxM ? W4A16_ARM_DECODE : W4A16_ARM_TENSOR;
     if (arm == W4A16_ARM_DECODE && forced_bt != 0) return W4A16_ERR_INVALID_ARG;
     p->arm = arm;
@@ -515,11 +517,17 @@ w4a16_status w4a16_gemm(const w4a16_bf16 *X, const uint8_t *W_packed, const w4a1
 
 w4a16_status w4a16_plan_batched(int batch, int M, int N, int K, int group_size,
                                 const w4a16_options *opts, w4a16_plan_info *info) {
+    return w4a16_plan_for_sms(0, batch, M, N, K, group_size, opts, info);
+}
+
+w4a16_status w4a16_plan_for_sms(int sms, int batch, int M, int N, int K, int group_size,
+                                const w4a16_options *opts, w4a16_plan_info *info) {
     w4a16_status st = check_shape(M, N, K, group_size);
     if (st != W4A16_OK) return st;
+    if (sms < 0 || sms > 4096) return W4A16_ERR_INVALID_ARG;
     if (batch < 1 || batch > kMaxGroups || (long long)batch * M > (1 << 24)) return W4A16_ERR_INVALID_ARG;
     Plan p;
-    st = plan_call(M, N, K, opts, &p, batch, kGroup / group_size);
+    st = plan_call(M, N, K, opts, &p, batch, kGroup / group_size, sms);
     if (st != W4A16_OK) return st;
     if (info) {
         info->arm = p.arm;

@@ -199,6 +199,14 @@ w4a16_status w4a16_gemm_partials(const w4a16_bf16 *X, const uint8_t *W_packed,
  * M == 0 launches nothing. */
 w4a16_status w4a16_plan_batched(int batch, int M, int N, int K, int group_size,
                                 const w4a16_options *opts, w4a16_plan_info *info);
+
+/* Host-only planning for a device with `sms` streaming multiprocessors (152 on
+ * GB300) instead of the current device: the plan w4a16_plan_batched (batch > 1)
+ * or w4a16_plan (batch == 1) would make there.  sms == 0 queries the current
+ * device.  Needs no GPU when sms > 0 (plan tables built ahead of time, tests).
+ * 0 <= sms <= 4096, else W4A16_ERR_INVALID_ARG. */
+w4a16_status w4a16_plan_for_sms(int sms, int batch, int M, int N, int K, int group_size,
+                                const w4a16_options *opts, w4a16_plan_info *info);
 w4a16_status w4a16_gemm_batched(const w4a16_bf16 *X, const uint8_t *W_packed,
                                 const w4a16_bf16 *scales, w4a16_bf16 *Y, int batch, int M, int N,
                                 int K, int group_size, void *workspace, size_t workspace_bytes,

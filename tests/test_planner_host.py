@@ -1,0 +1,110 @@
+"""The planner's rules, checked on the CPU through w4a16_plan_for_sms (plans
+for a GB300's 152 SMs without a GPU): dispatch by token count, slice caps for
+32/64-column groups and zero points, the whole-K kernel's scope, workspace
+sizes, the split-K choices measured on GB300, and determinism."""
+from __future__ import annotations
+
+import ctypes
+
+import pytest
+
+from bf16_activation_quantized_gb300 import _lib
+
+SMS = 152
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def L():
+    from bf16_activation_quantized_gb300 import build as build_mod
+    build_mod.build()
+    return _lib.lib()
+
+
+def plan(L, M, N, K, G=128, batch=1, arm=0, split_k=0, tile=0, flags=0, sms=SMS):
+    info = _lib.PlanInfo()
+    o = _lib.Options(arm, split_k, tile, flags)
+    st = L.w4a16_plan_for_sms(sms, batch, M, N, K, G, ctypes.byref(o), ctypes.byref(info))
+    return st, info
+
+
+SHAPES = [(1, 8192, 8192), (1, 17408, 5120), (1, 19456, 2560), (8, 2560, 9728), (16, 19456, 2560),
+          (4, 256, 512), (13, 300, 640), (2, 2560, 1024)]
+
+
+def test_arguments(L):
+    assert plan(L, 1, 256, 512, sms=-1)[0] == INVALID
+    assert plan(L, 1, 256, 512, sms=5000)[0] == INVALID
+    assert plan(L, 1, 256, 500)[0] == INVALID
+    assert plan(L, 1, 256, 512, G=16)[0] == UNSUPPORTED
+    assert plan(L, 2, 256, 512, batch=2, flags=8)[0] == UNSUPPORTED    # no batched zero points
+
+
+@pytest.mark.parametrize("M", [1, 8, 16, 17, 32, 1322])
+def test_dispatch_by_token_count(L, M):
+    st, info = plan(L, M, 2560, 9728)
+    assert st == OK
+    assert info.arm == (1 if M <= 16 else 2)
+
+
+@pytest.mark.parametrize("G", [128, 64, 32])
+@pytest.mark.parametrize("zp", [False, True])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_decode_slice_caps(L, M, N, K, G, zp):
+    # A slice's scale groups of a row stay in registers: at most 16 (one token
+    # octet) or 8 (two), halved with zero points; slices divide K exactly.
+    st, info = plan(L, M, N, K, G=G, flags=8 if zp else 0)
+    assert st == OK and info.arm == 1
+    blocks = K // 128
+    assert blocks % info.split_k == 0
+    gps = blocks // info.split_k
+    cap = (16 if M <= 8 else 8) // (128 // G) // (2 if zp else 1)
+    if info.whole_k:
+        assert G == 128 and not zp and info.split_k == 1
+    else:
+        assert gps <= cap, (gps, cap)
+    assert info.workspace_bytes == (info.split_k * M * N * 4 if info.split_k > 1 else 0)
+
+
+@pytest.mark.parametrize("G", [64, 32])
+def test_whole_k_kernel_only_for_128_column_symmetric_groups(L, G):
+    assert plan(L, 1, 19456, 2560)[1].whole_k                      # the measured winner at G=128
+    assert not plan(L, 1, 19456, 2560, G=G)[1].whole_k
+    assert not plan(L, 1, 19456, 2560, flags=8)[1].whole_k
+    assert plan(L, 1, 19456, 2560, G=G, flags=2)[0] == UNSUPPORTED   # forced whole-K refused
+    assert plan(L, 1, 19456, 2560, flags=8 | 2)[0] == UNSUPPORTED
+
+
+def test_headline_plans(L):
+    # The decode GEMV shapes' plans on a GB300 (the figures quoted for them).
+    st, a = plan(L, 1, 8192, 8192)
+    assert st == OK and a.arm == 1 and a.split_k == 8 and not a.whole_k
+    st, b = plan(L, 1, 17408, 5120)
+    assert st == OK and b.arm == 1 and b.split_k == 10
+    st, c = plan(L, 1322, 19456, 2560)
+    assert st == OK and c.arm == 2 and c.split_k == 1 and c.tile_tokens == 192 and c.ctas == SMS
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 7168, 8192), (2048, 8192, 8192), (1024, 2560, 9728)])
+def test_split_drain_keeps_these_unsplit(L, M, N, K):
+    # Measured on GB300: splitting these in wide plain-epilogue tiles was
+    # 11-32 % slower than the unsplit plans.
+    st, info = plan(L, M, N, K)
+    assert st == OK and info.arm == 2 and info.split_k == 1
+
+
+def test_planning_is_deterministic_and_scales_with_sms(L):
+    a = plan(L, 1, 8192, 8192)[1]
+    b = plan(L, 1, 8192, 8192)[1]
+    assert (a.split_k, a.ctas) == (b.split_k, b.ctas)
+    small = plan(L, 1, 8192, 8192, sms=16)[1]
+    assert small.ctas <= 2 * 16 * max(1, small.split_k)
+    big = plan(L, 1322, 19456, 2560, sms=16)[1]
+    assert big.ctas <= 2 * 16
+
+
+def test_batched_plans_share_the_slots(L):
+    one = plan(L, 4, 8192, 3584)[1]
+    four = plan(L, 4, 8192, 3584, batch=4)[1]
+    assert four.arm == one.arm == 1
+    assert four.workspace_bytes == (four.split_k * 4 * 4 * 8192 * 4 if four.split_k > 1 else 0)
