@@ -108,3 +108,57 @@ def test_batched_plans_share_the_slots(L):
     four = plan(L, 4, 8192, 3584, batch=4)[1]
     assert four.arm == one.arm == 1
     assert four.workspace_bytes == (four.split_k * 4 * 4 * 8192 * 4 if four.split_k > 1 else 0)
+
+
+@pytest.mark.parametrize("M,N,K", [(1322, 19456, 2560), (64, 2560, 9728), (200, 300, 640),
+                                   (4096, 2560, 9728), (33, 8192, 8192)])
+def test_tensor_tiles_are_valid(L, M, N, K):
+    st, info = plan(L, M, N, K)
+    assert st == OK and info.arm == 2
+    assert 32 <= info.tile_tokens <= 256 and info.tile_tokens % 32 == 0
+    assert 1 <= info.ctas <= 2 * SMS
+    blocks = K // 128
+    assert 1 <= info.split_k <= min(blocks, 16)
+    assert info.workspace_bytes == (info.split_k * M * N * 4 if info.split_k > 1 else 0)
+
+
+@pytest.mark.parametrize("tile", [32, 64, 128, 192, 256])
+def test_forced_tile_is_honoured(L, tile):
+    st, info = plan(L, 300, 2560, 1024, arm=2, tile=tile)
+    assert st == OK and info.tile_tokens == tile
+
+
+@pytest.mark.parametrize("bad", [16, 48, 288, -32])
+def test_bad_forced_tiles_are_refused(L, bad):
+    assert plan(L, 300, 2560, 1024, arm=2, tile=bad)[0] != OK
+
+
+def test_forced_tile_on_the_decode_arm_is_refused(L):
+    assert plan(L, 4, 2560, 1024, arm=1, tile=64)[0] == INVALID
+
+
+@pytest.mark.parametrize("request_,want", [(1, 1), (2, 2), (3, 4), (5, 8), (8, 8), (16, 16), (40, 16)])
+def test_forced_decode_split_rounds_up_to_a_slice_count(L, request_, want):
+    # K = 2048 is 16 blocks; slices hold 1, 2, 4, 8 or 16 of them, and a request
+    # becomes the nearest feasible count from above (16 at most).
+    st, info = plan(L, 1, 384, 2048, arm=1, split_k=request_, flags=4)
+    assert st == OK and info.split_k == want
+
+
+def test_forced_tensor_split(L):
+    for sk in (1, 2, 5, 20):
+        st, info = plan(L, 128, 2560, 2560, arm=2, split_k=sk)
+        assert st == OK and info.split_k == min(sk, 20)
+
+
+def test_forced_arms(L):
+    assert plan(L, 1, 2560, 1024, arm=2)[1].arm == 2            # one token on the tensor arm
+    assert plan(L, 64, 2560, 1024, arm=1)[1].arm == 1           # 64 tokens on the decode arm
+    assert plan(L, 1, 2560, 1024, arm=7)[0] == INVALID
+
+
+def test_whole_k_refused_where_x_does_not_fit(L):
+    # The whole-K kernel stages all of X: up to 8 tokens with M * K <= 16384.
+    assert plan(L, 2, 2560, 8192, flags=2)[1].whole_k
+    assert plan(L, 4, 2560, 8192, flags=2)[0] == UNSUPPORTED
+    assert plan(L, 9, 256, 512, flags=2)[0] == UNSUPPORTED
