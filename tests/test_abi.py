@@ -180,3 +180,27 @@ def test_zero_point_entry_points_check_arguments(L):
     assert L.w4a16_plan_batched(2, 4, 256, 512, 128, ctypes.byref(zp), ctypes.byref(info)) == UNSUPPORTED
     assert L.w4a16_dequant_zp_fp32(FAKE, FAKE, None, FAKE, 16, 128, 128, None) == INVALID
     assert L.w4a16_dequant_zp_bf16(FAKE, FAKE, FAKE, FAKE, 16, 128, 48, None) == UNSUPPORTED
+
+
+def test_python_binding_refuses_cpu_tensors():
+    # No CPU path: host tensors are an error before any library call.
+    import torch
+    import bf16_activation_quantized_gb300 as w4
+    x = torch.zeros(2, 256, dtype=torch.bfloat16)
+    wp = torch.zeros(256 * 128, dtype=torch.uint8)
+    s = torch.zeros(256, 2, dtype=torch.bfloat16)
+    for call in (lambda: w4.gemm(x, wp, s),
+                 lambda: w4.gemm(x, wp, s, zeros=torch.zeros(256, 2, dtype=torch.uint8)),
+                 lambda: w4.pack(torch.zeros(256, 128, dtype=torch.uint8)),
+                 lambda: w4.dequant_fp32(wp, s),
+                 lambda: w4.gemm_batched(x[None], wp[None], s[None])):
+        with pytest.raises(ValueError):
+            call()
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    from bf16_activation_quantized_gb300 import _lib as lib_mod
+    monkeypatch.setattr(lib_mod, "_lib", None)
+    monkeypatch.setattr(lib_mod, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        lib_mod.lib()
