@@ -101,6 +101,12 @@ def _workspace_need(M: int, N: int, K: int, G: int, o: Options, dev_index: int) 
     return need
 
 
+def _plan_dict(info: PlanInfo) -> dict:
+    return {"arm": {1: "decode", 2: "tensor"}.get(info.arm, info.arm), "split_k": info.split_k,
+            "tile_tokens": info.tile_tokens, "ctas": info.ctas,
+            "workspace_bytes": int(info.workspace_bytes), "whole_k": bool(info.whole_k)}
+
+
 def layout_version() -> int:
     return int(_lib.lib().w4a16_layout_version())
 
@@ -130,10 +136,15 @@ def pack(w_canon: torch.Tensor) -> torch.Tensor:
 
 def plan(M: int, N: int, K: int, arm=None, split_k: int = 0, tile_tokens: int = 0,
          device=None, decode_kernel=None, group_size: int = GROUP,
-         zero_points: bool = False) -> dict:
-    """What the dispatcher picks for this shape on the (current) device."""
+         zero_points: bool = False, sms: int | None = None) -> dict:
+    """What the dispatcher picks for this shape on the (current) device, or,
+    with ``sms``, on a device with that many SMs (host only, no GPU needed)."""
     info = PlanInfo()
     o = _opts(arm, split_k, tile_tokens, decode_kernel=decode_kernel, zero_points=zero_points)
+    if sms is not None:
+        _lib.check(_lib.lib().w4a16_plan_for_sms(int(sms), 1, M, N, K, group_size, ctypes.byref(o),
+                                                 ctypes.byref(info)), "w4a16_plan_for_sms")
+        return _plan_dict(info)
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         _lib.check(_lib.lib().w4a16_plan(M, N, K, group_size, ctypes.byref(o), ctypes.byref(info)),
                    "w4a16_plan")

@@ -162,3 +162,14 @@ def test_whole_k_refused_where_x_does_not_fit(L):
     assert plan(L, 2, 2560, 8192, flags=2)[1].whole_k
     assert plan(L, 4, 2560, 8192, flags=2)[0] == UNSUPPORTED
     assert plan(L, 9, 256, 512, flags=2)[0] == UNSUPPORTED
+
+
+def test_python_plan_for_sms_needs_no_gpu():
+    import bf16_activation_quantized_gb300 as w4
+    p = w4.plan(1, 8192, 8192, sms=SMS)
+    assert p == {"arm": "decode", "split_k": 8, "tile_tokens": 8, "ctas": p["ctas"],
+                 "workspace_bytes": 8 * 8192 * 4, "whole_k": False}
+    assert w4.plan(1322, 19456, 2560, sms=SMS)["tile_tokens"] == 192
+    assert w4.plan(1, 19456, 2560, sms=SMS, group_size=32, zero_points=True)["whole_k"] is False
+    with pytest.raises(w4.W4A16Error):
+        w4.plan(1, 256, 512, sms=SMS, group_size=16)
