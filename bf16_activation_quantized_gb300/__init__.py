@@ -148,9 +148,7 @@ def plan(M: int, N: int, K: int, arm=None, split_k: int = 0, tile_tokens: int = 
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         _lib.check(_lib.lib().w4a16_plan(M, N, K, group_size, ctypes.byref(o), ctypes.byref(info)),
                    "w4a16_plan")
-    return {"arm": {1: "decode", 2: "tensor"}.get(info.arm, info.arm), "split_k": info.split_k,
-            "tile_tokens": info.tile_tokens, "ctas": info.ctas,
-            "workspace_bytes": int(info.workspace_bytes), "whole_k": bool(info.whole_k)}
+    return _plan_dict(info)
 
 
 def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=None,
@@ -241,9 +239,7 @@ def plan_batched(batch: int, M: int, N: int, K: int, arm=None, split_k: int = 0,
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         _lib.check(_lib.lib().w4a16_plan_batched(batch, M, N, K, group_size, ctypes.byref(o),
                                                  ctypes.byref(info)), "w4a16_plan_batched")
-    return {"arm": {1: "decode", 2: "tensor"}.get(info.arm, info.arm), "split_k": info.split_k,
-            "tile_tokens": info.tile_tokens, "ctas": info.ctas,
-            "workspace_bytes": int(info.workspace_bytes), "whole_k": bool(info.whole_k)}
+    return _plan_dict(info)
 
 
 def gemm_batched(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=None,
