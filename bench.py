@@ -11,11 +11,14 @@ while the kernel before it is still running).  Metric: algorithmic bytes (packed
 second, in GB/s.
 
 Timing: W eager warm-up steps, then exactly K steps replayed from CUDA graphs
-(graphs of up to G steps), bracketed by a barrier and a synchronize, timed
-with CUDA events on the launching stream.  Each step uses the next of C
-weight copies whose total exceeds 4x the L2 size, so every call streams its
-weights from HBM.  SM clocks and throttle reasons are sampled with nvidia-smi
-during the timed region.
+(one graph of K steps when K <= 2000, else graphs of G steps), bracketed by a
+barrier and a synchronize, timed with CUDA events on the launching stream.
+A device-side sleep kernel is queued just before the start event, so the
+host has enqueued the graph launches by the time the start event fires and
+the timed region holds the K steps back to back, not the host's launch
+latency.  Each step uses the next of C weight copies whose total exceeds 4x
+the L2 size, so every call streams its weights from HBM.  SM clocks and
+throttle reasons are sampled with nvidia-smi during the timed region.
 
 Also reported: the roofline of the dominant kernel (the decode kernel, timed
 alone from a graph of back-to-back launches, so inter-launch gaps count
@@ -192,6 +195,10 @@ class Shape:
         self.M, self.N, self.K = M, N, K
         to_bf16 = lambda a: torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(device)
         self.x = to_bf16(inp.x)
+        # X rotates with the weights (a copy per weight copy), so no call finds
+        # its activations in L2 either; end_to_end pins self.x instead.
+        self.xs = [self.x] + [self.x.clone() for _ in range(copies - 1)]
+        self.pin_x = False
         s = to_bf16(inp.scales)
         wp = w4.pack(torch.from_numpy(inp.w_canon.copy()).to(device))
         self.w = [wp] + [wp.clone() for _ in range(copies - 1)]
@@ -205,9 +212,12 @@ class Shape:
         self.ws = torch.empty(max(self.plan["workspace_bytes"], 256), dtype=torch.uint8, device=device)
         self.launches = 1 + (1 if self.plan["split_k"] > 1 else 0)
 
+    def xin(self, c):
+        return self.x if self.pin_x else self.xs[c]
+
     def call(self, w4, i):
         c = i % len(self.w)
-        w4.gemm(self.x, self.w[c], self.s[c], out=self.y, workspace=self.ws, resident_weights=True,
+        w4.gemm(self.xin(c), self.w[c], self.s[c], out=self.y, workspace=self.ws, resident_weights=True,
                 zeros=self.z[c] if self.z else None)
 
     def partials(self, w4, i):
@@ -216,7 +226,7 @@ class Shape:
         c = i % len(self.w)
         if self.plan["split_k"] == 1:
             return self.call(w4, i)
-        return w4.gemm_partials(self.x, self.w[c], self.s[c], out=self.y, workspace=self.ws,
+        return w4.gemm_partials(self.xin(c), self.w[c], self.s[c], out=self.y, workspace=self.ws,
                                 resident_weights=True)
 
     def reduce(self, w4):
@@ -245,10 +255,19 @@ def capture(torch, fn, n):
     return g
 
 
+def hide_launch_latency(torch, launches: int):
+    """Queue a device-side sleep long enough for the host to enqueue
+    `launches` graph launches behind it (about 20 us each), so that a start
+    event recorded after it fires with the timed work already queued."""
+    us = min(20000, 50 + 20 * launches)
+    torch.cuda._sleep(int(us * 2000))        # cycles at about 2 GHz
+
+
 def time_graph(torch, g, reps=1):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    hide_launch_latency(torch, reps)
     e0.record()
     for _ in range(reps):
         g.replay()
@@ -283,8 +302,13 @@ def our_arm(args, world, rank, local, dist):
         step(i)
     torch.cuda.synchronize()
 
-    G = max(1, min(args.graph_steps, args.steps))
-    G = max(C, (G // C) * C)
+    # Up to 2000 steps are one graph of exactly K steps; longer runs replay
+    # graphs of G steps (a multiple of the weight copies) and a remainder.
+    if args.steps <= 2000:
+        G = args.steps
+    else:
+        G = max(1, min(args.graph_steps, args.steps))
+        G = max(C, (G // C) * C)
     full, rem = divmod(args.steps, G)
     g_full = capture(torch, step, G) if full else None
     g_rem = capture(torch, step, rem) if rem else None
@@ -301,6 +325,7 @@ def our_arm(args, world, rank, local, dist):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    hide_launch_latency(torch, full + (1 if g_rem else 0))
     e0.record()
     for _ in range(full):
         g_full.replay()
@@ -351,7 +376,8 @@ def our_arm(args, world, rank, local, dist):
         "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
     }
     if rank == 0 and not args.no_shapes:
-        out["per_shape"] = per_shape_table(torch, w4, syn, metrics, device, peaks)
+        out["per_shape"] = per_shape_table(torch, w4, syn, metrics, device, peaks,
+                                           cpu=world == 1 and not args.no_cpu_baseline)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return out
@@ -390,6 +416,7 @@ def end_to_end(torch, w4, shapes, steps, step_bytes):
     for s, nx, ny in zip(shapes, xs, ys):     # offsets keep every X 16-byte aligned
         dx[ox:ox + nx].copy_(s.x.reshape(-1))
         s.x = dx[ox:ox + nx].view(s.M, s.K)
+        s.pin_x = True
         s.y = dy[oy:oy + ny].view(s.M, s.N)
         ox += nx
         oy += ny
@@ -430,6 +457,7 @@ def end_to_end(torch, w4, shapes, steps, step_bytes):
     finally:
         for s, (x, y) in zip(shapes, saved):
             s.x, s.y = x, y
+            s.pin_x = False
     return {"value": round(step_bytes * steps / dt_graph / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
             "eager_value": round(step_bytes * steps / dt_eager / 1e9, 1),
@@ -449,7 +477,58 @@ ZP_SHAPES = [("decode_gemv_zp", 1, 8192, 8192, 128), ("decode_gemv_zp", 1, 17408
              ("prefill_zp", 1322, 19456, 2560, 128), ("prefill_zp", 1322, 19456, 2560, 32)]
 
 
-def per_shape_table(torch, w4, syn, metrics, device, peaks, only=None, group_size=128, zp=False):
+def oracle_sample_rate(compute_cols, N, nbytes, flops, budget_s=0.3):
+    """The CPU oracle on a bounded sample of a row's work: compute_cols(c)
+    computes output features [0, c) of every token; the time is scaled to the
+    whole shape's algorithmic bytes and FLOPs (the oracle's work per feature is
+    the same for every feature)."""
+    import oracle
+    c = max(1, N // 256)
+    t0 = time.perf_counter()
+    compute_cols(c)
+    t = time.perf_counter() - t0
+    want = min(N, max(1, int(c * budget_s / max(t, 1e-6))))
+    if want > c:
+        c = want
+        t0 = time.perf_counter()
+        compute_cols(c)
+        t = time.perf_counter() - t0
+    frac = c / N
+    return {"value": round(nbytes * frac / t / 1e9, 4), "unit": "GB/s",
+            "tflops": round(flops * frac / t / 1e12, 6), "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"output features [0, {c}) of {N} ({frac:.4f} of the shape), {t:.2f} s"}
+
+
+def row_e2e(torch, w4, s, reps, nbytes, flops):
+    """One shape through the public API with host buffers: every call copies X
+    in from pinned host memory and Y back to it (wall clock, eager calls)."""
+    hx = s.x.cpu().pin_memory()
+    hy = torch.empty((s.M, s.N), dtype=torch.bfloat16).pin_memory()
+    s.pin_x = True
+    try:
+        def one(i):
+            s.x.copy_(hx, non_blocking=True)
+            s.call(w4, i)
+            hy.copy_(s.y, non_blocking=True)
+        for i in range(3):
+            one(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(reps):
+            one(i)
+        torch.cuda.synchronize()
+        dt = (time.perf_counter() - t0) / reps
+    finally:
+        s.pin_x = False
+    return {"value": round(nbytes / dt / 1e9, 1), "unit": "GB/s", "tflops": round(flops / dt / 1e12, 3),
+            "h2d_bytes_per_call": int(hx.numel() * 2), "d2h_bytes_per_call": int(hy.numel() * 2),
+            "calls": reps, "note": "wall clock, eager calls through w4a16_gemm; X copied in "
+                                   "from pinned host memory and Y read back every call"}
+
+
+def per_shape_table(torch, w4, syn, metrics, device, peaks, only=None, group_size=128, zp=False,
+                    cpu=True):
     shapes = [("tiny", 4, 256, 512, 128, False)]
     for name, lst in (("decode_gemv", syn.WORKLOADS["decode_gemv"]),
                       ("decode_sweep_gate_up", syn.WORKLOADS["decode_sweep_gate_up"]),
@@ -477,18 +556,31 @@ def per_shape_table(torch, w4, syn, metrics, device, peaks, only=None, group_siz
         nbytes = metrics.algorithmic_bytes(M, N, K, G) + (N * (K // G) if with_zp else 0)
         fl = metrics.flops(M, N, K)
         t_roof = metrics.roofline_seconds(fl, nbytes, peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
-        rows.append({"workload": name, "M": M, "N": N, "K": K, "group_size": G, "zero_points": with_zp,
-                     "us": round(t * 1e6, 3),
-                     "tflops": round(fl / t / 1e12, 3), "gbs": round(nbytes / t / 1e9, 1),
-                     "roofline_frac": round(t_roof / t, 4),
-                     "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) >= fl / (peaks["bf16_tflops"] * 1e12) else "tensor",
-                     "arm": s.plan["arm"], "split_k": s.plan["split_k"], "copies": C})
+        row = {"workload": name, "M": M, "N": N, "K": K, "group_size": G, "zero_points": with_zp,
+               "us": round(t * 1e6, 3),
+               "tflops": round(fl / t / 1e12, 3), "gbs": round(nbytes / t / 1e9, 1),
+               "roofline_frac": round(t_roof / t, 4),
+               "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) >= fl / (peaks["bf16_tflops"] * 1e12) else "tensor",
+               "arm": s.plan["arm"], "split_k": s.plan["split_k"], "whole_k": s.plan["whole_k"],
+               "copies": C}
+        if name == "prefill":
+            row["e2e"] = row_e2e(torch, w4, s, 20, nbytes, fl)
+        if cpu:
+            import oracle
+            inp = s.inp
+            if with_zp:
+                zc = syn.make_zeros(N, K, G, seed=0)
+                fn = lambda c: oracle.gemm_zp(inp.x, inp.w_canon[:c], inp.scales[:c], zc[:c], M, c, K, G=G)
+            else:
+                fn = lambda c: oracle.gemm(inp.x, inp.w_canon[:c], inp.scales[:c], M, c, K, G=G)
+            row["cpu_baseline"] = oracle_sample_rate(fn, N, nbytes, fl)
+        rows.append(row)
         del g, s
         torch.cuda.empty_cache()
     if only is None:
-        rows.append(grouped_row(torch, w4, syn, metrics, device, peaks))
+        rows.append(grouped_row(torch, w4, syn, metrics, device, peaks, cpu))
         for B, M, N, K in BATCHED_SHAPES:
-            rows.append(batched_row(torch, w4, syn, metrics, device, peaks, B, M, N, K))
+            rows.append(batched_row(torch, w4, syn, metrics, device, peaks, B, M, N, K, cpu))
     return rows
 
 
@@ -497,7 +589,7 @@ def per_shape_table(torch, w4, syn, metrics, device, peaks, only=None, group_siz
 BATCHED_SHAPES = [(4, 128, 8192, 3584), (2, 2048, 7168, 8192)]
 
 
-def batched_row(torch, w4, syn, metrics, device, peaks, B, M, N, K):
+def batched_row(torch, w4, syn, metrics, device, peaks, B, M, N, K, cpu=True):
     inps = [syn.make_gemm_inputs(M, N, K, seed=b) for b in range(B)]
     bits = lambda a: torch.from_numpy(a.view("int16").copy()).view(torch.bfloat16).to(device)
     x = torch.stack([bits(i.x) for i in inps])
@@ -519,12 +611,17 @@ def batched_row(torch, w4, syn, metrics, device, peaks, B, M, N, K):
            "roofline_frac": round(t_roof / t, 4),
            "bound": "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) >= fl / (peaks["bf16_tflops"] * 1e12) else "tensor",
            "arm": plan["arm"], "split_k": plan["split_k"], "copies": C}
+    if cpu:
+        import oracle
+        row["cpu_baseline"] = oracle_sample_rate(
+            lambda c: [oracle.gemm(i.x, i.w_canon[:c], i.scales[:c], M, c, K) for i in inps],
+            N, nbytes, fl)
     del g, ws
     torch.cuda.empty_cache()
     return row
 
 
-def grouped_row(torch, w4, syn, metrics, device, peaks):
+def grouped_row(torch, w4, syn, metrics, device, peaks, cpu=True):
     """The grouped workload: one launch over all groups, sizes read on the device."""
     G, MT, N, K = (syn.GROUPED_WORKLOAD[k] for k in ("num_groups", "M_total", "N", "K"))
     inp = syn.make_grouped_inputs(G, MT, N, K, seed=0)
@@ -549,6 +646,11 @@ def grouped_row(torch, w4, syn, metrics, device, peaks):
            "us": round(t * 1e6, 3), "tflops": round(fl / t / 1e12, 3), "gbs": round(nbytes / t / 1e9, 1),
            "roofline_frac": round(t_roof / t, 4), "bound": "tensor", "arm": "tensor (grouped)",
            "split_k": 1, "copies": C}
+    if cpu:
+        import oracle
+        row["cpu_baseline"] = oracle_sample_rate(
+            lambda c: oracle.gemm_grouped(inp.x, inp.w_canon[:, :c], inp.scales[:, :c], inp.m_sizes,
+                                          MT, c, K), N, nbytes, fl)
     del g, ws
     torch.cuda.empty_cache()
     return row

@@ -26,7 +26,8 @@ ARM_AUTO, ARM_DECODE, ARM_TENSOR = 0, 1, 2
 _ARMS = {None: ARM_AUTO, "auto": ARM_AUTO, "decode": ARM_DECODE, "tensor": ARM_TENSOR}
 
 __all__ = ["GROUP", "pack", "gemm", "gemm_partials", "gemm_grouped", "gemm_batched", "plan_batched", "dequant_fp32", "dequant_bf16",
-           "splitk_reduce", "plan", "packed_weight_bytes", "layout_version", "W4A16Error"]
+           "splitk_reduce", "plan", "packed_weight_bytes", "layout_version", "read_error_word",
+           "ERROR_WAIT_TIMEOUT", "W4A16Error"]
 
 
 def _stream_ptr(device) -> int:
@@ -46,6 +47,8 @@ FLAG_RESIDENT_WEIGHTS = 1
 FLAG_DECODE_WHOLE_K = 2
 FLAG_DECODE_K_SLICES = 4
 FLAG_ZERO_POINTS = 8
+FLAG_TEST_STALL = 16
+ERROR_WAIT_TIMEOUT = 1       # error-word bit: a bounded wait in a kernel ran out
 _KERNELS = {None: 0, "auto": 0, "whole_k": FLAG_DECODE_WHOLE_K, "k_slices": FLAG_DECODE_K_SLICES}
 
 
@@ -57,13 +60,14 @@ def _group_size(K: int, cols: int, what: str) -> int:
     return K // cols
 
 
-def _opts(arm, split_k, tile_tokens, resident_weights=False, decode_kernel=None, zero_points=False):
+def _opts(arm, split_k, tile_tokens, resident_weights=False, decode_kernel=None, zero_points=False,
+          test_stall=False):
     if arm not in _ARMS:
         raise ValueError(f"arm must be one of {list(_ARMS)}")
     if decode_kernel not in _KERNELS:
         raise ValueError(f"decode_kernel must be one of {list(_KERNELS)}")
     flags = ((FLAG_RESIDENT_WEIGHTS if resident_weights else 0) | _KERNELS[decode_kernel]
-             | (FLAG_ZERO_POINTS if zero_points else 0))
+             | (FLAG_ZERO_POINTS if zero_points else 0) | (FLAG_TEST_STALL if test_stall else 0))
     return Options(_ARMS[arm], int(split_k), int(tile_tokens), flags)
 
 
@@ -111,6 +115,17 @@ def layout_version() -> int:
     return int(_lib.lib().w4a16_layout_version())
 
 
+def read_error_word(clear: bool = True, device=None) -> int:
+    """The device error word (w4a16_read_error_word): OR of the ERROR_* bits
+    the kernels recorded since it was last cleared; 0 means no kernel gave up.
+    Waits for all work on the device first; ``clear`` resets the word."""
+    v = ctypes.c_int(0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _lib.check(_lib.lib().w4a16_read_error_word(ctypes.byref(v), 1 if clear else 0),
+                   "w4a16_read_error_word")
+    return int(v.value)
+
+
 def packed_weight_bytes(N: int, K: int) -> int:
     key = (N, K)
     nb = _pwb_cache.get(key)
@@ -154,7 +169,8 @@ def plan(M: int, N: int, K: int, arm=None, split_k: int = 0, tile_tokens: int = 
 def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=None,
          split_k: int = 0, tile_tokens: int = 0, out: torch.Tensor | None = None,
          workspace: torch.Tensor | None = None, resident_weights: bool = False,
-         decode_kernel=None, zeros: torch.Tensor | None = None) -> torch.Tensor:
+         decode_kernel=None, zeros: torch.Tensor | None = None,
+         test_stall: bool = False) -> torch.Tensor:
     """Y = X . dequant(W)^T.  x: bf16 [M, K]; scales: bf16 [N, K/G]; returns bf16 [M, N].
 
     ``zeros`` (uint8 [N, K/G], low four bits) selects the zero-point variant,
@@ -163,7 +179,9 @@ def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=N
     ``resident_weights=True`` promises that no kernel still running on the
     current stream writes ``w_packed`` or ``scales`` (W4A16_FLAG_RESIDENT_WEIGHTS):
     the call may then start streaming them before the previous kernel ends.
-    ``decode_kernel`` ("whole_k" or "k_slices") forces the decode arm's kernel."""
+    ``decode_kernel`` ("whole_k" or "k_slices") forces the decode arm's kernel.
+    ``test_stall`` (tests only, W4A16_FLAG_TEST_STALL) makes the decode kernel's
+    bounded waits run out: the outputs become NaN and the error word is set."""
     _need_cuda(x, "x", torch.bfloat16)
     _need_cuda(scales, "scales", torch.bfloat16)
     _need_cuda(w_packed, "w_packed", torch.uint8)
@@ -180,7 +198,8 @@ def gemm(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=N
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     else:
         _need_cuda(out, "out", torch.bfloat16)
-    o = _opts(arm, split_k, tile_tokens, resident_weights, decode_kernel, zeros is not None)
+    o = _opts(arm, split_k, tile_tokens, resident_weights, decode_kernel, zeros is not None,
+              test_stall)
     L = _lib.lib()
     dev = x.device
     switch = dev.index != torch.cuda.current_device()
@@ -217,6 +236,11 @@ def gemm_partials(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor,
 
     With SPLIT_K > 1 the fp32 partial sums land in ``workspace`` as
     [SPLIT_K, M, N] and ``out`` is untouched; splitk_reduce() finishes the call."""
+    _need_cuda(x, "x", torch.bfloat16)
+    _need_cuda(scales, "scales", torch.bfloat16)
+    _need_cuda(w_packed, "w_packed", torch.uint8)
+    _need_cuda(out, "out", torch.bfloat16)
+    _need_cuda(workspace, "workspace")
     M, K = x.shape
     N = scales.shape[0]
     G = _group_size(K, scales.shape[1], "scales [N, K/G]")

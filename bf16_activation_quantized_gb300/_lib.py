@@ -28,6 +28,7 @@ class PlanInfo(ctypes.Structure):
 # name -> (restype, argtypes); mirrors include/w4a16.h one to one.
 SIGNATURES = {
     "w4a16_status_string": (ctypes.c_char_p, [I]),
+    "w4a16_read_error_word": (I, [ctypes.POINTER(I), I]),
     "w4a16_layout_version": (I, []),
     "w4a16_packed_weight_bytes": (SZ, [I, I]),
     "w4a16_pack_weights": (I, [P, P, I, I, P]),

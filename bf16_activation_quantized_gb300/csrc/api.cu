@@ -45,8 +45,7 @@ using namespace w4a16;
 namespace {
 
 constexpr int kDecodeCtasPerSm = 2;           // resident decode CTAs per SM
-constexpr int kDecodeRing = 8;                // weight-ring stages per decode CTA
-constexpr int kDecodeInFlight = 3;            // bulk copies in the air per decode CTA
+constexpr int kDecodeInFlight = 3;            // bulk copies (ring stages) in the air per decode CTA
 constexpr double kHbmBytesPerS = 6.5e12;      // planning figures, not measurements
 constexpr double kCtaBytesPerS = 25e9;        // one CTA's streaming rate (32 KB in flight)
 constexpr double kL2BytesPerS = 20e12;
@@ -135,7 +134,7 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int bat
     d->split_k = groups;
     d->groups_per_slice = 1;
     d->ctas_per_slice = 1;
-    d->ring = kDecodeRing;
+    d->ring = 0;
     d->in_flight = kDecodeInFlight;
     d->wk_blocks = 0;
     if (wk != 2 && forced_split <= 1 && sub == 1 && !zp) {
@@ -176,6 +175,7 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int bat
     for (int gps : {16, 8, 4, 2, 1}) {
         if (gps > gps_max || groups % gps) continue;
         if (forced_gps && gps != forced_gps) continue;
+        if (decode_ring_stages(M, d->mt, gps, sub) == 0) continue;   // shared memory
         const int sk = groups / gps;
         const long long per_slice = slots / ((long long)sk * d->token_blocks);
         const int cmax = int(per_slice < 1 ? 1 : (per_slice > d->n_tiles ? d->n_tiles : per_slice));
@@ -196,6 +196,7 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int bat
                 d->groups_per_slice = gps;
                 d->ctas_per_slice = C;
                 d->wk_blocks = 0;
+                d->ring = decode_ring_stages(M, d->mt, gps, sub);
             }
         }
     }
@@ -347,13 +348,19 @@ w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, 
     if (opts && opts->split_k < 0) return W4A16_ERR_INVALID_ARG;
     const int flags = opts ? opts->flags : 0;
     if (flags & ~int(W4A16_FLAG_RESIDENT_WEIGHTS | W4A16_FLAG_DECODE_WHOLE_K | W4A16_FLAG_DECODE_K_SLICES |
-                     W4A16_FLAG_ZERO_POINTS))
+                     W4A16_FLAG_ZERO_POINTS | W4A16_FLAG_TEST_STALL))
         return W4A16_ERR_INVALID_ARG;
+    const bool stall = (flags & W4A16_FLAG_TEST_STALL) != 0;
     const bool zp = (flags & W4A16_FLAG_ZERO_POINTS) != 0;
     if (zp && batch > 1) return W4A16_ERR_UNSUPPORTED;
     if ((flags & W4A16_FLAG_DECODE_WHOLE_K) && (flags & W4A16_FLAG_DECODE_K_SLICES))
         return W4A16_ERR_INVALID_ARG;
-    const int wk = (flags & W4A16_FLAG_DECODE_WHOLE_K) ? 1 : (flags & W4A16_FLAG_DECODE_K_SLICES) ? 2 : 0;
+    int wk = (flags & W4A16_FLAG_DECODE_WHOLE_K) ? 1 : (flags & W4A16_FLAG_DECODE_K_SLICES) ? 2 : 0;
+    if (stall) {
+        // Only the K-slice decode kernel has the stall mode.
+        if (wk == 1) return W4A16_ERR_UNSUPPORTED;
+        wk = 2;
+    }
     const int forced_bt = opts ? opts->tile_tokens : 0;
     if (forced_bt != 0 && (forced_bt < 32 || forced_bt > 256 || forced_bt % 32))
         return W4A16_ERR_UNSUPPORTED;
@@ -361,11 +368,17 @@ w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, 
     if (sms <= 0 && (device_sm_count(&sms) != 0 || sms < 1)) return W4A16_ERR_CUDA;
     if (arm == W4A16_ARM_AUTO) arm = M <= kDecodeMaxM ? W4A16_ARM_DECODE : W4A16_ARM_TENSOR;
     if (arm == W4A16_ARM_DECODE && forced_bt != 0) return W4A16_ERR_INVALID_ARG;
+    if (stall && arm != W4A16_ARM_DECODE) return W4A16_ERR_UNSUPPORTED;
     p->arm = arm;
     if (arm == W4A16_ARM_DECODE) {
         DecodePlan &d = p->decode;
         plan_decode(M, N, K, sms, opts ? opts->split_k : 0, wk, batch, sub, zp, &d);
         if (wk == 1 && d.wk_blocks == 0) return W4A16_ERR_UNSUPPORTED;
+        if (stall) {
+            // Test only: no weight copies, and waits that give up after 1 ms.
+            d.in_flight = 0;
+            d.wait_us = 1000;
+        }
         p->split_k = d.split_k;
         p->ctas = batch * (d.wk_blocks ? d.ctas_per_slice : d.ctas_per_slice * d.split_k * d.token_blocks);
         p->tile_tokens = 8 * d.mt;

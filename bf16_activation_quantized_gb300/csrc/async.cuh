@@ -4,7 +4,8 @@
 // %globaltimer time sets an error bit in the kernel's error word and returns
 // false, and once a CTA has seen a timeout (its shared abort flag is set) all
 // later waits return immediately, so a broken pipeline ends the kernel instead
-// of hanging the GPU.
+// of hanging the GPU.  A CTA that aborts writes NaN to every output it owns
+// (see the kernels), so an incomplete result is never a plausible number.
 #pragma once
 
 #include <cstdint>
@@ -14,7 +15,8 @@ namespace w4a16 {
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
-// Error bits a kernel may record (read back with w4a16_debug_error_word).
+// Error bits a kernel may record in the library's device error word (read
+// back, and cleared, with w4a16_read_error_word).
 constexpr int kErrWaitTimeout = 1;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -88,21 +90,44 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return ok != 0;
 }
 
+// Whether more than limit_ns have passed since *t0 on %globaltimer.  The timer
+// is a wall clock that the driver may adjust; a reading below *t0 restarts the
+// interval instead of being taken, as an unsigned difference would be, for a
+// wait of about 2^64 ns.
+__device__ __forceinline__ bool elapsed_beyond(unsigned long long *t0, unsigned long long limit_ns) {
+    const unsigned long long now = global_timer_ns();
+    if (now < *t0) {
+        *t0 = now;
+        return false;
+    }
+    return now - *t0 > limit_ns;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false on
-// timeout or when the CTA is already aborting.
+// timeout (after limit_ns) or when the CTA is already aborting.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          int *err_word) {
+                                          int *err_word,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_timer_ns();
+    unsigned long long t0 = global_timer_ns();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (elapsed_beyond(&t0, limit_ns)) {
             *abort_flag = 1;
             if (err_word) atomicOr(err_word, kErrWaitTimeout);
             return false;
         }
     }
+}
+
+// Wait, ignoring the abort flag, for a phase that copies still in flight will
+// complete (used only when aborting, so that no copy lands in shared memory
+// after the CTA has exited); gives up after 100 ms.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (elapsed_beyond(&t0, 100000000ull)) break;
 }
 
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,

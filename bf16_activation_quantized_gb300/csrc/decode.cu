@@ -25,7 +25,7 @@ namespace {
 // the kernel writes Y itself: no workspace, no second kernel.
 struct WkSmem {
     int x_stride, n_groups;
-    int off_ring, off_bar, off_abort, off_xmax, off_x, off_corr, off_scale, off_red, total;
+    int off_ring, off_bar, off_abort, off_xmax, off_x, off_scale, off_red, total;
 };
 
 // Scale vectors (8 bf16) a consumer thread stages: B * 16 rows x K / 128
@@ -42,8 +42,7 @@ __host__ __device__ inline WkSmem wk_smem_layout(int B, int rows, int K) {
     L.off_abort = L.off_bar + 2 * kRing * 8;
     L.off_xmax = L.off_abort + 16;             // [8 tokens][P parts] int
     L.off_x = L.off_xmax + 8 * 8 * 4;
-    L.off_corr = L.off_x + ((rows * L.x_stride * 2 + 15) & ~15);
-    L.off_scale = L.off_corr + L.n_groups * 4 * 16;           // float4 per (group, quad)
+    L.off_scale = L.off_x + ((rows * L.x_stride * 2 + 15) & ~15);
     L.off_red = L.off_scale + ((B * 16 * L.n_groups * 2 + 15) & ~15);   // bf16 [B*16 rows][groups]
     L.total = L.off_red + (P - 1) * B * 512;   // float4 per lane per (part > 0, block)
     return L;
@@ -84,7 +83,6 @@ decode_wk_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_abort);
     int *s_xmax = reinterpret_cast<int *>(smem + L.off_xmax);
     uint16_t *s_x = reinterpret_cast<uint16_t *>(smem + L.off_x);
-    float *s_corr = reinterpret_cast<float *>(smem + L.off_corr);
     uint16_t *s_scale = reinterpret_cast<uint16_t *>(smem + L.off_scale);
     float4 *s_red = reinterpret_cast<float4 *>(smem + L.off_red);
 
@@ -259,44 +257,28 @@ decode_wk_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         }
     }
     consumer_bar();
-    // Convert X in place to fp16 x * 2^-sh(token, part) and build the
-    // per-group correction table (as decode_kernel): 8 lanes per (token, group).
+    // Convert X in place to fp16 x * 2^-sh(token, part) (as decode_kernel):
+    // 8 lanes per (token, group).
     {
         const int pairs = rows * G;
         const int part = threadIdx.x & 7;
-        for (int base = 0; base < pairs; base += kDecodeWarps * 32 / 8) {
-            const int pi = base + (threadIdx.x >> 3);
+        for (int pi = threadIdx.x >> 3; pi < pairs; pi += kDecodeWarps * 32 / 8) {
             const int r = pi / G, gi = pi - r * G;
-            float a = 0.f;
-            if (pi < pairs) {
-                int kp = 0;
-                while (kp + 1 < P && wk_part_start(kp + 1, P, G) <= gi) ++kp;
-                const float down = pow2f(-slice_shift(s_xmax[r * 8 + kp]));
-                uint4 *src = reinterpret_cast<uint4 *>(s_x + r * L.x_stride + gi * kGroup) + part;
+            int kp = 0;
+            while (kp + 1 < P && wk_part_start(kp + 1, P, G) <= gi) ++kp;
+            const float down = pow2f(-slice_shift(s_xmax[r * 8 + kp]));
+            uint4 *src = reinterpret_cast<uint4 *>(s_x + r * L.x_stride + gi * kGroup) + part;
 #pragma unroll
-                for (int hh = 0; hh < 16; hh += 8) {
-                    const uint4 q = src[hh];
-                    const uint32_t qv[4] = {q.x, q.y, q.z, q.w};
-                    uint32_t hv[4];
+            for (int hh = 0; hh < 16; hh += 8) {
+                const uint4 q = src[hh];
+                const uint32_t qv[4] = {q.x, q.y, q.z, q.w};
+                uint32_t hv[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float lo = bf16_lo_to_f32(qv[e]), hi = bf16_hi_to_f32(qv[e]);
-                        a += lo + hi;
-                        uint32_t pk;
-                        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(pk) : "f"(hi * down), "f"(lo * down));
-                        hv[e] = pk;
-                    }
-                    src[hh] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                for (int e = 0; e < 4; ++e) {
+                    const float lo = bf16_lo_to_f32(qv[e]), hi = bf16_hi_to_f32(qv[e]);
+                    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hv[e]) : "f"(hi * down), "f"(lo * down));
                 }
-                a *= down;
-            }
-            a += __shfl_xor_sync(0xffffffffu, a, 1);
-            a += __shfl_xor_sync(0xffffffffu, a, 2);
-            a += __shfl_xor_sync(0xffffffffu, a, 4);
-            if (pi < pairs && part == 0) {
-                float *e = s_corr + (gi * 4 + (r >> 1)) * 4 + (r & 1);
-                e[0] = -1032.f * a;
-                e[2] = -1152.f * a;
+                src[hh] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
             }
         }
     }
@@ -306,14 +288,14 @@ decode_wk_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
     const int ga = wk_part_start(kp, P, G), gb = wk_part_start(kp + 1, P, G);
     const int n_st = (gb - ga + SG - 1) / SG;
     const uint16_t *xs = s_x + min(g, rows - 1) * L.x_stride + t * 8;
-    const float4 *cs = reinterpret_cast<const float4 *>(s_corr) + t;
     const uint16_t *srow = s_scale + (b * 16 + g) * G;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const unsigned char *wlane = ring + b * kBlockBytes + lane * 16;
     bool alive = true;
     for (int j = 0; j < n_st && alive; ++j) {
         const int slot = kp + P * (j % B);
-        if (!mbar_wait(full0 + 8 * slot, (j / B) & 1, abort_flag, err)) {
+        // Warp-uniform outcome: the MMAs below need every lane.
+        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * slot, (j / B) & 1, abort_flag, err))) {
             alive = false;
             break;
         }
@@ -336,17 +318,18 @@ decode_wk_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         for (int gg = 0; gg < SG; ++gg) {
             if (gg >= ng) break;
             const int gi = g0 + gg;
+            // Exact A operands code - 8 (rows g) and 16 (code - 8) (rows g + 8),
+            // as in decode_kernel.
             uint32_t af[8][4];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
                 const uint32_t w8 = wv[gg][jj] >> 8;
-                af[jj][0] = lop3_and_or(wv[gg][jj], 0x000F000Fu, kMagicF16x2_1024);
-                af[jj][1] = lop3_and_or(wv[gg][jj], 0x00F000F0u, kMagicF16x2_1024);
-                af[jj][2] = lop3_and_or(w8, 0x000F000Fu, kMagicF16x2_1024);
-                af[jj][3] = lop3_and_or(w8, 0x00F000F0u, kMagicF16x2_1024);
+                af[jj][0] = f16x2_sub(lop3_and_or(wv[gg][jj], 0x000F000Fu, kMagicF16x2_1024), kF16x2_1032);
+                af[jj][1] = f16x2_sub(lop3_and_or(wv[gg][jj], 0x00F000F0u, kMagicF16x2_1024), kF16x2_1152);
+                af[jj][2] = f16x2_sub(lop3_and_or(w8, 0x000F000Fu, kMagicF16x2_1024), kF16x2_1032);
+                af[jj][3] = f16x2_sub(lop3_and_or(w8, 0x00F000F0u, kMagicF16x2_1024), kF16x2_1152);
             }
-            const float4 cc = cs[gi * 4];
-            float c[4] = {cc.x, cc.y, cc.z, cc.w};
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k16 = 0; k16 < 4; ++k16) {
                 const uint4 xv = *reinterpret_cast<const uint4 *>(xs + gi * kGroup + 32 * k16);
@@ -382,6 +365,13 @@ decode_wk_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
     for (int q = 1; q < P; ++q) {
         const float4 v = s_red[((q - 1) * B + b) * 32 + lane];
         acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
+    }
+    // A wait of this CTA ran out (every consumer warp has passed the barrier
+    // above, so the flag covers them all): the outputs become NaN, never a
+    // plausible partial result; the error word holds kErrWaitTimeout.
+    if (!alive || *abort_flag) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r] = __int_as_float(0x7fc00000);
     }
     const int f0 = tile * kTileRows + (bb0 + b) * 16 + g;
 #pragma unroll
@@ -489,16 +479,25 @@ int decode_smem_needed(int M, int mt, int groups_per_slice, int sub) {
     return decode_smem_layout(mt, M < 8 * mt ? M : 8 * mt, groups_per_slice, sub).total;
 }
 
+int decode_ring_stages(int M, int mt, int groups_per_slice, int sub) {
+    const int st = decode_smem_layout(mt, M < 8 * mt ? M : 8 * mt, groups_per_slice, sub).stages;
+    return st >= decode_ring_min(groups_per_slice) ? st : 0;
+}
+
 cudaError_t launch_decode(const DecodePlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, bool res, int M, int N, int K,
                           cudaStream_t s, const uint8_t *Z) {
-    if (p.ring != kRing || p.in_flight < 1 || p.in_flight > p.ring) return cudaErrorInvalidValue;
+    if (p.in_flight < 0 || p.in_flight > p.ring || p.wait_us < 0) return cudaErrorInvalidValue;
+    // in_flight == 0 (test-only stall) only together with a short wait limit.
+    if (p.in_flight == 0 && (p.wait_us == 0 || p.wait_us > 100000)) return cudaErrorInvalidValue;
     if (p.batch < 1 || (long long)p.token_blocks * p.batch > 65535) return cudaErrorInvalidValue;
     if (p.sub != 1 && p.sub != 2 && p.sub != 4) return cudaErrorInvalidValue;
     if (p.groups_per_slice < 1 || p.groups_per_slice > kDecodeMaxGps || p.ctas_per_slice < 1 ||
         p.groups_per_slice * p.sub > (p.mt == 1 ? 16 : 8) / (Z ? 2 : 1) ||
         decode_smem_needed(M, p.mt, p.groups_per_slice, p.sub) > kDecodeMaxSmem ||
-        decode_smem_layout(p.mt, M < 8 * p.mt ? M : 8 * p.mt, p.groups_per_slice, p.sub).stages < kRing)
+        decode_smem_layout(p.mt, M < 8 * p.mt ? M : 8 * p.mt, p.groups_per_slice, p.sub).stages !=
+            p.ring ||
+        p.ring < decode_ring_min(p.groups_per_slice))
         return cudaErrorInvalidValue;
     if ((K / kGroup) % p.groups_per_slice != 0) return cudaErrorInvalidValue;
     if (Z) return launch_decode_zp(p, X, Wp, S, Z, Y, ws, res, M, N, K, s);

@@ -16,19 +16,17 @@
 // in shared memory.
 //
 // Each 32-bit word becomes, with one LOP3 per register, the A fragment of an
-// m16n8k16 bf16 mma.sync holding 128 + code (the magic-constant trick of that
-// page's section 1, two codes per register).  The B fragment is 8 tokens of X,
-// so the K reduction across a quad of lanes happens inside the tensor core
-// instead of a shuffle tree.  The constant 128 + 8 = 136 that every weight
-// carries is removed once per 128-wide group instead of once per weight:
-//     sum_k (code_k - 8) x_k = sum_k (128 + code_k) x_k - 136 * sum_k x_k,
-// with the per-group sums of X computed when X is staged; the products are
-// exact in fp32, and the fp32 group scale is applied to the corrected partial
-// sum.  With split-K the fp32 partials go to a [SPLIT_K][M][N] workspace with
-// plain stores and a separate kernel sums the slices in order ("Add Triton
-// BF16xINT4 rowwise GEMM for ROCm gfx942/gfx950", "Split-K without atomics");
-// that kernel is chained with programmatic dependent launch so its launch
-// overlaps this one.
+// m16n8k16 fp16 mma.sync holding 1024 + code (the magic-constant trick of that
+// page's section 1, moved from bf16 to fp16, two codes per register), and one
+// exact fp16x2 subtraction turns it into code - 8.  The B fragment is 8 tokens
+// of X (staged as fp16 with a power-of-two shift per token, exact), so the K
+// reduction across a quad of lanes happens inside the tensor core instead of a
+// shuffle tree; every product is exact in fp32 and the fp32 group scale is
+// applied to each group's sum.  With split-K the fp32 partials go to a
+// [SPLIT_K][M][N] workspace with plain stores and a separate kernel sums the
+// slices in order ("Add Triton BF16xINT4 rowwise GEMM for ROCm gfx942/gfx950",
+// "Split-K without atomics"); that kernel is chained with programmatic
+// dependent launch so its launch overlaps this one.
 #pragma once
 
 #include <atomic>
@@ -43,37 +41,59 @@ namespace {
 
 constexpr int kDecodeWarps = 8;                                 // consumer warps
 constexpr uint32_t kMagicF16x2_1024 = 0x64006400u;              // fp16x2 {1024, 1024}
+constexpr uint32_t kF16x2_1032 = 0x64086408u;                   // fp16x2 {1032, 1032} = 1024 + 8
+constexpr uint32_t kF16x2_1152 = 0x64806480u;                   // fp16x2 {1152, 1152} = 1024 + 16 * 8
+
+// fp16x2 a - b.  Exact wherever it is used here: both operands and the
+// difference are integers of at most 11 significant bits.
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
 constexpr int kDecodeThreads = (kDecodeWarps + 1) * 32;         // + one producer warp
 constexpr int kStageBytes = 2 * kChunkBytes;                    // one 128-wide group of a tile
 constexpr int kDecodeMaxStages = 16;
-constexpr int kRing = 8;   // weight-ring stages in use (every layout holds at least this many)
+constexpr int kRing = 8;   // whole-K kernel: ring slots of one group (kStageBytes) each
 
-// Shared memory: the weight ring first (as many 8 KB stages as the budget
-// leaves, at most kDecodeMaxStages), then its barriers, the abort flag, the
-// per-token maxima, the staged X rows of the token block and the per-group
-// correction table.  Host and kernel size it from the same row count,
-// min(8 * MT, M).
+// Sliced kernel: groups per weight-ring stage.  One bulk copy fills a stage;
+// measured on GB300, a stream of 16 KB copies with three in flight per CTA
+// (two CTAs per SM) reaches 0.94-0.99 of the copy bandwidth where 8 KB
+// copies reach 0.74-0.78, so slices of two or more groups copy two groups
+// at a time.
+__host__ __device__ constexpr int decode_stage_groups(int gps) { return gps >= 2 ? 2 : 1; }
+// Ring stages the sliced kernel uses at most, and needs at least.
+__host__ __device__ constexpr int decode_ring_max(int gps) { return gps >= 2 ? 6 : 8; }
+__host__ __device__ constexpr int decode_ring_min(int gps) { return gps >= 2 ? 4 : 8; }
+
+// Shared memory: the weight ring first (as many stages of
+// decode_stage_groups(gps) groups as the budget leaves, at most
+// decode_ring_max(gps)), then its barriers, the abort flag, the per-token
+// maxima and the staged X rows of the token block.  Host and kernel size it
+// from the same row count, min(8 * MT, M).
 struct DecodeSmem {
     int x_stride;      // 16-bit elements per staged X row: slice + 32 (row stride = 64 B mod 128 B)
-    int stages;
-    int off_ring, off_bar, off_abort, off_xmax, off_x, off_corr, total;
+    int stages;        // ring stages
+    int stage_bytes;   // bytes per ring stage
+    int off_ring, off_bar, off_abort, off_xmax, off_x, total;
 };
 
 // sub: scale groups per 128-wide block (1, 2 or 4 for groups of 128, 64, 32).
 __host__ __device__ inline DecodeSmem decode_smem_layout(int mt, int rows, int gps, int sub = 1) {
     DecodeSmem L;
     L.x_stride = gps * kGroup + 32;
-    const int corr_bytes = gps * sub * mt * 4 * 16;  // one float4 per (scale group, octet, quad)
-    const int rest = 2 * kDecodeMaxStages * 8 + 16 + 64 + rows * L.x_stride * 2 + corr_bytes;
-    int n = (kDecodeMaxSmem - rest) / kStageBytes;
-    L.stages = n > kDecodeMaxStages ? kDecodeMaxStages : n;
+    L.stage_bytes = decode_stage_groups(gps) * kStageBytes;
+    (void)mt;
+    (void)sub;
+    const int rest = 2 * kDecodeMaxStages * 8 + 16 + 64 + rows * L.x_stride * 2;
+    int n = (kDecodeMaxSmem - rest) / L.stage_bytes;
+    L.stages = n > decode_ring_max(gps) ? decode_ring_max(gps) : n;
     L.off_ring = 0;
-    L.off_bar = L.stages * kStageBytes;
+    L.off_bar = L.stages * L.stage_bytes;
     L.off_abort = L.off_bar + 2 * kDecodeMaxStages * 8;
     L.off_xmax = L.off_abort + 16;
     L.off_x = L.off_xmax + 64;
-    L.off_corr = L.off_x + rows * L.x_stride * 2;
-    L.total = L.off_corr + corr_bytes;
+    L.total = L.off_x + rows * L.x_stride * 2;
     return L;
 }
 
@@ -110,14 +130,6 @@ __device__ __forceinline__ void prefetch_tile_scales(const uint16_t *S, int tile
     const uintptr_t lo = (reinterpret_cast<uintptr_t>(S + r0 * n_groups) + 15) & ~uintptr_t(15);
     const uintptr_t hi = reinterpret_cast<uintptr_t>(S + r1 * n_groups) & ~uintptr_t(15);
     if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void *>(lo), uint32_t(hi - lo));
-}
-
-// Wait, ignoring the abort flag, for copies still in flight (used only when
-// aborting, so that no copy lands after the CTA has exited).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-    const unsigned long long t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (global_timer_ns() - t0 > 100000000ull) break;
 }
 
 // One weight row's GPS scales of a slice, as raw bf16 pairs (group 2i in the
@@ -208,8 +220,8 @@ __device__ __forceinline__ ZeroRow<NS> load_zero_row(const uint8_t *p, bool ok, 
 
 // The zero point (low four bits) of scale group i of a row.
 template <int NS>
-__device__ __forceinline__ float zero_of(const ZeroRow<NS> &r, int i) {
-    return float((r.w[i / 4] >> (8 * (i & 3))) & 0xFu);
+__device__ __forceinline__ uint32_t zero_of(const ZeroRow<NS> &r, int i) {
+    return (r.w[i / 4] >> (8 * (i & 3))) & 0xFu;
 }
 
 // Zero points of the rows of weight tile `tile` into L2 (as prefetch_tile_scales).
@@ -232,32 +244,34 @@ __device__ __forceinline__ void prefetch_tile_zeros(const uint8_t *Z, int tile, 
 // half's four nibbles lie inside the 10-bit mantissa, so a 32-bit word gives
 // its four A fragments with one shift and four LOP3s -- 1024 + code for rows
 // g (nibbles at bits 0-3) and 1024 + 16 code for rows g + 8 (bits 4-7) --
-// where bf16's 7-bit mantissa would need three shifts.  Each consumer warp
-// owns one 16-row block of a tile.  Per group it waits for the stage, reads
-// its 16 B of each chunk, builds the 32 A fragments, releases the stage and
-// runs a chain of 8 MMAs whose accumulator starts at -1032 S (rows g) or
-// -1152 S (rows g + 8), S the group's scaled sum of x, so the chain yields
-// sum_k (code_k - 8) x_k, times 16 for rows g + 8.  The group scales, the
-// 1/16 and 2^sh are applied when the tile (or, for 16 tokens, a batch of
-// groups) is done, so the scale loads -- issued a tile ahead -- are off the
-// critical path.
+// where bf16's 7-bit mantissa would need three shifts.  One fp16x2
+// subtraction per fragment then removes the offset exactly: (1024 + code) -
+// 1032 = code - 8 and (1024 + 16 code) - 1152 = 16 (code - 8), small integers
+// that fp16 holds exactly, so every product in the MMA is exact and codes of 8
+// contribute exact zeros.  Each consumer warp owns one 16-row block of a
+// tile.  Per stage it waits, reads its 16 B of each chunk of the stage's
+// groups, releases the stage, and per group builds the 32 A fragments and
+// runs a chain of 8 MMAs from a zero accumulator, which yields
+// sum_k (code_k - 8) x_k, times 16 for rows g + 8; the group's fp32 scale is
+// applied to that sum.  The 1/16 and 2^sh are applied when the tile is done;
+// the scale loads are issued a tile ahead, off the critical path.
 //
-// SUB > 1 (scale groups of 128 / SUB columns): a stage still holds one
-// 128-wide block, whose 32-column quarter q is exactly k16 step q of the
-// chain (both the weight words and the staged X are permuted only inside a
-// quarter), so the chain is cut into SUB chains of 4 / SUB steps, each
-// started from its own scale group's correction and scaled by its own scale.
+// SUB > 1 (scale groups of 128 / SUB columns): a stage's 128-wide block has
+// 32-column quarters q that are exactly k16 step q of the chain (both the
+// weight words and the staged X are permuted only inside a quarter), so the
+// chain is cut into SUB chains of 4 / SUB steps, each scaled by its own
+// scale group's scale.
 //
-// kZp (zero-point variant, Z = uint8 zero points [N][K/G]): the correction
-// table holds the plain scaled sums S and a chain starts from -(1024 + z) S
-// (rows g) or -(1024 + 16 z) S (rows g + 8), z the row's zero point of the
-// chain's scale group, so it yields sum_k (code_k - z) x_k (times 16).
+// kZp (zero-point variant, Z = uint8 zero points [N][K/G]): the subtracted
+// offsets are 1024 + z (rows g) and 1024 + 16 z (rows g + 8), z the row's zero
+// point of the chain's scale group, so the chain yields sum_k (code_k - z) x_k
+// (times 16), again with exact products.
 // decode_kernel and decode_zp_kernel below are the entry points.
 template <int MT, int GPS, bool kSplit, int SUB, bool kZp>
 __device__ __forceinline__ void
 decode_body(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
             const uint16_t *__restrict__ S, const uint8_t *__restrict__ Z, uint16_t *__restrict__ Y,
-            float *__restrict__ ws, int M, int N, int K, int n_tiles, int ring_stages, int in_flight,
+            float *__restrict__ ws, int M, int N, int K, int n_tiles, int wait_us, int in_flight,
             int s_vec, int z_vec, int resident, int token_blocks, int *err) {
     extern __shared__ __align__(128) unsigned char smem[];
     // Batched products: grid.z = entries x token blocks; entry b's X, W,
@@ -285,17 +299,20 @@ decode_body(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
     const int KC = K / kChunkK;
     const int rows_alloc = min(8 * MT, M);
     const DecodeSmem L = decode_smem_layout(MT, rows_alloc, GPS, SUB);
-    constexpr int NS = kRing;
-    (void)ring_stages;
+    constexpr int SG = decode_stage_groups(GPS);     // groups per ring stage
+    constexpr int SPT = GPS / SG;                    // stages per tile of the slice
+    constexpr int kStage = SG * kStageBytes;         // bytes per stage (one bulk copy)
+    const int NS = L.stages;                         // ring stages (the host checks the minimum)
     // A window deeper than the ring would wait on a slot's next phase before
-    // issuing it: keep it within the ring.
+    // issuing it: keep it within the ring.  in_flight == 0 (test only): no
+    // copies at all, so every consumer wait runs out after wait_us.
     const int IF = min(in_flight, NS);
+    const unsigned long long wait_ns = wait_us > 0 ? 1000ull * unsigned(wait_us) : kWaitLimitNs;
     unsigned char *ring = smem + L.off_ring;
     const uint32_t full0 = smem_u32(smem + L.off_bar);
     const uint32_t empty0 = full0 + 8 * kDecodeMaxStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_abort);
     uint16_t *s_x = reinterpret_cast<uint16_t *>(smem + L.off_x);
-    float *s_corr = reinterpret_cast<float *>(smem + L.off_corr);
     int *s_xmax = reinterpret_cast<int *>(smem + L.off_xmax);
 
     // Let the next kernel in the stream be scheduled while this grid runs.
@@ -317,9 +334,9 @@ decode_body(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         if (!resident) {
             const uint8_t *src = Wp + (size_t(c0) * KC + size_t(2 * grp0)) * kChunkBytes;
             const size_t tile_step = size_t(C) * KC * kChunkBytes;
-            const int first = min(n_my * GPS, NS);
+            const int first = min(n_my * SPT, NS);
             for (int q = 0; q < first; ++q)
-                bulk_prefetch_l2(src + (q / GPS) * tile_step + (q % GPS) * kStageBytes, kStageBytes);
+                bulk_prefetch_l2(src + (q / SPT) * tile_step + (q % SPT) * kStage, kStage);
         }
         // The scales of the first tiles (the consumers load a tile's scales
         // two tiles ahead of its use).
@@ -369,26 +386,25 @@ decode_body(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
             // At most IF copies are in the air at once (the ring may
             // hold more that have landed): a small burst per CTA lets the
             // first stages land early instead of all of them near the end.
-            const int total = n_my * GPS;
-            int issued = 0, st = 0, gi = 0, lst = 0;
+            const int total = IF > 0 ? n_my * SPT : 0;     // stages
+            int issued = 0, st = 0, gs = 0, lst = 0;
             uint32_t epar = 1;   // parity of the empty phase to wait for (first lap: none)
             uint32_t lpar = 0;   // parity of the full phase of copy q - IF
             for (int q = 0; q < total; ++q) {
-                if (q >= NS && !mbar_wait(empty0 + 8 * st, epar, abort_flag, err)) break;
+                if (q >= NS && !mbar_wait(empty0 + 8 * st, epar, abort_flag, err, wait_ns)) break;
                 if (q >= IF) {
-                    if (!mbar_wait(full0 + 8 * lst, lpar, abort_flag, err)) break;
+                    if (!mbar_wait(full0 + 8 * lst, lpar, abort_flag, err, wait_ns)) break;
                     if (++lst == NS) { lst = 0; lpar ^= 1; }
                 }
-                mbar_arrive_expect_tx(full0 + 8 * st, kStageBytes);
-                bulk_g2s(smem_u32(ring + st * kStageBytes), src + gi * kStageBytes, kStageBytes,
-                         full0 + 8 * st);
+                mbar_arrive_expect_tx(full0 + 8 * st, kStage);
+                bulk_g2s(smem_u32(ring + st * kStage), src + gs * kStage, kStage, full0 + 8 * st);
                 ++issued;
-                if (++gi == GPS) {
-                    gi = 0;
+                if (++gs == SPT) {
+                    gs = 0;
                     src += tile_step;
-                    // Entering tile q / GPS: warm L2 with the scales of tile
-                    // q / GPS + 3, which the consumers load about two tiles later.
-                    const int ahead = (q + 1) / GPS + 3;
+                    // Entering tile (q + 1) / SPT: warm L2 with the scales of the
+                    // tile three ahead, which the consumers load about two tiles later.
+                    const int ahead = (q + 1) / SPT + 3;
                     if (ahead < n_my) {
                         prefetch_tile_scales(S, c0 + ahead * C, N, n_sg);
                         if (kZp) prefetch_tile_zeros(Z, c0 + ahead * C, N, n_sg);
@@ -463,80 +479,38 @@ decode_body(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
     if (n_my > 1) load_scales(c0 + C, s_next, z_next);
     consumer_bar();
     {
-        // Per (token, group): 8 lanes take 16 values each, convert them in
-        // place to fp16 x * 2^-sh, and sum them (fp32, then a shuffle
-        // reduction) for the correction table: token r, group gi ->
-        // s_corr[(gi * MT + r / 8) * 4 + (r % 8) / 2] = {-1032 S(r), -1032 S(r^1),
-        // -1152 S(r), -1152 S(r^1)} (pairs of tokens 2t, 2t + 1), S the scaled sum.
-        // With SUB scale groups per block the table has an entry per scale
-        // group (gi * SUB + j in place of gi): a lane's piece `part` lies in
-        // the block's first half, piece 8 + part in the second, so their sums
-        // are kept apart (a, b) and reduced over the lanes of one scale group.
-        const int pairs = rows * GPS;       // entries of absent tokens stay unwritten
+        // Per (token, group): 8 lanes take 16 values each and convert them in
+        // place to fp16 x * 2^-sh.
+        const int pairs = rows * GPS;
         const int part = threadIdx.x & 7;
-        for (int base = 0; base < pairs; base += kDecodeWarps * 32 / 8) {
-            const int pi = base + (threadIdx.x >> 3);
+        for (int pi = threadIdx.x >> 3; pi < pairs; pi += kDecodeWarps * 32 / 8) {
             const int r = pi / GPS, gi = pi - r * GPS;
-            float a = 0.f, b = 0.f;   // SUB == 1: both pieces go to a
-            if (pi < pairs) {
-                const float down = pow2f(-slice_shift(s_xmax[r]));
-                // Lane `part` takes 8-element pieces part and 8 + part, so each
-                // access of 8 lanes covers 128 contiguous bytes.
-                uint4 *src = reinterpret_cast<uint4 *>(s_x + r * L.x_stride + gi * kGroup) + part;
+            const float down = pow2f(-slice_shift(s_xmax[r]));
+            // Lane `part` takes 8-element pieces part and 8 + part, so each
+            // access of 8 lanes covers 128 contiguous bytes.
+            uint4 *src = reinterpret_cast<uint4 *>(s_x + r * L.x_stride + gi * kGroup) + part;
 #pragma unroll
-                for (int h = 0; h < 16; h += 8) {
-                    const uint4 q = src[h];
-                    const uint32_t qv[4] = {q.x, q.y, q.z, q.w};
-                    uint32_t hv[4];
+            for (int h = 0; h < 16; h += 8) {
+                const uint4 q = src[h];
+                const uint32_t qv[4] = {q.x, q.y, q.z, q.w};
+                uint32_t hv[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float lo = bf16_lo_to_f32(qv[e]), hi = bf16_hi_to_f32(qv[e]);
-                        if (SUB == 1 || h == 0) a += lo + hi;
-                        else b += lo + hi;
-                        uint32_t pk;
-                        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(pk) : "f"(hi * down), "f"(lo * down));
-                        hv[e] = pk;
-                    }
-                    src[h] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                for (int e = 0; e < 4; ++e) {
+                    const float lo = bf16_lo_to_f32(qv[e]), hi = bf16_hi_to_f32(qv[e]);
+                    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hv[e]) : "f"(hi * down), "f"(lo * down));
                 }
-                a *= down;
-                b *= down;
-            }
-            a += __shfl_xor_sync(0xffffffffu, a, 1);
-            a += __shfl_xor_sync(0xffffffffu, a, 2);
-            if (SUB < 4) a += __shfl_xor_sync(0xffffffffu, a, 4);
-            if (SUB > 1) {
-                b += __shfl_xor_sync(0xffffffffu, b, 1);
-                b += __shfl_xor_sync(0xffffffffu, b, 2);
-                if (SUB < 4) b += __shfl_xor_sync(0xffffffffu, b, 4);
-            }
-            // SUB == 4: parts 0-3 and 4-7 cover different quarters.
-            if (pi < pairs && (part & (SUB == 4 ? 3 : 7)) == 0) {
-                const int ga = gi * SUB + (SUB == 4 ? (part >> 2) : 0);
-                // (kZp: the plain sums; the chains apply their rows' offsets)
-                const float ka = kZp ? 1.f : -1032.f, kb = kZp ? 1.f : -1152.f;
-                float *e = s_corr + ((ga * MT + (r >> 3)) * 4 + ((r & 7) >> 1)) * 4 + (r & 1);
-                e[0] = ka * a;
-                e[2] = kb * a;
-                if (SUB > 1) {
-                    const int gb = ga + SUB / 2;
-                    float *f = s_corr + ((gb * MT + (r >> 3)) * 4 + ((r & 7) >> 1)) * 4 + (r & 1);
-                    f[0] = ka * b;
-                    f[2] = kb * b;
-                }
+                src[h] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
             }
         }
     }
     consumer_bar();
 
-    // Fragment sources: X rows 8o + g (B), correction for tokens 8o + 2t, +1 (C).
-    // Lanes of rows past the staged ones read the last staged row instead
-    // (their tokens' columns are never stored).
+    // Fragment sources: X rows 8o + g (B).  Lanes of rows past the staged ones
+    // read the last staged row instead (their tokens' columns are never stored).
     const uint16_t *xs = s_x + t * 8;
     int xrow[MT];
 #pragma unroll
     for (int o = 0; o < MT; ++o) xrow[o] = min(8 * o + g, rows_alloc - 1) * L.x_stride;
-    const float4 *cs = reinterpret_cast<const float4 *>(s_corr) + t;
     // Per-token factors of this lane's C columns (tokens 8o + 2t + e): undo the
     // slice shift, and for rows g + 8 (whose codes carry weight 16) also 1/16.
     float fac[MT][2], fac16[MT][2];
@@ -550,84 +524,9 @@ decode_body(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         }
 
     const unsigned char *wlane = ring + warp * kBlockBytes + lane * 16;
-    for (int it = 0; it < n_my; ++it) {
-        float acc[MT][4];
-#pragma unroll
-        for (int o = 0; o < MT; ++o)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) acc[o][r] = 0.f;
-#pragma unroll
-        for (int gi = 0; gi < GPS; ++gi) {
-            // Stage q of this CTA's stream sits in ring slot q % kRing (a
-            // power of two, so with the loop unrolled the slot and its phase
-            // parity cost at most a shift and a mask per tile).
-            const uint32_t q = uint32_t(it) * GPS + gi;
-            const uint32_t slot = q % kRing;
-            if (!mbar_wait(full0 + 8 * slot, (q / kRing) & 1u, abort_flag, err)) return;
-            const unsigned char *wsrc = wlane + slot * kStageBytes;
-            const uint4 wa = *reinterpret_cast<const uint4 *>(wsrc);
-            const uint4 wb = *reinterpret_cast<const uint4 *>(wsrc + kChunkBytes);
-            const uint32_t wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-            // fp16 A fragments: rows g hold 1024 + code (nibble in mantissa
-            // bits 0-3), rows g + 8 hold 1024 + 16 code (bits 4-7), so one
-            // shift per word serves both halves of the upper byte pair.
-            uint32_t af[8][4];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t w8 = wv[j] >> 8;
-                af[j][0] = lop3_and_or(wv[j], 0x000F000Fu, kMagicF16x2_1024);
-                af[j][1] = lop3_and_or(wv[j], 0x00F000F0u, kMagicF16x2_1024);
-                af[j][2] = lop3_and_or(w8, 0x000F000Fu, kMagicF16x2_1024);
-                af[j][3] = lop3_and_or(w8, 0x00F000F0u, kMagicF16x2_1024);
-            }
-            // The stage's bytes are now in registers: release it.
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-#pragma unroll
-            for (int j = 0; j < SUB; ++j) {
-                // Scales of rows g (C elements 0, 1) and g + 8 (2, 3) for
-                // scale group gi * SUB + j, loaded a tile ahead.
-                const float s0 = scale_of<NSC>(s_cur[0], gi * SUB + j);
-                const float s1 = scale_of<NSC>(s_cur[1], gi * SUB + j);
-                float kz0 = 0.f, kz1 = 0.f;
-                if constexpr (kZp) {
-                    kz0 = -1024.f - zero_of<NSC>(z_cur[0], gi * SUB + j);
-                    kz1 = fmaf(-16.f, zero_of<NSC>(z_cur[1], gi * SUB + j), -1024.f);
-                }
-#pragma unroll
-                for (int o = 0; o < MT; ++o) {
-                    const float4 cc = cs[((gi * SUB + j) * MT + o) * 4];
-                    float c[4] = {cc.x, cc.y, cc.z, cc.w};
-                    if constexpr (kZp) {
-                        c[0] *= kz0;
-                        c[1] *= kz0;
-                        c[2] *= kz1;
-                        c[3] *= kz1;
-                    }
-#pragma unroll
-                    for (int k16 = j * (4 / SUB); k16 < (j + 1) * (4 / SUB); ++k16) {
-                        // Lanes of absent tokens read the last staged row (xrow is
-                        // clamped): those values reach only absent tokens' output
-                        // columns, which are never stored.
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(xs + xrow[o] + gi * kGroup + 32 * k16);
-                        mma_16816_f16_acc(c, af[2 * k16], xv.x, xv.y);
-                        mma_16816_f16_acc(c, af[2 * k16 + 1], xv.z, xv.w);
-                    }
-                    acc[o][0] = fmaf(s0, c[0], acc[o][0]);
-                    acc[o][1] = fmaf(s0, c[1], acc[o][1]);
-                    acc[o][2] = fmaf(s1, c[2], acc[o][2]);
-                    acc[o][3] = fmaf(s1, c[3], acc[o][3]);
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 0; o < MT; ++o) {
-            acc[o][0] *= fac[o][0];
-            acc[o][1] *= fac[o][1];
-            acc[o][2] *= fac16[o][0];
-            acc[o][3] *= fac16[o][1];
-        }
-        // C fragment: {row g: tokens 2t, 2t+1}, {row g+8: tokens 2t, 2t+1}.
+    // This warp's outputs of tile `it` (C fragment: {row g: tokens 2t, 2t+1},
+    // {row g+8: tokens 2t, 2t+1}) to Y, or to this slice of the workspace.
+    auto store_tile = [&](int it, const float (&v)[MT][4]) {
         const int f0 = (c0 + it * C) * kTileRows + warp * 16 + g;
 #pragma unroll
         for (int o = 0; o < MT; ++o) {
@@ -639,12 +538,126 @@ decode_body(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
                 if (m < M && f < N) {
                     const size_t off = size_t(m) * N + f;
                     if (kSplit)
-                        ws[(size_t(blockIdx.y) * n_entries + bz) * size_t(M) * N + off] = acc[o][r];
+                        ws[(size_t(blockIdx.y) * n_entries + bz) * size_t(M) * N + off] = v[o][r];
                     else
-                        Y[off] = f32_to_bf16_rn(acc[o][r]);
+                        Y[off] = f32_to_bf16_rn(v[o][r]);
                 }
             }
         }
+    };
+    int failed_at = -1;   // first tile this warp could not complete (a wait ran out)
+    int slot = 0;         // ring stage of the next wait, and its phase parity
+    uint32_t phase = 0;
+    for (int it = 0; it < n_my; ++it) {
+        float acc[MT][4];
+#pragma unroll
+        for (int o = 0; o < MT; ++o)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[o][r] = 0.f;
+#pragma unroll
+        for (int gs = 0; gs < GPS; gs += SG) {
+            // Warp-uniform outcome: the MMAs below need every lane.
+            if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * slot, phase, abort_flag, err, wait_ns))) {
+                failed_at = it;
+                break;
+            }
+            // This lane's 16 B of both chunks of each of the stage's groups.
+            const unsigned char *wsrc = wlane + slot * kStage;
+            uint32_t wvs[SG][8];
+#pragma unroll
+            for (int gg = 0; gg < SG; ++gg) {
+                const uint4 wa = *reinterpret_cast<const uint4 *>(wsrc + gg * kStageBytes);
+                const uint4 wb = *reinterpret_cast<const uint4 *>(wsrc + gg * kStageBytes + kChunkBytes);
+                wvs[gg][0] = wa.x; wvs[gg][1] = wa.y; wvs[gg][2] = wa.z; wvs[gg][3] = wa.w;
+                wvs[gg][4] = wb.x; wvs[gg][5] = wb.y; wvs[gg][6] = wb.z; wvs[gg][7] = wb.w;
+            }
+            // The stage's bytes are now in registers: release it.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+            if (++slot == NS) {
+                slot = 0;
+                phase ^= 1u;
+            }
+            // The stage's SG groups as SG independent MMA chains, interleaved
+            // k16 step by k16 step (the groups' fragments are built just
+            // before their MMAs): the chains' latencies overlap.  A chain
+            // restarts from zero at each scale group and is added to the
+            // accumulator times that group's scale.
+            float c[SG][MT][4];
+#pragma unroll
+            for (int gg = 0; gg < SG; ++gg)
+#pragma unroll
+                for (int o = 0; o < MT; ++o)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) c[gg][o][r] = 0.f;
+#pragma unroll
+            for (int k16 = 0; k16 < 4; ++k16) {
+                constexpr int kSteps = 4 / SUB;           // k16 steps per scale group
+                const int j = k16 / kSteps;                // scale group within the block
+#pragma unroll
+                for (int gg = 0; gg < SG; ++gg) {
+                    const int gi = gs + gg;
+                    // Offsets of rows g and g + 8 as fp16x2 pairs.
+                    uint32_t off0 = kF16x2_1032, off1 = kF16x2_1152;
+                    if constexpr (kZp) {
+                        off0 = (0x6400u | zero_of<NSC>(z_cur[0], gi * SUB + j)) * 0x10001u;
+                        off1 = (0x6400u | (zero_of<NSC>(z_cur[1], gi * SUB + j) << 4)) * 0x10001u;
+                    }
+                    // fp16 A fragments of words 2 k16 and 2 k16 + 1: rows g hold
+                    // 1024 + code (nibble in mantissa bits 0-3), rows g + 8 hold
+                    // 1024 + 16 code (bits 4-7), so one shift per word serves
+                    // both halves of the upper byte pair; the exact subtraction
+                    // leaves code - 8 (16 (code - 8) for rows g + 8).
+                    uint32_t af[2][4];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t w = wvs[gg][2 * k16 + h];
+                        const uint32_t w8 = w >> 8;
+                        af[h][0] = f16x2_sub(lop3_and_or(w, 0x000F000Fu, kMagicF16x2_1024), off0);
+                        af[h][1] = f16x2_sub(lop3_and_or(w, 0x00F000F0u, kMagicF16x2_1024), off1);
+                        af[h][2] = f16x2_sub(lop3_and_or(w8, 0x000F000Fu, kMagicF16x2_1024), off0);
+                        af[h][3] = f16x2_sub(lop3_and_or(w8, 0x00F000F0u, kMagicF16x2_1024), off1);
+                    }
+#pragma unroll
+                    for (int o = 0; o < MT; ++o) {
+                        // Lanes of absent tokens read the last staged row (xrow is
+                        // clamped): those values reach only absent tokens' output
+                        // columns, which are never stored.
+                        const uint4 xv = *reinterpret_cast<const uint4 *>(xs + xrow[o] + gi * kGroup + 32 * k16);
+                        mma_16816_f16_acc(c[gg][o], af[0], xv.x, xv.y);
+                        mma_16816_f16_acc(c[gg][o], af[1], xv.z, xv.w);
+                    }
+                }
+                if ((k16 + 1) % kSteps == 0) {
+                    // End of scale group j: scale each chain (rows g: C elements
+                    // 0, 1; rows g + 8: 2, 3; scales loaded a tile ahead).
+#pragma unroll
+                    for (int gg = 0; gg < SG; ++gg) {
+                        const int gi = gs + gg;
+                        const float s0 = scale_of<NSC>(s_cur[0], gi * SUB + j);
+                        const float s1 = scale_of<NSC>(s_cur[1], gi * SUB + j);
+#pragma unroll
+                        for (int o = 0; o < MT; ++o) {
+                            acc[o][0] = fmaf(s0, c[gg][o][0], acc[o][0]);
+                            acc[o][1] = fmaf(s0, c[gg][o][1], acc[o][1]);
+                            acc[o][2] = fmaf(s1, c[gg][o][2], acc[o][2]);
+                            acc[o][3] = fmaf(s1, c[gg][o][3], acc[o][3]);
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) c[gg][o][r] = 0.f;
+                        }
+                    }
+                }
+            }
+        }
+        if (failed_at >= 0) break;
+#pragma unroll
+        for (int o = 0; o < MT; ++o) {
+            acc[o][0] *= fac[o][0];
+            acc[o][1] *= fac[o][1];
+            acc[o][2] *= fac16[o][0];
+            acc[o][3] *= fac16[o][1];
+        }
+        store_tile(it, acc);
         s_cur[0] = s_next[0];
         s_cur[1] = s_next[1];
         if (kZp) {
@@ -653,15 +666,26 @@ decode_body(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
         }
         if (it + 2 < n_my) load_scales(c0 + (it + 2) * C, s_next, z_next);
     }
+    if (failed_at >= 0) {
+        // The CTA is aborting: this warp's remaining outputs become NaN, so
+        // the result of an incomplete call is never a plausible number (the
+        // error word holds kErrWaitTimeout).
+        float nan4[MT][4];
+#pragma unroll
+        for (int o = 0; o < MT; ++o)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) nan4[o][r] = __int_as_float(0x7fc00000);
+        for (int it = failed_at; it < n_my; ++it) store_tile(it, nan4);
+    }
 }
 
 template <int MT, int GPS, bool kSplit, int SUB>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 decode_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
               const uint16_t *__restrict__ S, uint16_t *__restrict__ Y, float *__restrict__ ws,
-              int M, int N, int K, int n_tiles, int ring_stages, int in_flight, int s_vec,
+              int M, int N, int K, int n_tiles, int wait_us, int in_flight, int s_vec,
               int resident, int token_blocks, int *err) {
-    decode_body<MT, GPS, kSplit, SUB, false>(X, Wp, S, nullptr, Y, ws, M, N, K, n_tiles, ring_stages,
+    decode_body<MT, GPS, kSplit, SUB, false>(X, Wp, S, nullptr, Y, ws, M, N, K, n_tiles, wait_us,
                                              in_flight, s_vec, 0, resident, token_blocks, err);
 }
 
@@ -670,9 +694,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 decode_zp_kernel(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
                  const uint16_t *__restrict__ S, const uint8_t *__restrict__ Z,
                  uint16_t *__restrict__ Y, float *__restrict__ ws, int M, int N, int K, int n_tiles,
-                 int ring_stages, int in_flight, int s_vec, int z_vec, int resident, int token_blocks,
+                 int wait_us, int in_flight, int s_vec, int z_vec, int resident, int token_blocks,
                  int *err) {
-    decode_body<MT, GPS, kSplit, SUB, true>(X, Wp, S, Z, Y, ws, M, N, K, n_tiles, ring_stages,
+    decode_body<MT, GPS, kSplit, SUB, true>(X, Wp, S, Z, Y, ws, M, N, K, n_tiles, wait_us,
                                             in_flight, s_vec, z_vec, resident, token_blocks, err);
 }
 
@@ -717,10 +741,10 @@ cudaError_t launch_decode_t(const DecodePlan &p, const uint16_t *X, const uint8_
     const int s_vec = (reinterpret_cast<uintptr_t>(S) % (2 * GPS * SUB)) == 0;
     if constexpr (kZp) {
         const int z_vec = (reinterpret_cast<uintptr_t>(Z) % (GPS * SUB)) == 0;
-        return cudaLaunchKernelEx(&cfg, kern, X, Wp, S, Z, Y, ws, M, N, K, p.n_tiles, p.ring,
+        return cudaLaunchKernelEx(&cfg, kern, X, Wp, S, Z, Y, ws, M, N, K, p.n_tiles, p.wait_us,
                                   p.in_flight, s_vec, z_vec, int(resident), p.token_blocks, err);
     } else {
-        return cudaLaunchKernelEx(&cfg, kern, X, Wp, S, Y, ws, M, N, K, p.n_tiles, p.ring,
+        return cudaLaunchKernelEx(&cfg, kern, X, Wp, S, Y, ws, M, N, K, p.n_tiles, p.wait_us,
                                   p.in_flight, s_vec, int(resident), p.token_blocks, err);
     }
 }

@@ -3,10 +3,12 @@
 // Kernels that can detect a broken pipeline (a bounded wait that timed out)
 // record it by OR-ing bits into one int in device memory instead of trapping.
 // The word is a file-scope __device__ variable; its device address is looked
-// up once per device with cudaGetSymbolAddress and passed to the kernels.
+// up once per device with cudaGetSymbolAddress and passed to the kernels, and
+// w4a16_read_error_word copies it back to the host.
 #include <atomic>
 #include <cuda_runtime.h>
 
+#include "w4a16.h"
 #include "internal.h"
 
 namespace w4a16 {
@@ -33,3 +35,19 @@ int *device_error_word() {
 }
 
 }  // namespace w4a16
+
+extern "C" w4a16_status w4a16_read_error_word(int *out, int clear) {
+    if (!out) return W4A16_ERR_INVALID_ARG;
+    // Every kernel that may still set a bit has finished once the device is
+    // idle; the copies below are synchronous.
+    if (cudaDeviceSynchronize() != cudaSuccess) return W4A16_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, w4a16::g_error_word, sizeof v) != cudaSuccess) return W4A16_ERR_CUDA;
+    if (clear) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(w4a16::g_error_word, &zero, sizeof zero) != cudaSuccess)
+            return W4A16_ERR_CUDA;
+    }
+    *out = v;
+    return W4A16_OK;
+}

@@ -14,8 +14,10 @@ struct DecodePlan {
     int ctas_per_slice;   // grid.x: CTA c of a slice takes tiles c, c + ctas_per_slice, ...
     int split_k;          // K slices (grid.y)
     int groups_per_slice; // 128-wide K groups per slice (<= kDecodeMaxGps)
-    int ring;             // weight-ring stages to use (capped by shared memory)
-    int in_flight;        // bulk copies a CTA keeps in the air (<= ring)
+    int ring;             // weight-ring stages (decode_ring_stages: from the shared-memory layout)
+    int in_flight;        // bulk copies a CTA keeps in the air (<= ring); 0 only in the
+                          // test-only stall mode (no copies: every wait runs out)
+    int wait_us;          // bounded-wait limit in microseconds (0: the default 2 s)
     int wk_blocks;        // > 0: whole-K kernel, each CTA owns this many 16-row blocks over all
                           // of K (split_k is 1, ctas_per_slice the grid); 0: the slice kernel
     int batch;            // independent products of this shape (batched op; 1 otherwise)
@@ -47,6 +49,8 @@ int *device_error_word();        // device address of the error word (nullptr on
 constexpr int kDecodeMaxGps = 16;
 constexpr int kDecodeMaxSmem = 113 * 1024;
 int decode_smem_needed(int M, int mt, int groups_per_slice, int sub);
+// Ring stages of the sliced kernel for a plan (0: the layout does not fit).
+int decode_ring_stages(int M, int mt, int groups_per_slice, int sub);
 // Whole-K decode kernel: whether M tokens of K fit its staging, and its launch.
 bool decode_wk_fits(int M, int K, int blocks_per_cta);
 cudaError_t launch_decode_wk(int blocks_per_cta, int ctas, int batch, const uint16_t *X, const uint8_t *Wp,

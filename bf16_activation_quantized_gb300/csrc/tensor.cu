@@ -276,12 +276,6 @@ __device__ __forceinline__ uint32_t scale_pair_of(const ScaleRaw<kSub> &r, int i
     return __byte_perm(r.w[i / 2], 0, (i & 1) ? 0x3232 : 0x1010);
 }
 
-__device__ __forceinline__ void drain_wait_tc(uint32_t bar, uint32_t parity) {
-    const unsigned long long t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (global_timer_ns() - t0 > 100000000ull) break;
-}
-
 __device__ __forceinline__ void tc_st_16x256b_x8(uint32_t taddr, const uint32_t (&v)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], "
@@ -496,7 +490,7 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                     t_progress = global_timer_ns();
                 } else {
                     if (*abort_flag) break;
-                    if (global_timer_ns() - t_progress > kWaitLimitNs) {
+                    if (elapsed_beyond(&t_progress, kWaitLimitNs)) {
                         *abort_flag = 1;
                         atomicOr(a.err, kErrWaitTimeout);
                         break;
@@ -504,8 +498,8 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                 }
             }
             if (*abort_flag) {
-                for (int u = xq > SX ? xq - SX : 0; u < xq; ++u) drain_wait_tc(xfull_bar(u % SX), (u / SX) & 1);
-                for (int u = wq > SW ? wq - SW : 0; u < wq; ++u) drain_wait_tc(wfull_bar(u % SW), (u / SW) & 1);
+                for (int u = xq > SX ? xq - SX : 0; u < xq; ++u) drain_wait(xfull_bar(u % SX), (u / SX) & 1);
+                for (int u = wq > SW ? wq - SW : 0; u < wq; ++u) drain_wait(wfull_bar(u % SW), (u / SW) & 1);
             }
         }
     } else if (warp == kTcMmaWarp) {
@@ -552,7 +546,7 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
             }
             // Every MMA this thread issued has completed before TMEM is freed.
             tc_commit(done_bar);
-            drain_wait_tc(done_bar, 0);
+            drain_wait(done_bar, 0);
         }
     } else if (warp < kTcDequantWarps) {
         // Dequantisers (and, without a separate epilogue, the epilogue).
@@ -634,7 +628,11 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                     }
                     have_next = true;
                 }
-                if (!mbar_wait(wfull_bar(st), wph, abort_flag, a.err)) { ok = false; break; }
+                // Warp-uniform outcomes below: tcgen05.st needs every lane.
+                if (!__all_sync(0xffffffffu, mbar_wait(wfull_bar(st), wph, abort_flag, a.err))) {
+                    ok = false;
+                    break;
+                }
                 const unsigned char *wsrc = smem + L.off_w + st * kGroupBytes + block * kBlockBytes + lane * 16;
                 const uint4 wa = *reinterpret_cast<const uint4 *>(wsrc);
                 const uint4 wb = *reinterpret_cast<const uint4 *>(wsrc + kChunkBytes);
@@ -679,7 +677,7 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                 }
                 if (++st == S) { st = 0; wph ^= 1; }
                 flush();
-                if (qa >= SA && !mbar_wait(aempty_bar(sa), eph, abort_flag, a.err)) {
+                if (qa >= SA && !__all_sync(0xffffffffu, mbar_wait(aempty_bar(sa), eph, abort_flag, a.err))) {
                     ok = false;
                     break;
                 }
@@ -695,7 +693,7 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
             if (kSep) continue;
             // Epilogue: warp (sub, half) reads lanes 32 sub .. 32 sub + 31 (its
             // weight rows) for every other 32-token column block.
-            if (!mbar_wait(dfull_bar(0), tiles & 1, abort_flag, a.err)) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(dfull_bar(0), tiles & 1, abort_flag, a.err))) break;
             tc_fence_after();
             const int fb = ti.ft * kTileRows + 32 * sub;           // first weight row of the warp
             for (int cb = half; cb * 32 < a.bt; cb += 2) {
@@ -719,7 +717,7 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
         TileInfo ti;
         for (int id = blockIdx.x; tc_tile<kBatched>(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
             const int db = tiles & 1;
-            if (!mbar_wait(dfull_bar(db), (tiles >> 1) & 1, abort_flag, a.err)) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(dfull_bar(db), (tiles >> 1) & 1, abort_flag, a.err))) break;
             tc_fence_after();
             const int fb = ti.ft * kTileRows + 32 * sub;
             for (int cb = 0; cb * 32 < a.bt; ++cb) {
@@ -741,6 +739,22 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
     __syncthreads();
     tc_fence_after();
     if (warp == kTcMmaWarp) tc_dealloc(tmem_base, uint32_t(a.tmem_cols));
+    if (*abort_flag && warp < kTcDequantWarps) {
+        // A wait ran out (the error word holds kErrWaitTimeout): every output
+        // of this CTA's tiles becomes NaN, so an incomplete result is never a
+        // plausible number.
+        TileInfo ti;
+        for (int id = blockIdx.x; tc_tile<kBatched>(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
+            for (int e = threadIdx.x; e < ti.rows * kTileRows; e += kTcDequantWarps * 32) {
+                const int m = ti.x_row0 + e / kTileRows;
+                const int f = ti.ft * kTileRows + e % kTileRows;
+                if (f >= a.N) continue;
+                const size_t off = size_t(m) * a.N + f;
+                if (kSplit) a.ws[size_t(ti.slice) * a.M_total * a.N + off] = __int_as_float(0x7fc00000);
+                else a.Y[off] = uint16_t(0x7fc0);
+            }
+        }
+    }
 }
 
 template <bool kSplit, bool kSep, bool kBatched, int kSub>

@@ -21,7 +21,9 @@
  *    16-bit patterns (w4a16_bf16).
  *  - The library never allocates, frees or synchronises, and never copies
  *    between host and device inside a call; kernels are enqueued on `stream`
- *    and the call returns.  No entry point reads the environment.
+ *    and the call returns.  (The one exception is the checking call
+ *    w4a16_read_error_word, which is not on the GEMM's path.)  No entry point
+ *    reads the environment.
  *  - Arguments are validated on the host before anything is enqueued; a
  *    failed check returns an error status and launches nothing.  A launch
  *    failure returns W4A16_ERR_CUDA.  Kernels never trap.
@@ -86,7 +88,24 @@ enum {
     /* Plan for the zero-point variant (w4a16_plan / w4a16_workspace_bytes
      * queries; w4a16_gemm_zp sets it itself).  Passing it to any other call
      * is W4A16_ERR_INVALID_ARG. */
-    W4A16_FLAG_ZERO_POINTS = 8
+    W4A16_FLAG_ZERO_POINTS = 8,
+    /* Test only: exercises the failure path without faulting the GPU.  The
+     * decode arm's K-slice kernel is launched with no weight copies and with
+     * its bounded waits cut from 2 s to 1 ms, so every CTA gives up: the call
+     * returns W4A16_OK (the launch itself succeeds), every output it owns
+     * (Y, or the split-K workspace and through the reduce Y) becomes NaN, and
+     * the device error word gets W4A16_ERROR_WAIT_TIMEOUT.  With the tensor
+     * arm or the whole-K kernel the call returns W4A16_ERR_UNSUPPORTED. */
+    W4A16_FLAG_TEST_STALL = 16
+};
+
+/* Bits of the device error word (w4a16_read_error_word). */
+enum {
+    /* A bounded wait inside a kernel ran out (2 s without progress): the CTA
+     * stopped, let its copies in flight land, released its tensor memory and
+     * wrote NaN to every output it owned, so the call's result holds NaN
+     * where it is incomplete. */
+    W4A16_ERROR_WAIT_TIMEOUT = 1
 };
 
 /* Overrides for tests and tuning.  Zero-initialised = automatic. */
@@ -113,6 +132,17 @@ typedef struct {
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *w4a16_status_string(int status);
+
+/* The device-side error word of the current device: the OR of the
+ * W4A16_ERROR_* bits that this library's kernels have recorded since it was
+ * last cleared (kernels never trap; a pipeline that cannot make progress
+ * records a bit and ends).  *out receives the word; clear != 0 resets it to 0.
+ * Host only and synchronous: it waits for all work on the device
+ * (cudaDeviceSynchronize) and copies the word back, so it is a checking call,
+ * not one for the GEMM's path, and it cannot be captured in a CUDA graph.  The
+ * pages have no counterpart (their kernels report nothing on the device); this
+ * is the library's own failure report. */
+w4a16_status w4a16_read_error_word(int *out, int clear);
 
 /* Version of the packed-weight layout written by w4a16_pack_weights.  A packed
  * buffer is only valid for a library reporting the same version. */

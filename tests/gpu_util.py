@@ -15,6 +15,47 @@ def require_gpu():
     build_mod.build()
 
 
+NAN_BF16 = float("nan")
+
+
+def _nan_workspace(nbytes: int) -> torch.Tensor:
+    """A workspace whose every fp32 word is NaN (16-byte aligned, >= 16 bytes)."""
+    n = max(16, (nbytes + 15) // 16 * 16)
+    return torch.full((n // 4,), float("nan"), dtype=torch.float32, device="cuda").view(torch.uint8)
+
+
+def poisoned_gemm(x, w_packed, scales, **kw):
+    """w4.gemm with Y and the split-K workspace filled with NaN before the call,
+    so an output the kernels skipped shows up as NaN instead of a stale value."""
+    M, K = x.shape
+    N = scales.shape[0]
+    G = K // scales.shape[1]
+    zeros = kw.get("zeros")
+    plan = w4.plan(M, N, K, arm=kw.get("arm"), split_k=kw.get("split_k", 0),
+                   tile_tokens=kw.get("tile_tokens", 0), decode_kernel=kw.get("decode_kernel"),
+                   group_size=G, zero_points=zeros is not None)
+    if "out" not in kw:
+        kw["out"] = torch.full((M, N), NAN_BF16, dtype=torch.bfloat16, device=x.device)
+    if "workspace" not in kw:
+        kw["workspace"] = _nan_workspace(plan["workspace_bytes"])
+    return w4.gemm(x, w_packed, scales, **kw)
+
+
+def poisoned_gemm_batched(x, w_packed, scales, **kw):
+    """w4.gemm_batched with Y and the workspace filled with NaN before the call."""
+    B, M, K = x.shape
+    N = scales.shape[1]
+    G = K // scales.shape[2]
+    plan = w4.plan_batched(B, M, N, K, arm=kw.get("arm"), split_k=kw.get("split_k", 0),
+                           tile_tokens=kw.get("tile_tokens", 0),
+                           decode_kernel=kw.get("decode_kernel"), group_size=G)
+    if "out" not in kw:
+        kw["out"] = torch.full((B, M, N), NAN_BF16, dtype=torch.bfloat16, device=x.device)
+    if "workspace" not in kw:
+        kw["workspace"] = _nan_workspace(plan["workspace_bytes"])
+    return w4.gemm_batched(x, w_packed, scales, **kw)
+
+
 def dev_u16_as_bf16(bits: np.ndarray) -> torch.Tensor:
     a = np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16)
     return torch.from_numpy(a.copy()).view(torch.bfloat16).cuda()

@@ -134,7 +134,8 @@ def test_plan_without_a_gpu_reports_cuda_error(L):
 def test_options_are_checked_before_the_device_is_queried(L):
     # Unknown flag bits, bad arms and bad tile sizes are host-side errors.
     info = _lib.PlanInfo()
-    for o, want in ((_lib.Options(0, 0, 0, 16), INVALID), (_lib.Options(0, 0, 0, 1 << 30), INVALID),
+    for o, want in ((_lib.Options(0, 0, 0, 32), INVALID), (_lib.Options(0, 0, 0, 1 << 30), INVALID),
+                    (_lib.Options(0, 0, 0, 16 | 2), UNSUPPORTED),
                     (_lib.Options(0, 0, 0, 2 | 4), INVALID),
                     (_lib.Options(7, 0, 0, 0), INVALID), (_lib.Options(0, -1, 0, 0), INVALID),
                     (_lib.Options(2, 0, 48, 0), UNSUPPORTED)):
@@ -145,7 +146,7 @@ def test_header_flag_values_match_the_binding():
     import bf16_activation_quantized_gb300 as w4
     text = open(HEADER).read()
     for name, value in (("RESIDENT_WEIGHTS", 1), ("DECODE_WHOLE_K", 2), ("DECODE_K_SLICES", 4),
-                        ("ZERO_POINTS", 8)):
+                        ("ZERO_POINTS", 8), ("TEST_STALL", 16)):
         assert re.search(rf"W4A16_FLAG_{name}\s*=\s*{value}\b", text)
         assert getattr(w4, f"FLAG_{name}") == value
 
@@ -204,3 +205,15 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(lib_mod, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         lib_mod.lib()
+
+
+def test_header_error_bits_match_the_binding():
+    import bf16_activation_quantized_gb300 as w4
+    text = open(HEADER).read()
+    assert re.search(r"W4A16_ERROR_WAIT_TIMEOUT\s*=\s*1\b", text)
+    assert w4.ERROR_WAIT_TIMEOUT == 1
+
+
+def test_read_error_word_checks_its_pointer(L):
+    # A null output pointer is refused before the device is touched.
+    assert L.w4a16_read_error_word(None, 0) == INVALID

@@ -10,7 +10,7 @@ import bf16_activation_quantized_gb300 as w4
 import oracle
 from bf16_activation_quantized_gb300 import synthetic as syn
 
-from gpu_util import bf16_to_f64, bf16_to_u16, dev_u16_as_bf16, dev_u8, require_gpu
+from gpu_util import bf16_to_f64, bf16_to_u16, dev_u16_as_bf16, dev_u8, poisoned_gemm_batched, require_gpu
 from parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -38,7 +38,7 @@ class Batch:
         return oracle.gemm(i.x, i.w_canon[cols], i.scales[cols], self.M, len(cols), self.K)
 
     def run(self, **kw):
-        y = w4.gemm_batched(self.x, self.w, self.scales, **kw)
+        y = poisoned_gemm_batched(self.x, self.w, self.scales, **kw)
         torch.cuda.synchronize()
         return y
 

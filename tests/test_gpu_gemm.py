@@ -19,7 +19,7 @@ import oracle
 from bf16_activation_quantized_gb300 import _lib
 from bf16_activation_quantized_gb300 import synthetic as syn
 
-from gpu_util import DeviceProblem, bf16_to_f64, bf16_to_u16, require_gpu
+from gpu_util import DeviceProblem, bf16_to_f64, bf16_to_u16, poisoned_gemm, require_gpu
 from parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -60,7 +60,7 @@ def sample_cols(N, count=192, seed=0):
 
 
 def run(p, **kw):
-    y = w4.gemm(p.x, p.w_packed, p.scales, **kw)
+    y = poisoned_gemm(p.x, p.w_packed, p.scales, **kw)
     torch.cuda.synchronize()
     return y
 
@@ -196,28 +196,23 @@ def _bf16_bits_to_f64(bits):
 
 
 def test_all_eights_and_zero_scales_give_zero():
+    # Every weight is scale * (8 - 8) = 0, or has a zero scale: Y_ref is 0, so
+    # the bound |y - y_ref| <= 8e-3 |y_ref| + 2e-3 max|y_ref| is 0 and every
+    # arm, kernel and split must return exact zeros.  (The decode arm removes
+    # the 1024 + 8 offset of its fp16 operands exactly, before the MMA.)
     M, N, K = 5, 300, 640
     inp = syn.make_gemm_inputs(M, N, K, seed=3)
     inp.w_canon[:] = 0x88
     p = DeviceProblem(inp)
-    # The tensor arm multiplies exact zeros (code - 8 = 0): exactly 0.
-    assert np.all(bf16_to_f64(run(p, arm="tensor")) == 0.0)
-    # The decode arm feeds the tensor core 1024 + code (or 1024 + 16 code) and
-    # removes 1032 (or 1152) times the group's sum of x, so zero codes cancel
-    # only up to fp32 rounding of terms of size 1152 * sum|x|: bound each
-    # output by that, with margin (2^-18 relative; the observed residue is
-    # near 2^-22).
-    x = _bf16_bits_to_f64(inp.x).reshape(M, K // 128, 128)
-    s = _bf16_bits_to_f64(inp.scales)                        # [N][K/128]
-    bound = 1152.0 * np.abs(x).sum(axis=2) @ np.abs(s).T * 2.0 ** -18   # [M][N]
-    y = bf16_to_f64(run(p, arm="decode"))
-    assert np.all(np.abs(y) <= bound)
-    assert np.max(np.abs(y)) < 1e-4
-    inp2 = syn.make_gemm_inputs(M, N, K, seed=3)
+    for kw in (dict(arm="tensor"), dict(arm="tensor", split_k=5), dict(arm="decode"),
+               dict(arm="decode", split_k=5), dict(arm="decode", split_k=1)):
+        y = bf16_to_f64(run(p, **kw))
+        assert np.all(y == 0.0), f"{kw}: max |y| {np.max(np.abs(y))}"
+    inp2 = syn.make_gemm_inputs(M, N, K, seed=4)
     inp2.scales[:] = 0
     p2 = DeviceProblem(inp2)
-    for arm in ("decode", "tensor"):
-        assert np.all(bf16_to_f64(run(p2, arm=arm)) == 0.0)
+    for kw in (dict(arm="tensor"), dict(arm="decode"), dict(arm="decode", split_k=5)):
+        assert np.all(bf16_to_f64(run(p2, **kw)) == 0.0), kw
 
 
 def test_unit_scales_one_hot_is_exact():
@@ -421,13 +416,12 @@ def test_whole_k_kernel_in_a_graph_replays_exactly():
         assert np.array_equal(bf16_to_u16(out), eager)
 
 
-def test_whole_k_all_eights_give_near_zero():
-    # All codes 8: every weight is 0; the fp32 offset cancellation leaves a
-    # residue far below the output scale (as in the sliced kernel).
+def test_whole_k_all_eights_give_zero():
+    # All codes 8: every weight is 0, so Y_ref is 0 and the output must be
+    # exactly 0 (the offset of the fp16 operands is removed exactly).
     M, N, K = 1, 1024, 4096
     inp = syn.make_gemm_inputs(M, N, K, seed=3)
     inp.w_canon[:] = 0x88
     p = DeviceProblem(inp)
     y = bf16_to_f64(run(p, arm="decode", decode_kernel="whole_k"))
-    x = np.abs(bf16_to_f64(p.x)).sum()
-    assert np.all(np.abs(y) <= 1152 * x * 0.02 * 2.0 ** -18)
+    assert np.all(y == 0.0), f"max |y| {np.max(np.abs(y))}"

@@ -13,7 +13,7 @@ import bf16_activation_quantized_gb300 as w4
 import oracle
 from bf16_activation_quantized_gb300 import synthetic as syn
 
-from gpu_util import bf16_to_f64, bf16_to_u16, dev_u16_as_bf16, dev_u8, require_gpu
+from gpu_util import bf16_to_f64, bf16_to_u16, dev_u16_as_bf16, dev_u8, poisoned_gemm, require_gpu
 from parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -33,7 +33,7 @@ def device(inp):
 def check(M, N, K, G, seed=0, cols=None, **kw):
     inp = syn.make_gemm_inputs(M, N, K, G=G, seed=seed)
     x, wp, s = device(inp)
-    y = w4.gemm(x, wp, s, **kw)
+    y = poisoned_gemm(x, wp, s, **kw)
     torch.cuda.synchronize()
     got = bf16_to_f64(y)
     if cols is None:
@@ -188,3 +188,15 @@ def test_scales_only_2_byte_aligned(G, M, arm):
     torch.cuda.synchronize()
     ref = oracle.gemm(inp.x, inp.w_canon, inp.scales, M, 384, 1024, G=G)
     assert_close(bf16_to_f64(y), ref, what=f"odd scales G={G} {arm}")
+
+
+@pytest.mark.parametrize("G", [64, 32])
+@pytest.mark.parametrize("kw", [dict(arm="decode"), dict(arm="decode", split_k=4), dict(arm="tensor")])
+def test_all_eights_give_exact_zeros(G, kw):
+    # Every weight is scale * (8 - 8) = 0: Y_ref is 0 and so is the bound.
+    M, N, K = 6, 260, 1024
+    inp = syn.make_gemm_inputs(M, N, K, G=G, seed=8)
+    inp.w_canon[:] = 0x88
+    x, wp, s = device(inp)
+    y = bf16_to_f64(poisoned_gemm(x, wp, s, **kw))
+    assert np.all(y == 0.0), f"G={G} {kw}: max |y| {np.max(np.abs(y))}"

@@ -12,7 +12,7 @@ import bf16_activation_quantized_gb300 as w4
 import oracle
 from bf16_activation_quantized_gb300 import synthetic as syn
 
-from gpu_util import bf16_to_f64, dev_u16_as_bf16, dev_u8, require_gpu
+from gpu_util import bf16_to_f64, dev_u16_as_bf16, dev_u8, poisoned_gemm, require_gpu
 from parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -27,7 +27,7 @@ def _gpu():
 def test_prefill_long_sampled(M, N, K):
     assert w4.plan(M, N, K)["arm"] == "tensor"
     inp = syn.make_gemm_inputs(M, N, K, seed=M % 7)
-    y = w4.gemm(dev_u16_as_bf16(inp.x), w4.pack(dev_u8(inp.w_canon)), dev_u16_as_bf16(inp.scales))
+    y = poisoned_gemm(dev_u16_as_bf16(inp.x), w4.pack(dev_u8(inp.w_canon)), dev_u16_as_bf16(inp.scales))
     torch.cuda.synchronize()
     rng = np.random.default_rng(M + N)
     cols = np.unique(np.r_[rng.choice(N, 48, replace=False), 0, 127, 128, N - 1])

@@ -13,7 +13,7 @@ import bf16_activation_quantized_gb300 as w4
 import oracle
 from bf16_activation_quantized_gb300 import synthetic as syn
 
-from gpu_util import bf16_to_f64, bf16_to_u16, dev_u16_as_bf16, dev_u8, require_gpu
+from gpu_util import bf16_to_f64, bf16_to_u16, dev_u16_as_bf16, dev_u8, poisoned_gemm, require_gpu
 from parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -35,7 +35,7 @@ def check(M, N, K, G, seed=0, cols=None, **kw):
     inp = syn.make_gemm_inputs(M, N, K, G=G, seed=seed)
     z = syn.make_zeros(N, K, G, seed=seed)
     x, wp, s, zd = device(inp, z)
-    y = w4.gemm(x, wp, s, zeros=zd, **kw)
+    y = poisoned_gemm(x, wp, s, zeros=zd, **kw)
     torch.cuda.synchronize()
     got = bf16_to_f64(y)
     if cols is None:
@@ -126,3 +126,19 @@ def test_zero_points_shape_checked():
     x, wp, s, zd = device(inp, syn.make_zeros(256, 512))
     with pytest.raises(ValueError):
         w4.gemm(x, wp, s, zeros=zd[:, :1].contiguous())
+
+
+@pytest.mark.parametrize("G", [128, 64, 32])
+@pytest.mark.parametrize("kw", [dict(arm="decode"), dict(arm="decode", split_k=4), dict(arm="tensor")])
+def test_codes_equal_to_their_zero_points_give_exact_zeros(G, kw):
+    # code = z everywhere: every weight is scale * 0, Y_ref is 0, and the
+    # bound is 0, so the output must be exactly 0 for every zero point.
+    M, N, K = 6, 260, 1024
+    inp = syn.make_gemm_inputs(M, N, K, G=G, seed=9)
+    rng = np.random.default_rng(9)
+    zg = rng.integers(0, 16, size=(N, K // G)).astype(np.uint8)
+    codes = np.repeat(zg, G, axis=1)                      # [N][K]: code(n, k) = z(n, k / G)
+    inp.w_canon[:] = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    x, wp, s, zd = device(inp, zg)
+    y = bf16_to_f64(poisoned_gemm(x, wp, s, zeros=zd, **kw))
+    assert np.all(y == 0.0), f"G={G} {kw}: max |y| {np.max(np.abs(y))}"
