@@ -746,7 +746,8 @@ def main(argv=None):
                 [int(v) for v in args.shape.split(",")])
         if rank == 0:
             print(json.dumps(per_shape_table(torch, w4, syn, metrics, device, peaks, only,
-                                             args.group_size, args.zero_points)[0]), flush=True)
+                                             args.group_size, args.zero_points,
+                                             cpu=not args.no_cpu_baseline)[0]), flush=True)
         return 0
     dist = maybe_init_dist(world, local)
     out = our_arm(args, world, rank, local, dist)

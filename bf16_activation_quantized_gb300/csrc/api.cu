@@ -49,13 +49,17 @@ constexpr int kDecodeInFlight = 3;            // bulk copies (ring stages) in th
 constexpr double kHbmBytesPerS = 6.5e12;      // planning figures, not measurements
 constexpr double kCtaBytesPerS = 25e9;        // one CTA's streaming rate (32 KB in flight)
 constexpr double kL2BytesPerS = 20e12;
-constexpr double kReduceSeconds = 1.0e-6;        // reduce kernel and its launch boundary (measured)
+// Measured on GB300 with per-CTA %globaltimer timelines of back-to-back
+// calls: after the decode kernel's last CTA, the reduce kernel waits about
+// 0.7 us for the grid to complete, works about 0.85 us, and the next kernel
+// starts about 0.7 us after it (one such boundary every plan has).
+constexpr double kReduceSeconds = 1.5e-6;        // reduce kernel and its extra launch boundary
 constexpr double kTensorReduceSeconds = 0.5e-6;  // the tensor arm's plans were tuned with this
 constexpr double kWholeKSeconds = 0.2e-6;        // whole-K kernel: part sums
-// Whole-K kernel: every CTA stages all of X at the start; measured on GB300
-// the CTAs together draw X from L2 at about this rate (the same lines, half
-// of the CTAs on the other die).
-constexpr double kXBroadcastBytesPerS = 2.8e12;
+// The K-slice kernel stages its slice of X (converted to fp16) before its
+// first stage, about 0.5 us longer than the whole-K kernel takes to receive
+// the first stage's X with its weights.
+constexpr double kSliceStagingSeconds = 0.5e-6;
 constexpr double kReducePerSliceSeconds = 0.01e-6;  // reduce latency per extra slice
 constexpr int kDecodeMaxM = 16;               // auto dispatch: M <= 16 -> decode arm
 constexpr double kClockHz = 1.9e9;            // planning clock
@@ -138,15 +142,16 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int bat
     d->in_flight = kDecodeInFlight;
     d->wk_blocks = 0;
     if (wk != 2 && forced_split <= 1 && sub == 1 && !zp) {
-        // (one block per CTA would leave each K-part a single ring slot)
-        for (int B : {8, 4, 2}) {
+        // Whole-K plans: B blocks of 16 rows per CTA, every CTA resident.
+        const long long blocks = (N + 15) / 16;
+        for (int B : {8, 4, 2, 1}) {
             if (!decode_wk_fits(M, K, B)) continue;
-            const long long ctas = (long long)d->n_tiles * (kTileRows / 16) / B;
+            const long long ctas = (blocks + B - 1) / B;
             if (ctas > slots) continue;   // per entry
             const double cta_bytes = double(B) * 16.0 * double(K) / 2.0;
             double t = w_bytes / kHbmBytesPerS;
             if (cta_bytes / kCtaBytesPerS > t) t = cta_bytes / kCtaBytesPerS;
-            t += kWholeKSeconds + double(ctas) * batch * M * K * 2.0 / kXBroadcastBytesPerS;
+            t += kWholeKSeconds;
             if (t < best * 0.999) {
                 best = t;
                 d->wk_blocks = B;
@@ -186,6 +191,7 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int bat
             double t = w_bytes * d->token_blocks / kHbmBytesPerS;
             const double t_cta = cta_bytes / kCtaBytesPerS;
             if (t_cta > t) t = t_cta;
+            t += kSliceStagingSeconds;
             if (sk > 1)
                 t += 2.0 * double(sk) * M * N * 4.0 / kL2BytesPerS + kReduceSeconds +
                      kReducePerSliceSeconds * sk;

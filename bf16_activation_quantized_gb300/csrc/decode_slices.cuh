@@ -578,76 +578,61 @@ decode_body(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
                 slot = 0;
                 phase ^= 1u;
             }
-            // The stage's SG groups as SG independent MMA chains, interleaved
-            // k16 step by k16 step (the groups' fragments are built just
-            // before their MMAs): the chains' latencies overlap.  A chain
-            // restarts from zero at each scale group and is added to the
-            // accumulator times that group's scale.
-            float c[SG][MT][4];
 #pragma unroll
-            for (int gg = 0; gg < SG; ++gg)
+            for (int gg = 0; gg < SG; ++gg) {
+            const int gi = gs + gg;
+            const uint32_t (&wv)[8] = wvs[gg];
+            // fp16 A fragments: rows g hold 1024 + code (nibble in mantissa
+            // bits 0-3), rows g + 8 hold 1024 + 16 code (bits 4-7), so one
+            // shift per word serves both halves of the upper byte pair.
+            uint32_t af[8][4];
 #pragma unroll
-                for (int o = 0; o < MT; ++o)
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t w8 = wv[j] >> 8;
+                af[j][0] = lop3_and_or(wv[j], 0x000F000Fu, kMagicF16x2_1024);
+                af[j][1] = lop3_and_or(wv[j], 0x00F000F0u, kMagicF16x2_1024);
+                af[j][2] = lop3_and_or(w8, 0x000F000Fu, kMagicF16x2_1024);
+                af[j][3] = lop3_and_or(w8, 0x00F000F0u, kMagicF16x2_1024);
+            }
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) c[gg][o][r] = 0.f;
+            for (int j = 0; j < SUB; ++j) {
+                // Scales of rows g (C elements 0, 1) and g + 8 (2, 3) for
+                // scale group gi * SUB + j, loaded a tile ahead.
+                const float s0 = scale_of<NSC>(s_cur[0], gi * SUB + j);
+                const float s1 = scale_of<NSC>(s_cur[1], gi * SUB + j);
+                // Offsets of rows g and g + 8 as fp16x2 pairs.
+                uint32_t off0 = kF16x2_1032, off1 = kF16x2_1152;
+                if constexpr (kZp) {
+                    off0 = (0x6400u | zero_of<NSC>(z_cur[0], gi * SUB + j)) * 0x10001u;
+                    off1 = (0x6400u | (zero_of<NSC>(z_cur[1], gi * SUB + j) << 4)) * 0x10001u;
+                }
+                // The exact A operands of this chain: code - offset.
 #pragma unroll
-            for (int k16 = 0; k16 < 4; ++k16) {
-                constexpr int kSteps = 4 / SUB;           // k16 steps per scale group
-                const int j = k16 / kSteps;                // scale group within the block
+                for (int w = j * (8 / SUB); w < (j + 1) * (8 / SUB); ++w) {
+                    af[w][0] = f16x2_sub(af[w][0], off0);
+                    af[w][1] = f16x2_sub(af[w][1], off1);
+                    af[w][2] = f16x2_sub(af[w][2], off0);
+                    af[w][3] = f16x2_sub(af[w][3], off1);
+                }
 #pragma unroll
-                for (int gg = 0; gg < SG; ++gg) {
-                    const int gi = gs + gg;
-                    // Offsets of rows g and g + 8 as fp16x2 pairs.
-                    uint32_t off0 = kF16x2_1032, off1 = kF16x2_1152;
-                    if constexpr (kZp) {
-                        off0 = (0x6400u | zero_of<NSC>(z_cur[0], gi * SUB + j)) * 0x10001u;
-                        off1 = (0x6400u | (zero_of<NSC>(z_cur[1], gi * SUB + j) << 4)) * 0x10001u;
-                    }
-                    // fp16 A fragments of words 2 k16 and 2 k16 + 1: rows g hold
-                    // 1024 + code (nibble in mantissa bits 0-3), rows g + 8 hold
-                    // 1024 + 16 code (bits 4-7), so one shift per word serves
-                    // both halves of the upper byte pair; the exact subtraction
-                    // leaves code - 8 (16 (code - 8) for rows g + 8).
-                    uint32_t af[2][4];
+                for (int o = 0; o < MT; ++o) {
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t w = wvs[gg][2 * k16 + h];
-                        const uint32_t w8 = w >> 8;
-                        af[h][0] = f16x2_sub(lop3_and_or(w, 0x000F000Fu, kMagicF16x2_1024), off0);
-                        af[h][1] = f16x2_sub(lop3_and_or(w, 0x00F000F0u, kMagicF16x2_1024), off1);
-                        af[h][2] = f16x2_sub(lop3_and_or(w8, 0x000F000Fu, kMagicF16x2_1024), off0);
-                        af[h][3] = f16x2_sub(lop3_and_or(w8, 0x00F000F0u, kMagicF16x2_1024), off1);
-                    }
-#pragma unroll
-                    for (int o = 0; o < MT; ++o) {
+                    for (int k16 = j * (4 / SUB); k16 < (j + 1) * (4 / SUB); ++k16) {
                         // Lanes of absent tokens read the last staged row (xrow is
                         // clamped): those values reach only absent tokens' output
                         // columns, which are never stored.
                         const uint4 xv = *reinterpret_cast<const uint4 *>(xs + xrow[o] + gi * kGroup + 32 * k16);
-                        mma_16816_f16_acc(c[gg][o], af[0], xv.x, xv.y);
-                        mma_16816_f16_acc(c[gg][o], af[1], xv.z, xv.w);
+                        mma_16816_f16_acc(c, af[2 * k16], xv.x, xv.y);
+                        mma_16816_f16_acc(c, af[2 * k16 + 1], xv.z, xv.w);
                     }
-                }
-                if ((k16 + 1) % kSteps == 0) {
-                    // End of scale group j: scale each chain (rows g: C elements
-                    // 0, 1; rows g + 8: 2, 3; scales loaded a tile ahead).
-#pragma unroll
-                    for (int gg = 0; gg < SG; ++gg) {
-                        const int gi = gs + gg;
-                        const float s0 = scale_of<NSC>(s_cur[0], gi * SUB + j);
-                        const float s1 = scale_of<NSC>(s_cur[1], gi * SUB + j);
-#pragma unroll
-                        for (int o = 0; o < MT; ++o) {
-                            acc[o][0] = fmaf(s0, c[gg][o][0], acc[o][0]);
-                            acc[o][1] = fmaf(s0, c[gg][o][1], acc[o][1]);
-                            acc[o][2] = fmaf(s1, c[gg][o][2], acc[o][2]);
-                            acc[o][3] = fmaf(s1, c[gg][o][3], acc[o][3]);
-#pragma unroll
-                            for (int r = 0; r < 4; ++r) c[gg][o][r] = 0.f;
-                        }
-                    }
+                    acc[o][0] = fmaf(s0, c[0], acc[o][0]);
+                    acc[o][1] = fmaf(s0, c[1], acc[o][1]);
+                    acc[o][2] = fmaf(s1, c[2], acc[o][2]);
+                    acc[o][3] = fmaf(s1, c[3], acc[o][3]);
                 }
             }
+            }   // gg
         }
         if (failed_at >= 0) break;
 #pragma unroll

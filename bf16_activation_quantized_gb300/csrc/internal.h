@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace w4a16 {
@@ -58,6 +59,13 @@ cudaError_t launch_decode_wk(int blocks_per_cta, int ctas, int batch, const uint
                              cudaStream_t s);
 
 size_t packed_bytes(int N, int K);
+
+// A tiled TMA descriptor (cuTensorMapEncodeTiled through the runtime's driver
+// entry point; element strides 1, L2 promotion 256 B, no OOB fill).
+// strides_bytes has rank - 1 entries.
+cudaError_t encode_tensor_map(CUtensorMap *map, CUtensorMapDataType type, int rank, const void *base,
+                              const cuuint64_t *dims, const cuuint64_t *strides_bytes,
+                              const cuuint32_t *box, CUtensorMapSwizzle swizzle);
 
 cudaError_t launch_pack(const uint8_t *w_canon, uint8_t *w_packed, int N, int K, cudaStream_t s);
 // G: scale group size (128, 64 or 32 columns); Z: zero points uint8 [N][K/G]

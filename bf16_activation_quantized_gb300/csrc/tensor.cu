@@ -770,6 +770,8 @@ tc_gemm_zp_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a,
     tc_gemm_body<kSplit, kSep, false, kSub, true>(tmap_x, a, Z);
 }
 
+}  // namespace
+
 using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
 
 EncodeTiledFn encode_tiled() {
@@ -790,7 +792,17 @@ EncodeTiledFn encode_tiled() {
     return f;
 }
 
-}  // namespace
+cudaError_t encode_tensor_map(CUtensorMap *map, CUtensorMapDataType type, int rank, const void *base,
+                              const cuuint64_t *dims, const cuuint64_t *strides_bytes,
+                              const cuuint32_t *box, CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, type, cuuint32_t(rank), const_cast<void *>(base), dims, strides_bytes, box,
+                     estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 // A ring depth: as many 64-column group stages (at most four) as fit next to
 // the bt accumulator columns in the CTA's share of the SM's 512 TMEM columns
@@ -877,18 +889,13 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
         (p.sub != 1 && p.sub != 2 && p.sub != 4) ||
         tensor_a_stages(p.tile_tokens, p.occupancy, p.sep_epilogue) < 2)
         return cudaErrorInvalidValue;
-    EncodeTiledFn enc = encode_tiled();
-    if (!enc) return cudaErrorNotSupported;
     CUtensorMap tmap;
     const cuuint64_t gdim[2] = {cuuint64_t(K), cuuint64_t(M_total)};
     const cuuint64_t gstride[1] = {cuuint64_t(K) * 2};
     const cuuint32_t box[2] = {64u, cuuint32_t(p.tile_tokens)};
-    const cuuint32_t estride[2] = {1u, 1u};
-    CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(X), gdim,
-                     gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    cudaError_t er = encode_tensor_map(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, gdim, gstride,
+                                       box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (er != cudaSuccess) return er;
 
     TcArgs a;
     a.Wp = Wp;

@@ -387,8 +387,9 @@ def test_whole_k_kernel_full_output(M, N, K):
 
 
 def test_whole_k_kernel_refuses_what_it_cannot_stage():
-    # 16 tokens, or X rows beyond its staging (M * K > 16384), are refused when forced.
-    for M, N, K in ((16, 2560, 9728), (3, 8192, 8192)):
+    # More than 8 tokens, or a CTA's scales beyond its shared memory (one
+    # 16-row block of K / 128 > 256 groups), are refused when forced.
+    for M, N, K in ((16, 2560, 9728), (9, 256, 512), (1, 256, 65536)):
         with pytest.raises(w4.W4A16Error):
             w4.plan(M, N, K, arm="decode", decode_kernel="whole_k")
     assert not w4.plan(1, 8192, 8192, decode_kernel="k_slices")["whole_k"]

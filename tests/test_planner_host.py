@@ -78,9 +78,9 @@ def test_whole_k_kernel_only_for_128_column_symmetric_groups(L, G):
 def test_headline_plans(L):
     # The decode GEMV shapes' plans on a GB300 (the figures quoted for them).
     st, a = plan(L, 1, 8192, 8192)
-    assert st == OK and a.arm == 1 and a.split_k == 8 and not a.whole_k
+    assert st == OK and a.arm == 1 and a.split_k == 1 and a.whole_k and a.ctas == 256
     st, b = plan(L, 1, 17408, 5120)
-    assert st == OK and b.arm == 1 and b.split_k == 10
+    assert st == OK and b.arm == 1 and b.split_k == 1 and b.whole_k and b.ctas == 272
     st, c = plan(L, 1322, 19456, 2560)
     assert st == OK and c.arm == 2 and c.split_k == 1 and c.tile_tokens == 192 and c.ctas == SMS
 
@@ -157,18 +157,22 @@ def test_forced_arms(L):
     assert plan(L, 1, 2560, 1024, arm=7)[0] == INVALID
 
 
-def test_whole_k_refused_where_x_does_not_fit(L):
-    # The whole-K kernel stages all of X: up to 8 tokens with M * K <= 16384.
+def test_whole_k_refused_where_it_does_not_fit(L):
+    # The whole-K kernel takes up to 8 tokens (their X columns travel in each
+    # ring stage) and keeps a CTA's scales in shared memory (K / 128 <= 256
+    # groups for one 16-row block).
     assert plan(L, 2, 2560, 8192, flags=2)[1].whole_k
-    assert plan(L, 4, 2560, 8192, flags=2)[0] == UNSUPPORTED
+    assert plan(L, 8, 2560, 8192, flags=2)[1].whole_k
     assert plan(L, 9, 256, 512, flags=2)[0] == UNSUPPORTED
+    assert plan(L, 1, 256, 65536, flags=2)[0] == UNSUPPORTED
 
 
 def test_python_plan_for_sms_needs_no_gpu():
     import bf16_activation_quantized_gb300 as w4
     p = w4.plan(1, 8192, 8192, sms=SMS)
-    assert p == {"arm": "decode", "split_k": 8, "tile_tokens": 8, "ctas": p["ctas"],
-                 "workspace_bytes": 8 * 8192 * 4, "whole_k": False}
+    assert p == {"arm": "decode", "split_k": 1, "tile_tokens": 8, "ctas": 256,
+                 "workspace_bytes": 0, "whole_k": True}
+    assert w4.plan(1, 8192, 8192, sms=SMS, decode_kernel="k_slices")["split_k"] == 8
     assert w4.plan(1322, 19456, 2560, sms=SMS)["tile_tokens"] == 192
     assert w4.plan(1, 19456, 2560, sms=SMS, group_size=32, zero_points=True)["whole_k"] is False
     with pytest.raises(w4.W4A16Error):
