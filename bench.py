@@ -340,7 +340,8 @@ def our_arm(args, world, rank, local, dist):
     value = whole_job_gbs(world, step_bytes, args.steps, elapsed)
     launches = args.steps * sum(s.launches for s in shapes)
 
-    # Dominant kernel alone: graphs of back-to-back decode-kernel launches.
+    # Dominant kernel alone: graphs of back-to-back decode-kernel launches
+    # (the whole call where the plan has one launch).
     R = max(C, (200 // C) * C)
     g_part = capture(torch, lambda i: [s.partials(w4, i) for s in shapes], R)
     t_part = min(time_graph(torch, g_part) for _ in range(3)) / R
@@ -354,7 +355,10 @@ def our_arm(args, world, rank, local, dist):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks[peak_key],
                 "unit": "GB/s", "frac": round(achieved / peaks[peak_key], 4),
                 "traffic": load_traffic(),
-                "kernel": "decode_kernel (one launch per shape per step)",
+                "kernel": ", ".join(sorted({("decode_rows_kernel (whole K, one launch)" if s.plan["whole_k"]
+                                             else "decode_kernel (K slices) + splitk_reduce_kernel"
+                                             if s.plan["split_k"] > 1 else "decode_kernel (K slices)")
+                                            for s in shapes})) + " per shape per step",
                 "kernel_us_per_step": round(t_part * 1e6, 3),
                 "reduce_us_per_step": round(t_red * 1e6, 3),
                 "peak_source": f"{peaks_src} (MEASURED_PEAKS.json hbm_gbs)" if peaks_src == "measured"
