@@ -256,10 +256,10 @@ def gemm_partials(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor,
 
 def plan_batched(batch: int, M: int, N: int, K: int, arm=None, split_k: int = 0,
                  tile_tokens: int = 0, device=None, decode_kernel=None,
-                 group_size: int = GROUP) -> dict:
+                 group_size: int = GROUP, zero_points: bool = False) -> dict:
     """What the dispatcher picks for a batch of ``batch`` products of shape (M, N, K)."""
     info = PlanInfo()
-    o = _opts(arm, split_k, tile_tokens, decode_kernel=decode_kernel)
+    o = _opts(arm, split_k, tile_tokens, decode_kernel=decode_kernel, zero_points=zero_points)
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         _lib.check(_lib.lib().w4a16_plan_batched(batch, M, N, K, group_size, ctypes.byref(o),
                                                  ctypes.byref(info)), "w4a16_plan_batched")
@@ -269,11 +269,12 @@ def plan_batched(batch: int, M: int, N: int, K: int, arm=None, split_k: int = 0,
 def gemm_batched(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, *, arm=None,
                  split_k: int = 0, tile_tokens: int = 0, out: torch.Tensor | None = None,
                  workspace: torch.Tensor | None = None, resident_weights: bool = False,
-                 decode_kernel=None) -> torch.Tensor:
+                 decode_kernel=None, zeros: torch.Tensor | None = None) -> torch.Tensor:
     """Y[b] = X[b] . dequant(W[b])^T for every b in one launch.
 
     x: bf16 [B, M, K]; w_packed: uint8 [B, packed_weight_bytes(N, K)] (or the same
-    bytes flat); scales: bf16 [B, N, K/G]; returns bf16 [B, M, N]."""
+    bytes flat); scales: bf16 [B, N, K/G]; returns bf16 [B, M, N].  ``zeros``
+    (uint8 [B, N, K/G]) selects the zero-point variant (w4a16_gemm_batched_zp)."""
     _need_cuda(x, "x", torch.bfloat16)
     _need_cuda(scales, "scales", torch.bfloat16)
     _need_cuda(w_packed, "w_packed", torch.uint8)
@@ -290,30 +291,41 @@ def gemm_batched(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor, 
         out = torch.empty((B, M, N), dtype=torch.bfloat16, device=x.device)
     else:
         _need_cuda(out, "out", torch.bfloat16)
-    o = _opts(arm, split_k, tile_tokens, resident_weights, decode_kernel)
+    if zeros is not None:
+        _need_cuda(zeros, "zeros", torch.uint8)
+        if tuple(zeros.shape) != tuple(scales.shape):
+            raise ValueError("zeros must be uint8 [B, N, K/G], the shape of scales")
+    o = _opts(arm, split_k, tile_tokens, resident_weights, decode_kernel, zeros is not None)
     with torch.cuda.device(x.device):
         info = PlanInfo()
         _lib.check(_lib.lib().w4a16_plan_batched(B, M, N, K, G, ctypes.byref(o), ctypes.byref(info)),
                    "w4a16_plan_batched")
         need = int(info.workspace_bytes)
         ws = workspace if workspace is not None else (_workspace(x.device, need) if need else None)
-        _lib.check(_lib.lib().w4a16_gemm_batched(
-            x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), out.data_ptr(), B, M, N, K, G,
-            ws.data_ptr() if ws is not None else None,
-            ws.numel() * ws.element_size() if ws is not None else 0, ctypes.byref(o),
-            _stream_ptr(x.device)), "w4a16_gemm_batched")
+        args = (ws.data_ptr() if ws is not None else None,
+                ws.numel() * ws.element_size() if ws is not None else 0, ctypes.byref(o),
+                _stream_ptr(x.device))
+        if zeros is None:
+            _lib.check(_lib.lib().w4a16_gemm_batched(
+                x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), out.data_ptr(), B, M, N, K, G,
+                *args), "w4a16_gemm_batched")
+        else:
+            _lib.check(_lib.lib().w4a16_gemm_batched_zp(
+                x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), zeros.data_ptr(),
+                out.data_ptr(), B, M, N, K, G, *args), "w4a16_gemm_batched_zp")
     return out
 
 
 def gemm_grouped(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor,
                  m_sizes: torch.Tensor, *, out: torch.Tensor | None = None,
-                 status: torch.Tensor | None = None):
+                 status: torch.Tensor | None = None, zeros: torch.Tensor | None = None):
     """Grouped product in one launch.
 
     x: bf16 [M_total, K]; w_packed: num_groups packed blocks; scales: bf16
     [num_groups, N, K/G]; m_sizes: int32 [num_groups] on the device (never
-    read on the host).  Returns (Y bf16 [M_total, N], status int32 tensor
-    whose element 0 the kernel sets; 0 = sizes consistent)."""
+    read on the host).  ``zeros`` (uint8 [num_groups, N, K/G]) selects the
+    zero-point variant (w4a16_gemm_grouped_zp).  Returns (Y bf16 [M_total, N],
+    status int32 tensor whose element 0 the kernel sets; 0 = sizes consistent)."""
     _need_cuda(x, "x", torch.bfloat16)
     _need_cuda(scales, "scales", torch.bfloat16)
     _need_cuda(w_packed, "w_packed", torch.uint8)
@@ -334,10 +346,20 @@ def gemm_grouped(x: torch.Tensor, w_packed: torch.Tensor, scales: torch.Tensor,
                    "w4a16_grouped_workspace_bytes")
         if status is None:
             status = torch.empty(max(4, (nb.value + 3) // 4), dtype=torch.int32, device=x.device)
-        _lib.check(L.w4a16_gemm_grouped(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(),
-                                        m_sizes.data_ptr(), out.data_ptr(), NG, M_total, N, K,
-                                        G, status.data_ptr(), status.numel() * 4,
-                                        _stream_ptr(x.device)), "w4a16_gemm_grouped")
+        if zeros is None:
+            _lib.check(L.w4a16_gemm_grouped(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(),
+                                            m_sizes.data_ptr(), out.data_ptr(), NG, M_total, N, K,
+                                            G, status.data_ptr(), status.numel() * 4,
+                                            _stream_ptr(x.device)), "w4a16_gemm_grouped")
+        else:
+            _need_cuda(zeros, "zeros", torch.uint8)
+            if tuple(zeros.shape) != tuple(scales.shape):
+                raise ValueError("zeros must be uint8 [num_groups, N, K/G], the shape of scales")
+            _lib.check(L.w4a16_gemm_grouped_zp(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(),
+                                               zeros.data_ptr(), m_sizes.data_ptr(), out.data_ptr(),
+                                               NG, M_total, N, K, G, status.data_ptr(),
+                                               status.numel() * 4, _stream_ptr(x.device)),
+                       "w4a16_gemm_grouped_zp")
     return out, status
 
 

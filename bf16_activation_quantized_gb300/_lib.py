@@ -42,6 +42,8 @@ SIGNATURES = {
     "w4a16_plan_for_sms": (I, [I, I, I, I, I, I, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]),
     "w4a16_gemm_batched": (I, [P, P, P, P, I, I, I, I, I, P, SZ, ctypes.POINTER(Options), P]),
     "w4a16_gemm_zp": (I, [P, P, P, P, P, I, I, I, I, P, SZ, ctypes.POINTER(Options), P]),
+    "w4a16_gemm_batched_zp": (I, [P, P, P, P, P, I, I, I, I, I, P, SZ, ctypes.POINTER(Options), P]),
+    "w4a16_gemm_grouped_zp": (I, [P, P, P, P, P, P, I, I, I, I, I, P, SZ, P]),
     "w4a16_grouped_workspace_bytes": (I, [I, I, I, I, I, ctypes.POINTER(SZ)]),
     "w4a16_gemm_grouped": (I, [P, P, P, P, P, I, I, I, I, I, P, SZ, P]),
     "w4a16_dequant_fp32": (I, [P, P, P, I, I, I, P]),

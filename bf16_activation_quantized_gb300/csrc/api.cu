@@ -358,7 +358,6 @@ w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, 
         return W4A16_ERR_INVALID_ARG;
     const bool stall = (flags & W4A16_FLAG_TEST_STALL) != 0;
     const bool zp = (flags & W4A16_FLAG_ZERO_POINTS) != 0;
-    if (zp && batch > 1) return W4A16_ERR_UNSUPPORTED;
     if ((flags & W4A16_FLAG_DECODE_WHOLE_K) && (flags & W4A16_FLAG_DECODE_K_SLICES))
         return W4A16_ERR_INVALID_ARG;
     int wk = (flags & W4A16_FLAG_DECODE_WHOLE_K) ? 1 : (flags & W4A16_FLAG_DECODE_K_SLICES) ? 2 : 0;
@@ -589,11 +588,11 @@ w4a16_status w4a16_grouped_workspace_bytes(int num_groups, int M_total, int N, i
     return W4A16_OK;
 }
 
-w4a16_status w4a16_gemm_grouped(const w4a16_bf16 *X, const uint8_t *W_packed,
-                                const w4a16_bf16 *scales, const int32_t *M_sizes_dev,
-                                w4a16_bf16 *Y, int num_groups, int M_total, int N, int K,
-                                int group_size, void *workspace, size_t workspace_bytes,
-                                void *stream) {
+static w4a16_status grouped_impl(const w4a16_bf16 *X, const uint8_t *W_packed,
+                                 const w4a16_bf16 *scales, const uint8_t *zeros,
+                                 const int32_t *M_sizes_dev, w4a16_bf16 *Y, int num_groups,
+                                 int M_total, int N, int K, int group_size, void *workspace,
+                                 size_t workspace_bytes, void *stream) {
     w4a16_status st = check_shape(M_total, N, K, group_size);
     if (st != W4A16_OK) return st;
     if (num_groups < 1 || num_groups > kMaxGroups) return W4A16_ERR_INVALID_ARG;
@@ -616,8 +615,40 @@ w4a16_status w4a16_gemm_grouped(const w4a16_bf16 *X, const uint8_t *W_packed,
     t.ctas = int(bound < slots ? bound : slots);
     cudaError_t e = launch_tensor(t, X, W_packed, scales, Y, nullptr, M_sizes_dev,
                                   static_cast<int *>(workspace), num_groups, M_total, N, K,
-                                  static_cast<cudaStream_t>(stream));
+                                  static_cast<cudaStream_t>(stream), 0, zeros);
     return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+w4a16_status w4a16_gemm_grouped(const w4a16_bf16 *X, const uint8_t *W_packed,
+                                const w4a16_bf16 *scales, const int32_t *M_sizes_dev,
+                                w4a16_bf16 *Y, int num_groups, int M_total, int N, int K,
+                                int group_size, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    return grouped_impl(X, W_packed, scales, nullptr, M_sizes_dev, Y, num_groups, M_total, N, K,
+                        group_size, workspace, workspace_bytes, stream);
+}
+
+w4a16_status w4a16_gemm_grouped_zp(const w4a16_bf16 *X, const uint8_t *W_packed,
+                                   const w4a16_bf16 *scales, const uint8_t *zeros,
+                                   const int32_t *M_sizes_dev, w4a16_bf16 *Y, int num_groups,
+                                   int M_total, int N, int K, int group_size, void *workspace,
+                                   size_t workspace_bytes, void *stream) {
+    if (!zeros) return W4A16_ERR_INVALID_ARG;
+    return grouped_impl(X, W_packed, scales, zeros, M_sizes_dev, Y, num_groups, M_total, N, K,
+                        group_size, workspace, workspace_bytes, stream);
+}
+
+w4a16_status w4a16_gemm_batched_zp(const w4a16_bf16 *X, const uint8_t *W_packed,
+                                   const w4a16_bf16 *scales, const uint8_t *zeros, w4a16_bf16 *Y,
+                                   int batch, int M, int N, int K, int group_size, void *workspace,
+                                   size_t workspace_bytes, const w4a16_options *opts,
+                                   void *stream) {
+    if (M > 0 && !zeros) return W4A16_ERR_INVALID_ARG;
+    w4a16_options o = {};
+    if (opts) o = *opts;
+    o.flags |= W4A16_FLAG_ZERO_POINTS;
+    return gemm_impl(X, W_packed, scales, Y, M, N, K, group_size, workspace, workspace_bytes, &o,
+                     true, nullptr, stream, batch, zeros);
 }
 
 w4a16_status w4a16_dequant_fp32(const uint8_t *W_packed, const w4a16_bf16 *scales, float *out,

@@ -103,20 +103,29 @@ __device__ __forceinline__ bool elapsed_beyond(unsigned long long *t0, unsigned 
     return now - *t0 > limit_ns;
 }
 
+// Reading %globaltimer is slow (measured on GB300: a producer loop that read
+// it once per iteration issued one copy every ~0.5 us), so the bounded waits
+// consult it only once every kTimerPollSpins failed polls.
+constexpr int kTimerPollSpins = 32;
+
 // Wait for the phase with the given parity to complete.  Returns false on
 // timeout (after limit_ns) or when the CTA is already aborting.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                           int *err_word,
                                           unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
-    unsigned long long t0 = global_timer_ns();
-    for (;;) {
+    unsigned long long t0 = 0;
+    for (int spins = 1;; ++spins) {
         if (mbar_try_wait_sleep(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (elapsed_beyond(&t0, limit_ns)) {
-            *abort_flag = 1;
-            if (err_word) atomicOr(err_word, kErrWaitTimeout);
-            return false;
+        if (spins % kTimerPollSpins == 0) {
+            if (t0 == 0) {
+                t0 = global_timer_ns();
+            } else if (elapsed_beyond(&t0, limit_ns)) {
+                *abort_flag = 1;
+                if (err_word) atomicOr(err_word, kErrWaitTimeout);
+                return false;
+            }
         }
     }
 }

@@ -97,7 +97,7 @@ int tensor_tmem_cols(int bt, int occupancy, bool sep);  // TMEM columns a CTA al
 cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t *Wp,
                           const uint16_t *S, uint16_t *Y, float *ws, const int32_t *m_sizes,
                           int *status, int num_groups, int M_total, int N, int K, cudaStream_t s,
-                          int batch_rows = 0, const uint8_t *Z = nullptr);   // Z: zero points, plain products
+                          int batch_rows = 0, const uint8_t *Z = nullptr);   // Z: zero points [groups][N][K/G]
 
 cudaError_t launch_reduce(const float *ws, uint16_t *Y, int splits, long long count, bool pdl,
                           cudaStream_t s);

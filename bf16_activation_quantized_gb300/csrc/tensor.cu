@@ -452,7 +452,10 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
             int gx = x_more ? tx.slice * a.gps : 0, gw = w_more ? tw.slice * a.gps : 0;
             int xq = 0, wq = 0, xs = 0, ws = 0;
             uint32_t xpar = 1, wpar = 1;     // parity of the empty phase to wait for (first lap: none)
-            unsigned long long t_progress = global_timer_ns();
+            // Time without progress, read from %globaltimer only every
+            // kTimerPollSpins idle iterations (a read is slow).
+            unsigned long long t_progress = 0;
+            int idle = 0;
             while (x_more || w_more) {
                 bool progressed = false;
                 if (x_more && (xq < SX || mbar_test_wait(xempty_bar(xs), xpar))) {
@@ -487,13 +490,18 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                     progressed = true;
                 }
                 if (progressed) {
-                    t_progress = global_timer_ns();
+                    idle = 0;
+                    t_progress = 0;
                 } else {
                     if (*abort_flag) break;
-                    if (elapsed_beyond(&t_progress, kWaitLimitNs)) {
-                        *abort_flag = 1;
-                        atomicOr(a.err, kErrWaitTimeout);
-                        break;
+                    if (++idle % kTimerPollSpins == 0) {
+                        if (t_progress == 0) {
+                            t_progress = global_timer_ns();
+                        } else if (elapsed_beyond(&t_progress, kWaitLimitNs)) {
+                            *abort_flag = 1;
+                            atomicOr(a.err, kErrWaitTimeout);
+                            break;
+                        }
                     }
                 }
             }
@@ -763,11 +771,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     tc_gemm_body<kSplit, kSep, kBatched, kSub, false>(tmap_x, a, nullptr);
 }
 
-template <bool kSplit, bool kSep, int kSub>
+template <bool kSplit, bool kSep, bool kBatched, int kSub>
 __global__ void __launch_bounds__(kSep ? kTcThreadsSep : kTcThreads, kSep ? 1 : 2)
 tc_gemm_zp_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a,
                   const uint8_t *__restrict__ Z) {
-    tc_gemm_body<kSplit, kSep, false, kSub, true>(tmap_x, a, Z);
+    tc_gemm_body<kSplit, kSep, kBatched, kSub, true>(tmap_x, a, Z);
 }
 
 }  // namespace
@@ -842,16 +850,17 @@ cudaError_t launch_tc_sub(const TensorPlan &p, const CUtensorMap &tmap, const Tc
                           size_t smem, cudaStream_t s, const uint8_t *Z) {
     const bool split = p.split_k > 1;
     const bool sep = p.sep_epilogue;
-    if (Z && batched) return cudaErrorInvalidValue;
     auto kern = batched ? (split ? (sep ? tc_gemm_kernel<true, true, true, kSub> : tc_gemm_kernel<true, false, true, kSub>)
                                  : (sep ? tc_gemm_kernel<false, true, true, kSub> : tc_gemm_kernel<false, false, true, kSub>))
                         : (split ? (sep ? tc_gemm_kernel<true, true, false, kSub> : tc_gemm_kernel<true, false, false, kSub>)
                                  : (sep ? tc_gemm_kernel<false, true, false, kSub> : tc_gemm_kernel<false, false, false, kSub>));
-    auto kern_zp = split ? (sep ? tc_gemm_zp_kernel<true, true, kSub> : tc_gemm_zp_kernel<true, false, kSub>)
-                         : (sep ? tc_gemm_zp_kernel<false, true, kSub> : tc_gemm_zp_kernel<false, false, kSub>);
-    static std::atomic<unsigned long long> opted[12];
-    const int ki = Z ? 8 + (split ? 2 : 0) + (sep ? 1 : 0)
-                     : (batched ? 4 : 0) + (split ? 2 : 0) + (sep ? 1 : 0);
+    auto kern_zp = batched
+        ? (split ? (sep ? tc_gemm_zp_kernel<true, true, true, kSub> : tc_gemm_zp_kernel<true, false, true, kSub>)
+                 : (sep ? tc_gemm_zp_kernel<false, true, true, kSub> : tc_gemm_zp_kernel<false, false, true, kSub>))
+        : (split ? (sep ? tc_gemm_zp_kernel<true, true, false, kSub> : tc_gemm_zp_kernel<true, false, false, kSub>)
+                 : (sep ? tc_gemm_zp_kernel<false, true, false, kSub> : tc_gemm_zp_kernel<false, false, false, kSub>));
+    static std::atomic<unsigned long long> opted[16];
+    const int ki = (Z ? 8 : 0) + (batched ? 4 : 0) + (split ? 2 : 0) + (sep ? 1 : 0);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -931,7 +940,6 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
     const size_t smem =
         tensor_smem_bytes(p.tile_tokens, p.x_stages, p.w_stages, p.occupancy, num_groups, p.sep_epilogue);
     if (smem > size_t(tensor_smem_budget(p.occupancy))) return cudaErrorInvalidValue;
-    if (Z && (m_sizes != nullptr || batched)) return cudaErrorInvalidValue;
     if (p.sub == 2) return launch_tc_sub<2>(p, tmap, a, batched, smem, s, Z);
     if (p.sub == 4) return launch_tc_sub<4>(p, tmap, a, batched, smem, s, Z);
     return launch_tc_sub<1>(p, tmap, a, batched, smem, s, Z);

@@ -250,13 +250,23 @@ w4a16_status w4a16_gemm_batched(const w4a16_bf16 *X, const uint8_t *W_packed,
  *  zeros:    device uint8 [N][K/G]; the low four bits of each byte are z
  *            (all z = 8 gives the symmetric result).
  *  Other arguments as for w4a16_gemm_ex; the workspace is what w4a16_plan
- *  reports with W4A16_FLAG_ZERO_POINTS in opts->flags.  Plain products only
- *  (no batched or grouped form); the decode arm always uses its K-slice
- *  kernel. */
+ *  reports with W4A16_FLAG_ZERO_POINTS in opts->flags.  The decode arm always
+ *  uses its K-slice kernel.  w4a16_gemm_batched_zp and w4a16_gemm_grouped_zp
+ *  below are the batched and grouped forms. */
 w4a16_status w4a16_gemm_zp(const w4a16_bf16 *X, const uint8_t *W_packed, const w4a16_bf16 *scales,
                            const uint8_t *zeros, w4a16_bf16 *Y, int M, int N, int K,
                            int group_size, void *workspace, size_t workspace_bytes,
                            const w4a16_options *opts, void *stream);
+
+/* Batched product with zero points (w4a16_gemm_batched with the dequant of
+ * w4a16_gemm_zp): zeros is device uint8 [batch][N][K/G], entry b's block
+ * following entry b - 1's as for the scales.  The workspace is what
+ * w4a16_plan_batched reports with W4A16_FLAG_ZERO_POINTS in opts->flags. */
+w4a16_status w4a16_gemm_batched_zp(const w4a16_bf16 *X, const uint8_t *W_packed,
+                                   const w4a16_bf16 *scales, const uint8_t *zeros, w4a16_bf16 *Y,
+                                   int batch, int M, int N, int K, int group_size, void *workspace,
+                                   size_t workspace_bytes, const w4a16_options *opts,
+                                   void *stream);
 
 /* Workspace bytes of a grouped call: 16 bytes holding the device status word
  * (see w4a16_gemm_grouped).  Host only. */
@@ -283,6 +293,15 @@ w4a16_status w4a16_gemm_grouped(const w4a16_bf16 *X, const uint8_t *W_packed,
                                 w4a16_bf16 *Y, int num_groups, int M_total, int N, int K,
                                 int group_size, void *workspace, size_t workspace_bytes,
                                 void *stream);
+
+/* Grouped product with zero points: w4a16_gemm_grouped with the dequant of
+ * w4a16_gemm_zp; zeros is device uint8 [num_groups][N][K/G] (group g's block
+ * after group g - 1's, as for the scales).  Same workspace and status word. */
+w4a16_status w4a16_gemm_grouped_zp(const w4a16_bf16 *X, const uint8_t *W_packed,
+                                   const w4a16_bf16 *scales, const uint8_t *zeros,
+                                   const int32_t *M_sizes_dev, w4a16_bf16 *Y, int num_groups,
+                                   int M_total, int N, int K, int group_size, void *workspace,
+                                   size_t workspace_bytes, void *stream);
 
 /* Dequantise a packed weight to fp32: out[n][k] = float(scale[n][k/G]) *
  * (code - 8), computed with the same in-register bit trick the GEMM arms use

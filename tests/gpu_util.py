@@ -48,7 +48,8 @@ def poisoned_gemm_batched(x, w_packed, scales, **kw):
     G = K // scales.shape[2]
     plan = w4.plan_batched(B, M, N, K, arm=kw.get("arm"), split_k=kw.get("split_k", 0),
                            tile_tokens=kw.get("tile_tokens", 0),
-                           decode_kernel=kw.get("decode_kernel"), group_size=G)
+                           decode_kernel=kw.get("decode_kernel"), group_size=G,
+                           zero_points=kw.get("zeros") is not None)
     if "out" not in kw:
         kw["out"] = torch.full((B, M, N), NAN_BF16, dtype=torch.bfloat16, device=x.device)
     if "workspace" not in kw:

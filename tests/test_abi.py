@@ -176,9 +176,11 @@ def test_zero_point_entry_points_check_arguments(L):
     assert L.w4a16_gemm_zp(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 512, 256, None, 0, None, None) == UNSUPPORTED
     assert L.w4a16_gemm_zp(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 500, 128, None, 0, None, None) == INVALID
     assert L.w4a16_gemm_zp(None, None, None, None, None, 0, 256, 512, 32, None, 0, None, None) == OK
-    # no batched zero-point form
-    info = _lib.PlanInfo()
-    assert L.w4a16_plan_batched(2, 4, 256, 512, 128, ctypes.byref(zp), ctypes.byref(info)) == UNSUPPORTED
+    # the batched and grouped forms also require their zeros pointer
+    assert L.w4a16_gemm_batched_zp(FAKE, FAKE, FAKE, None, FAKE, 2, 4, 256, 512, 128, None, 0, None,
+                                   None) == INVALID
+    assert L.w4a16_gemm_grouped_zp(FAKE, FAKE, FAKE, None, FAKE, FAKE, 8, 64, 256, 512, 128, FAKE, 16,
+                                   None) == INVALID
     assert L.w4a16_dequant_zp_fp32(FAKE, FAKE, None, FAKE, 16, 128, 128, None) == INVALID
     assert L.w4a16_dequant_zp_bf16(FAKE, FAKE, FAKE, FAKE, 16, 128, 48, None) == UNSUPPORTED
 

@@ -37,7 +37,8 @@ def test_arguments(L):
     assert plan(L, 1, 256, 512, sms=5000)[0] == INVALID
     assert plan(L, 1, 256, 500)[0] == INVALID
     assert plan(L, 1, 256, 512, G=16)[0] == UNSUPPORTED
-    assert plan(L, 2, 256, 512, batch=2, flags=8)[0] == UNSUPPORTED    # no batched zero points
+    st, info = plan(L, 2, 256, 512, batch=2, flags=8)                 # batched zero points
+    assert st == OK and info.arm == 1 and not info.whole_k
 
 
 @pytest.mark.parametrize("M", [1, 8, 16, 17, 32, 1322])
