@@ -238,11 +238,10 @@ bool tensor_rings(int bt, int num_groups, int occupancy, bool sep, int *x_stages
 }
 
 // Tensor-arm tiles: 128 weight rows x bt tokens, K split into sk slices, one
-// or two CTAs per SM (two when a CTA's TMEM and shared memory fit twice).
+// CTA per SM (576 threads in the plain form, 448 with a separate epilogue).
 // Per K block an SM needs at least max(MMA: 2 bt cycles, a dequant floor,
 // weight bytes at its HBM share + activation bytes at its L2 share), and a
-// CTA cannot go faster than its dependency chain (kTcChainClk per K block),
-// which a second resident CTA hides.
+// CTA cannot go faster than its dependency chain (kTcChainClk per K block).
 // batch_rows > 0: a batched product, num_groups entries of batch_rows rows
 // (M = their total): the plain product per entry, split-K allowed.
 // sub: scale groups per 128-wide block (1, 2, 4); the dequantisers load
@@ -259,10 +258,10 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
         if (forced_bt > 0 && bt != forced_bt) continue;
         // a batched entry's tile wider than the entry is all padding
         if (forced_bt == 0 && batch_rows > 0 && bt >= batch_rows + 32) continue;
-        for (int variant = 0; variant < 3; ++variant) {
-            // occupancy 2; occupancy 1; occupancy 1 with a separate epilogue
-            const int occ = variant == 0 ? 2 : 1;
-            const bool sep = variant == 2;
+        for (int variant = 0; variant < 2; ++variant) {
+            // the plain form; a separate epilogue
+            const int occ = 1;
+            const bool sep = variant == 1;
             if (tensor_a_stages(bt, occ, sep) < 2) continue;  // TMEM share too small
             int sx = 0, sw = 0;
             if (!tensor_rings(bt, num_groups, occ, sep, &sx, &sw)) continue;
@@ -283,12 +282,6 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                     !grouped ? (long long)num_groups * ceil_div((long long)M / num_groups, bt)
                              : (long long)std::ceil(num_groups * (rows_per_unit / bt + 0.5));
                 const long long tiles = (long long)t->n_tiles * t_tiles * sk;
-                // A grid that fits one CTA per SM gains nothing from a second
-                // CTA slot but shallower rings, and the slot lets the block
-                // scheduler put two CTAs of a launch that starts while the
-                // previous one is still resident (programmatic dependent
-                // launch) on the same SM while others stay idle.
-                if (occ == 2 && tiles <= sms) continue;
                 const long long slots = (long long)occ * sms;
                 const long long ctas = tiles < slots ? tiles : slots;
                 const int conc = int(ceil_div(ctas, sms));

@@ -103,6 +103,20 @@ __device__ __forceinline__ bool elapsed_beyond(unsigned long long *t0, unsigned 
     return now - *t0 > limit_ns;
 }
 
+// True in exactly one lane of a converged warp (elect.sync over all 32 lanes,
+// the lowest active lane).  Single-thread issue of TMA copies, MMAs and
+// commits goes through it: measured on GB300, a warp-wide loop that issues
+// tcgen05.mma under elect.sync issued an M=128, N=32 MMA every ~26 cycles,
+// the same loop under `lane == 0` every ~60 and a loop run by lane 0 alone
+// every ~55-100.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p = 0;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}"
+        : "=r"(p));
+    return p != 0;
+}
+
 // Reading %globaltimer is slow (measured on GB300: a producer loop that read
 // it once per iteration issued one copy every ~0.5 us), so the bounded waits
 // consult it only once every kTimerPollSpins failed polls.

@@ -139,56 +139,61 @@ decode_rows_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_consta
     __syncthreads();
 
     if (warp == kRowsWarps) {
-        // Producer: one lane.  Stage q = groups [q SG, q SG + SG) of the CTA's
-        // blocks; its barrier expects the weight box and the M activation rows.
-        if (lane == 0) {
-            tma_prefetch_desc(&wmap);
-            const bool tail = (G % SG) != 0;
-            const int zrow0 = (bz * n_tiles + tile) * KC;
-            auto groups_of = [&](int q) { return min(SG, G - q * SG); };
-            auto bytes_of = [&](int q) {
-                const int ng = groups_of(q);
-                return uint32_t(2 * ng * B * 512 + M * ng * kGroup * 2);
-            };
-            auto issue_w = [&](int q, int st) {
-                const CUtensorMap *m = (tail && q == n_st - 1) ? &wmap_tail : &wmap;
-                tma_load_3d(smem_u32(ring + st * L.stage_bytes), m, 0, bb, zrow0 + 2 * SG * q, full0 + 8 * st);
-            };
-            auto issue_x = [&](int q, int st) {
+        // Producer warp.  Stage q = groups [q SG, q SG + SG) of the CTA's
+        // blocks; its barrier expects the weight box and the M activation
+        // rows.  The whole warp runs the loop: one elected lane posts the
+        // expected bytes and issues the weight box, then lane m < M issues
+        // token m's activation row.
+        if (elect_one()) tma_prefetch_desc(&wmap);
+        const bool tail = (G % SG) != 0;
+        const int zrow0 = (bz * n_tiles + tile) * KC;
+        auto groups_of = [&](int q) { return min(SG, G - q * SG); };
+        auto bytes_of = [&](int q) {
+            const int ng = groups_of(q);
+            return uint32_t(2 * ng * B * 512 + M * ng * kGroup * 2);
+        };
+        auto issue_w = [&](int q, int st) {      // one lane
+            const CUtensorMap *m = (tail && q == n_st - 1) ? &wmap_tail : &wmap;
+            mbar_arrive_expect_tx(full0 + 8 * st, bytes_of(q));
+            tma_load_3d(smem_u32(ring + st * L.stage_bytes), m, 0, bb, zrow0 + 2 * SG * q, full0 + 8 * st);
+        };
+        auto issue_x = [&](int q, int st) {      // lane m: token m
+            if (lane < M) {
                 const uint32_t nb = uint32_t(groups_of(q) * kGroup * 2);
-                unsigned char *dst = ring + st * L.stage_bytes + kRowsStageW;
-                for (int m = 0; m < M; ++m)
-                    bulk_g2s(smem_u32(dst + m * L.x_stride), X + size_t(m) * K + size_t(q) * SG * kGroup, nb,
-                             full0 + 8 * st);
-            };
-            int q0 = 0, issued = 0;
-            if (resident) {
-                // The weights of the first stages stream in while the previous
-                // kernel finishes; X follows once it has completed.
-                q0 = min(NS, n_st);
-                for (int q = 0; q < q0; ++q) {
-                    mbar_arrive_expect_tx(full0 + 8 * q, bytes_of(q));
-                    issue_w(q, q);
-                }
-                pdl_wait();
-                for (int q = 0; q < q0; ++q) issue_x(q, q);
-                issued = q0;
-            } else {
-                pdl_wait();
+                unsigned char *dst = ring + st * L.stage_bytes + kRowsStageW + lane * L.x_stride;
+                bulk_g2s(smem_u32(dst), X + size_t(lane) * K + size_t(q) * SG * kGroup, nb, full0 + 8 * st);
             }
-            for (int q = q0; q < n_st; ++q) {
-                const int st = q % NS;
-                if (q >= NS && !mbar_wait(empty0 + 8 * st, ((q / NS) - 1) & 1, abort_flag, err)) break;
-                mbar_arrive_expect_tx(full0 + 8 * st, bytes_of(q));
-                issue_w(q, st);
-                issue_x(q, st);
-                ++issued;
-            }
-            if (*abort_flag) {
-                // Let every copy issued land before the CTA exits.
-                for (int q = issued > NS ? issued - NS : 0; q < issued; ++q)
-                    drain_wait(full0 + 8 * (q % NS), (q / NS) & 1);
-            }
+        };
+        int q0 = 0, issued = 0;
+        if (resident) {
+            // The weights of the first stages stream in while the previous
+            // kernel finishes; X follows once it has completed.
+            q0 = min(NS, n_st);
+            if (elect_one())
+                for (int q = 0; q < q0; ++q) issue_w(q, q);
+            __syncwarp();
+            pdl_wait();
+            for (int q = 0; q < q0; ++q) issue_x(q, q);
+            issued = q0;
+        } else {
+            pdl_wait();
+        }
+        // Ring slot and the parity of its empty phase, kept as counters
+        // (no division by the runtime ring depth in the loop).
+        int st = q0 % NS;
+        uint32_t epar = uint32_t(q0 / NS + 1) & 1u;
+        for (int q = q0; q < n_st; ++q) {
+            if (q >= NS && !__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * st, epar, abort_flag, err))) break;
+            if (elect_one()) issue_w(q, st);
+            __syncwarp();
+            issue_x(q, st);
+            ++issued;
+            if (++st == NS) { st = 0; epar ^= 1u; }
+        }
+        if (*abort_flag) {
+            // Let every copy issued land before the CTA exits.
+            for (int q = issued > NS ? issued - NS : 0; q < issued; ++q)
+                drain_wait(full0 + 8 * (q % NS), (q / NS) & 1);
         }
         return;
     }
@@ -196,38 +201,35 @@ decode_rows_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_consta
     // ---- consumers (256 threads) ----
     const int g = lane >> 2, t = lane & 3;
     const int b = warp % B, kp = warp / B;
-    // Scales of the CTA's 16 B rows (rows past N read as 0), one contiguous
-    // run of S read with 16-byte vectors when S allows, stored transposed.
-    // With resident weights they are loaded while the previous kernel
-    // finishes.
+    // Scales of the CTA's 16 B rows (rows past N read as 0), stored
+    // transposed.  Consecutive lanes take consecutive rows, each reading 8
+    // scales of its row (one 16-byte vector when S allows), so the transposed
+    // 2-byte stores of a warp fall in distinct banks.  With resident weights
+    // they are loaded while the previous kernel finishes.
     {
         if (!resident) pdl_wait();
-        const int R = B * 16;
-        const int E = R * G;
-        const long long rows_in = (long long)N - row0;
-        const int valid = rows_in <= 0 ? 0 : (rows_in >= R ? E : int(rows_in) * G);
-        const uint16_t *src = S + size_t(row0) * G;
-        auto put = [&](int i, uint16_t v) { s_scale[(i % G) * R + i / G] = v; };
-        if (s_vec) {
-            for (int i = threadIdx.x * 8; i < E; i += kRowsWarps * 32 * 8) {
-                uint16_t e[8];
-                if (i + 8 <= valid) {
-                    const uint4 v = ldg_nc16(src + i);
-                    const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+        constexpr int R = B * 16;
+        const int CH = (G + 7) / 8;
+        for (int idx = threadIdx.x; idx < R * CH; idx += kRowsWarps * 32) {
+            const int r = idx % R, c = idx / R;
+            const bool row_ok = row0 + r < N;
+            const uint16_t *src = S + size_t(row0 + r) * G + 8 * c;
+            uint16_t e[8];
+            if (s_vec && row_ok) {
+                const uint4 v = ldg_nc16(src);
+                const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        e[2 * u] = uint16_t(vv[u] & 0xFFFFu);
-                        e[2 * u + 1] = uint16_t(vv[u] >> 16);
-                    }
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) e[u] = i + u < valid ? src[i + u] : uint16_t(0);
+                for (int u = 0; u < 4; ++u) {
+                    e[2 * u] = uint16_t(vv[u] & 0xFFFFu);
+                    e[2 * u + 1] = uint16_t(vv[u] >> 16);
                 }
+            } else {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) put(i + u, e[u]);
+                for (int u = 0; u < 8; ++u) e[u] = (row_ok && 8 * c + u < G) ? src[u] : uint16_t(0);
             }
-        } else {
-            for (int i = threadIdx.x; i < E; i += kRowsWarps * 32) put(i, i < valid ? src[i] : uint16_t(0));
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (8 * c + u < G) s_scale[(8 * c + u) * R + r] = e[u];
         }
         rows_consumer_bar();
     }
@@ -235,10 +237,11 @@ decode_rows_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_consta
     const int xrow = min(g, M - 1);                            // absent tokens read the last row
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     bool alive = true;
+    int slot = 0;
+    uint32_t fpar = 0;       // parity of the slot's full phase
     for (int q = 0; q < n_st; ++q) {
-        const int slot = q % NS;
         // Warp-uniform outcome: the MMAs below need every lane.
-        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * slot, (q / NS) & 1, abort_flag, err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * slot, fpar, abort_flag, err))) {
             alive = false;
             break;
         }
@@ -294,6 +297,10 @@ decode_rows_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_consta
             acc[1] = fmaf(s0, c[h][1], acc[1]);
             acc[2] = fmaf(s1, c[h][2], acc[2]);
             acc[3] = fmaf(s1, c[h][3], acc[3]);
+        }
+        if (++slot == NS) {
+            slot = 0;
+            fpar ^= 1u;
         }
     }
     // Add the K-parts in ascending order through ring stage 0 (every stage
@@ -374,11 +381,9 @@ cudaError_t launch_rows_t(int ctas, int batch, const uint16_t *X, const uint8_t 
     cfg.numAttrs = 1;
     int *err = device_error_word();
     if (!err) return cudaErrorUnknown;
-    // 16-byte scale vectors: every CTA's first scale row (a multiple of 16
-    // rows) is 16-byte aligned when S is, and so is every batch entry's block
-    // when N * G * 2 bytes is a multiple of 16.
-    const int s_vec = (reinterpret_cast<uintptr_t>(S) % 16) == 0 &&
-                      (batch == 1 || (size_t(N) * G * 2) % 16 == 0);
+    // 16-byte scale vectors (8 scales of a row): every row's scales start
+    // 16-byte aligned, in every batch entry, when S is and G % 8 == 0.
+    const int s_vec = (reinterpret_cast<uintptr_t>(S) % 16) == 0 && G % 8 == 0;
     return cudaLaunchKernelEx(&cfg, kern, wmap, wmap_tail, X, S, Y, M, N, K, int(resident), s_vec, err);
 }
 

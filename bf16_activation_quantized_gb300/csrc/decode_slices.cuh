@@ -374,48 +374,53 @@ decode_body(const uint16_t *__restrict__ X, const uint8_t *__restrict__ Wp,
     if (!resident || warp < kDecodeWarps) pdl_wait();
 
     if (warp == kDecodeWarps) {
-        // Producer: one lane streams every (tile, group) block of this CTA.
+        // Producer warp: streams every (tile, group) block of this CTA.
         // Non-resident weights: it starts once the consumers have issued their
         // X and scale loads, so that those small reads are not queued behind
         // the weight stream.  Resident weights: it starts at once and fills
         // the ring while the previous grid finishes.
         if (!resident) named_bar_sync(2, kDecodeThreads);
-        if (lane == 0) {
-            const size_t tile_step = size_t(C) * KC * kChunkBytes;
-            const uint8_t *src = Wp + (size_t(c0) * KC + size_t(2 * grp0)) * kChunkBytes;
-            // At most IF copies are in the air at once (the ring may
-            // hold more that have landed): a small burst per CTA lets the
-            // first stages land early instead of all of them near the end.
-            const int total = IF > 0 ? n_my * SPT : 0;     // stages
-            int issued = 0, st = 0, gs = 0, lst = 0;
-            uint32_t epar = 1;   // parity of the empty phase to wait for (first lap: none)
-            uint32_t lpar = 0;   // parity of the full phase of copy q - IF
-            for (int q = 0; q < total; ++q) {
-                if (q >= NS && !mbar_wait(empty0 + 8 * st, epar, abort_flag, err, wait_ns)) break;
-                if (q >= IF) {
-                    if (!mbar_wait(full0 + 8 * lst, lpar, abort_flag, err, wait_ns)) break;
-                    if (++lst == NS) { lst = 0; lpar ^= 1; }
-                }
+        // The whole warp runs the loop (warp-uniform values); one elected
+        // lane issues the copies and prefetches.
+        const size_t tile_step = size_t(C) * KC * kChunkBytes;
+        const uint8_t *src = Wp + (size_t(c0) * KC + size_t(2 * grp0)) * kChunkBytes;
+        // At most IF copies are in the air at once (the ring may
+        // hold more that have landed): a small burst per CTA lets the
+        // first stages land early instead of all of them near the end.
+        const int total = IF > 0 ? n_my * SPT : 0;     // stages
+        int issued = 0, st = 0, gs = 0, lst = 0;
+        uint32_t epar = 1;   // parity of the empty phase to wait for (first lap: none)
+        uint32_t lpar = 0;   // parity of the full phase of copy q - IF
+        for (int q = 0; q < total; ++q) {
+            if (q >= NS && !__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * st, epar, abort_flag, err, wait_ns)))
+                break;
+            if (q >= IF) {
+                if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * lst, lpar, abort_flag, err, wait_ns))) break;
+                if (++lst == NS) { lst = 0; lpar ^= 1; }
+            }
+            if (elect_one()) {
                 mbar_arrive_expect_tx(full0 + 8 * st, kStage);
                 bulk_g2s(smem_u32(ring + st * kStage), src + gs * kStage, kStage, full0 + 8 * st);
-                ++issued;
-                if (++gs == SPT) {
-                    gs = 0;
-                    src += tile_step;
-                    // Entering tile (q + 1) / SPT: warm L2 with the scales of the
-                    // tile three ahead, which the consumers load about two tiles later.
-                    const int ahead = (q + 1) / SPT + 3;
-                    if (ahead < n_my) {
-                        prefetch_tile_scales(S, c0 + ahead * C, N, n_sg);
-                        if (kZp) prefetch_tile_zeros(Z, c0 + ahead * C, N, n_sg);
-                    }
+            }
+            __syncwarp();
+            ++issued;
+            if (++gs == SPT) {
+                gs = 0;
+                src += tile_step;
+                // Entering tile (q + 1) / SPT: warm L2 with the scales of the
+                // tile three ahead, which the consumers load about two tiles later.
+                const int ahead = (q + 1) / SPT + 3;
+                if (ahead < n_my && elect_one()) {
+                    prefetch_tile_scales(S, c0 + ahead * C, N, n_sg);
+                    if (kZp) prefetch_tile_zeros(Z, c0 + ahead * C, N, n_sg);
                 }
-                if (++st == NS) { st = 0; epar ^= 1; }
+                __syncwarp();
             }
-            if (*abort_flag) {
-                for (int q = issued > NS ? issued - NS : 0; q < issued; ++q)
-                    drain_wait(full0 + 8 * (q % NS), (q / NS) & 1);
-            }
+            if (++st == NS) { st = 0; epar ^= 1; }
+        }
+        if (*abort_flag) {
+            for (int q = issued > NS ? issued - NS : 0; q < issued; ++q)
+                drain_wait(full0 + 8 * (q % NS), (q / NS) & 1);
         }
         return;
     }

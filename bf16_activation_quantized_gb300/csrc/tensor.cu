@@ -45,16 +45,26 @@ namespace w4a16 {
 
 namespace {
 
-constexpr int kTcDequantWarps = 8;
-constexpr int kTcProducerWarp = 8;
-constexpr int kTcMmaWarp = 9;
-constexpr int kTcThreads = 10 * 32;
-// With a separate epilogue (one CTA per SM): warps 10-13 drain the
-// accumulator while the dequantisers and the MMA go on with the next tile
-// into the other of two TMEM accumulators.
-constexpr int kTcEpiWarp0 = 10;
+// Warp roles (one CTA per SM).  Plain form: 16 dequantisers in two teams of
+// 8, team t taking the CTA's groups t, t + 2, t + 4, ... (the two warps of a
+// team on one SM sub-partition work on one group while the other team's two
+// work on the next, so one pair's waits overlap the other's arithmetic),
+// then the X producer, the W producer and the MMA warp.  With a separate
+// epilogue: one team of 8, the two producers, the MMA warp and 4 epilogue
+// warps that drain one TMEM accumulator while the dequantisers and the MMA
+// go on with the next tile in the other.
+constexpr int kTcTeamWarps = 8;
 constexpr int kTcEpiWarps = 4;
-constexpr int kTcThreadsSep = (kTcEpiWarp0 + kTcEpiWarps) * 32;
+template <bool kSep>
+struct TcRoles {
+    static constexpr int kTeams = kSep ? 1 : 2;
+    static constexpr int kDequant = kTcTeamWarps * kTeams;     // warps 0 .. kDequant - 1
+    static constexpr int kProducerX = kDequant;                 // the X ring
+    static constexpr int kProducerW = kDequant + 1;             // the W ring
+    static constexpr int kMma = kDequant + 2;
+    static constexpr int kEpi0 = kDequant + 3;                  // kSep only
+    static constexpr int kThreads = (kDequant + 3 + (kSep ? kTcEpiWarps : 0)) * 32;
+};
 constexpr uint32_t kTcDCol = 0;      // accumulator: columns [0, bt); A stage sa: [bt + 32 sa, bt + 32 sa + 32)
 
 // TcArgs::opt_bits.
@@ -98,14 +108,23 @@ struct TcSmem {
 constexpr int kGroupBytes = 2 * kChunkBytes;           // packed weights of one 128-column group
 constexpr int kEpiBytesPerWarp = 32 * 32 * 2;          // 32 tokens x 32 rows of bf16
 
+// Epilogue staging buffers: one per warp that drains 32-token column blocks
+// (the 4 epilogue warps, or in the plain form 4 dequantisers per column
+// block, at most all 16).
+__host__ __device__ inline int tc_epi_buffers(int bt, bool sep) {
+    if (sep) return kTcEpiWarps;
+    const int cbs = (bt + 31) / 32;
+    return 4 * (cbs < 4 ? cbs : 4);
+}
+
 __host__ __device__ inline TcSmem tc_smem_layout(int bt, int x_stages, int w_stages, int a_stages,
-                                                 int num_groups) {
+                                                 int num_groups, bool sep) {
     TcSmem L;
     L.x_stage = 2 * bt * 128;
     L.off_x = 0;
     L.off_w = L.off_x + x_stages * L.x_stage;
     L.off_epi = L.off_w + w_stages * kGroupBytes;
-    L.off_bar = L.off_epi + kTcDequantWarps * kEpiBytesPerWarp;
+    L.off_bar = L.off_epi + tc_epi_buffers(bt, sep) * kEpiBytesPerWarp;
     L.off_misc = L.off_bar + (2 * x_stages + 2 * w_stages + 2 * a_stages + 5) * 8;
     L.off_tab = (L.off_misc + 16 + 15) & ~15;           // group tables: 2 x (G + 1) ints
     L.total = L.off_tab + 2 * (num_groups + 1) * 4;
@@ -347,7 +366,8 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled X tiles (the host adds the slack).
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    const TcSmem L = tc_smem_layout(a.bt, a.x_stages, a.w_stages, a.a_stages, a.num_groups);
+    using R = TcRoles<kSep>;
+    const TcSmem L = tc_smem_layout(a.bt, a.x_stages, a.w_stages, a.a_stages, a.num_groups, kSep);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int SX = a.x_stages;
@@ -377,25 +397,25 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
         }
         for (int s = 0; s < SW; ++s) {
             mbar_init(wfull_bar(s), 1);
-            mbar_init(wempty_bar(s), kTcDequantWarps);    // every dequantiser has read it
+            mbar_init(wempty_bar(s), kTcTeamWarps);       // the group's team has read it
         }
         for (int s = 0; s < SA; ++s) {
-            mbar_init(afull_bar(s), kTcDequantWarps);
+            mbar_init(afull_bar(s), kTcTeamWarps);
             mbar_init(aempty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(dfull_bar(b), 1);
-            mbar_init(dempty_bar(b), kSep ? kTcEpiWarps : kTcDequantWarps);
+            mbar_init(dempty_bar(b), kSep ? kTcEpiWarps : R::kDequant);
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == kTcMmaWarp) {
+    if (warp == R::kMma) {
         tc_alloc(smem_u32(tmem_slot), uint32_t(a.tmem_cols));
         tc_relinquish();
     }
-    if (warp == kTcProducerWarp && lane == 0) tma_prefetch_desc(&tmap_x);
+    if (warp == R::kProducerX && lane == 0) tma_prefetch_desc(&tmap_x);
     pdl_launch_dependents();
     pdl_wait();
 
@@ -426,148 +446,150 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
     const uint32_t x_bytes = uint32_t(a.bt) * 128u;          // one X box
     const uint32_t idesc = tc_idesc_bf16(128, a.bt);
 
-    if (warp == kTcProducerWarp) {
-        if (lane == 0) {
-            // Two cursors over the same (tile, group) sequence, one per ring.
-            // Each step issues at most one copy per ring; a stalled ring does
-            // not hold back the other.  The wait is bounded: no progress on
-            // either ring for kWaitLimitNs aborts the CTA.
-            TileInfo tx, tw;
-            int idx = blockIdx.x, idw = blockIdx.x;
-            bool x_more = tc_tile<kBatched>(a, tab_tiles, tab_rows, idx, tx);
-            bool w_more = tc_tile<kBatched>(a, tab_tiles, tab_rows, idw, tw);
-            // Each time the W cursor enters a tile, pull the tile's scales (128
-            // rows x all groups, one contiguous block) into L2, so the
-            // dequantisers' scale loads, issued one group ahead, hit L2.
-            auto prefetch_scales = [&](const TileInfo &ti) {
-                const uint16_t *sg = a.S + (unsigned long long)ti.group * a.s_group_stride;
-                const size_t r0 = size_t(ti.ft) * kTileRows;
-                const size_t r1 = min(size_t(a.N), r0 + kTileRows);
-                // Rounded inwards to 16 bytes: never outside the block.
-                const uintptr_t lo = (reinterpret_cast<uintptr_t>(sg + r0 * n_sg) + 15) & ~uintptr_t(15);
-                const uintptr_t hi = reinterpret_cast<uintptr_t>(sg + r1 * n_sg) & ~uintptr_t(15);
-                if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void *>(lo), uint32_t(hi - lo));
-            };
-            if (w_more) prefetch_scales(tw);
-            int gx = x_more ? tx.slice * a.gps : 0, gw = w_more ? tw.slice * a.gps : 0;
-            int xq = 0, wq = 0, xs = 0, ws = 0;
-            uint32_t xpar = 1, wpar = 1;     // parity of the empty phase to wait for (first lap: none)
-            // Time without progress, read from %globaltimer only every
-            // kTimerPollSpins idle iterations (a read is slow).
-            unsigned long long t_progress = 0;
-            int idle = 0;
-            while (x_more || w_more) {
-                bool progressed = false;
-                if (x_more && (xq < SX || mbar_test_wait(xempty_bar(xs), xpar))) {
-                    const uint32_t xdst = smem_u32(smem + L.off_x + xs * L.x_stage);
-                    mbar_arrive_expect_tx(xfull_bar(xs), 2 * x_bytes);
-                    tma_load_2d(xdst, &tmap_x, gx * kGroup, tx.x_row0, xfull_bar(xs));
-                    tma_load_2d(xdst + x_bytes, &tmap_x, gx * kGroup + kChunkK, tx.x_row0, xfull_bar(xs));
-                    ++xq;
-                    if (++xs == SX) { xs = 0; xpar ^= 1; }
-                    if (++gx == min(n_groups, (tx.slice + 1) * a.gps)) {
-                        idx += gridDim.x;
-                        x_more = tc_tile<kBatched>(a, tab_tiles, tab_rows, idx, tx);
-                        if (x_more) gx = tx.slice * a.gps;
-                    }
-                    progressed = true;
-                }
-                if (w_more && (wq < SW || mbar_test_wait(wempty_bar(ws), wpar))) {
-                    const uint8_t *wg = a.Wp + (unsigned long long)tw.group * a.w_group_stride;
-                    mbar_arrive_expect_tx(wfull_bar(ws), kGroupBytes);
-                    bulk_g2s(smem_u32(smem + L.off_w + ws * kGroupBytes),
-                             wg + ((size_t)tw.ft * KC + 2 * gw) * kChunkBytes, kGroupBytes, wfull_bar(ws));
-                    ++wq;
-                    if (++ws == SW) { ws = 0; wpar ^= 1; }
-                    if (++gw == min(n_groups, (tw.slice + 1) * a.gps)) {
-                        idw += gridDim.x;
-                        w_more = tc_tile<kBatched>(a, tab_tiles, tab_rows, idw, tw);
-                        if (w_more) {
-                            gw = tw.slice * a.gps;
-                            prefetch_scales(tw);
-                        }
-                    }
-                    progressed = true;
-                }
-                if (progressed) {
-                    idle = 0;
-                    t_progress = 0;
+    if (warp == R::kProducerX || warp == R::kProducerW) {
+        // Two producer warps, one per ring, each walking the CTA's (tile,
+        // group) sequence.  The whole warp runs the loop, so its values stay
+        // warp-uniform; one elected lane issues the copies.  (Measured on
+        // GB300: one thread serving both rings in a divergent loop issued one
+        // X and one W copy every ~0.5 us, which paced the whole pipeline at
+        // 32 tokens.)  Waits are bounded: a wait that runs out aborts the CTA.
+        const bool is_x = warp == R::kProducerX;
+        const int S = is_x ? SX : SW;
+        // Each time the W producer enters a tile, it pulls the tile's scales
+        // (128 rows x all groups, one contiguous block) into L2, so the
+        // dequantisers' scale loads, issued one group ahead, hit L2.
+        auto prefetch_scales = [&](const TileInfo &ti) {
+            const uint16_t *sg = a.S + (unsigned long long)ti.group * a.s_group_stride;
+            const size_t r0 = size_t(ti.ft) * kTileRows;
+            const size_t r1 = min(size_t(a.N), r0 + kTileRows);
+            // Rounded inwards to 16 bytes: never outside the block.
+            const uintptr_t lo = (reinterpret_cast<uintptr_t>(sg + r0 * n_sg) + 15) & ~uintptr_t(15);
+            const uintptr_t hi = reinterpret_cast<uintptr_t>(sg + r1 * n_sg) & ~uintptr_t(15);
+            if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void *>(lo), uint32_t(hi - lo));
+        };
+        TileInfo tk;
+        int id = blockIdx.x;
+        bool more = tc_tile<kBatched>(a, tab_tiles, tab_rows, id, tk);
+        int gk = more ? tk.slice * a.gps : 0;
+        if (!is_x && more && elect_one()) prefetch_scales(tk);
+        __syncwarp();
+        int slot = 0, issued = 0;
+        uint32_t epar = 1;              // parity of the slot's empty phase (first lap: no wait)
+        while (more) {
+            const uint32_t empty = is_x ? xempty_bar(slot) : wempty_bar(slot);
+            if (issued >= S && !__all_sync(0xffffffffu, mbar_wait(empty, epar, abort_flag, a.err))) break;
+            if (elect_one()) {
+                if (is_x) {
+                    const uint32_t xdst = smem_u32(smem + L.off_x + slot * L.x_stage);
+                    mbar_arrive_expect_tx(xfull_bar(slot), 2 * x_bytes);
+                    tma_load_2d(xdst, &tmap_x, gk * kGroup, tk.x_row0, xfull_bar(slot));
+                    tma_load_2d(xdst + x_bytes, &tmap_x, gk * kGroup + kChunkK, tk.x_row0, xfull_bar(slot));
                 } else {
-                    if (*abort_flag) break;
-                    if (++idle % kTimerPollSpins == 0) {
-                        if (t_progress == 0) {
-                            t_progress = global_timer_ns();
-                        } else if (elapsed_beyond(&t_progress, kWaitLimitNs)) {
-                            *abort_flag = 1;
-                            atomicOr(a.err, kErrWaitTimeout);
-                            break;
-                        }
-                    }
+                    const uint8_t *wg = a.Wp + (unsigned long long)tk.group * a.w_group_stride;
+                    mbar_arrive_expect_tx(wfull_bar(slot), kGroupBytes);
+                    bulk_g2s(smem_u32(smem + L.off_w + slot * kGroupBytes),
+                             wg + ((size_t)tk.ft * KC + 2 * gk) * kChunkBytes, kGroupBytes, wfull_bar(slot));
                 }
             }
-            if (*abort_flag) {
-                for (int u = xq > SX ? xq - SX : 0; u < xq; ++u) drain_wait(xfull_bar(u % SX), (u / SX) & 1);
-                for (int u = wq > SW ? wq - SW : 0; u < wq; ++u) drain_wait(wfull_bar(u % SW), (u / SW) & 1);
+            __syncwarp();
+            ++issued;
+            if (++slot == S) {
+                slot = 0;
+                epar ^= 1u;
+            }
+            if (++gk == min(n_groups, (tk.slice + 1) * a.gps)) {
+                id += gridDim.x;
+                more = tc_tile<kBatched>(a, tab_tiles, tab_rows, id, tk);
+                if (more) {
+                    gk = tk.slice * a.gps;
+                    if (!is_x && elect_one()) prefetch_scales(tk);
+                    __syncwarp();
+                }
             }
         }
-    } else if (warp == kTcMmaWarp) {
-        if (lane == 0) {
-            int st = 0, sa = 0, tiles = 0;
-            uint32_t xph = 0, aph = 0;      // parities of the phases to wait for
-            const int S = SX;
-            TileInfo ti;
-            for (int id = blockIdx.x; tc_tile<kBatched>(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
-                // Accumulator of this tile and the wait for its previous readers.
-                const int db = kSep ? (tiles & 1) : 0;
-                const int uses = kSep ? (tiles >> 1) : tiles;     // earlier tiles on this buffer
-                if (uses > 0 && !mbar_wait(dempty_bar(db), (uses - 1) & 1, abort_flag, a.err)) break;
+        if (*abort_flag) {
+            // Let every copy issued land before the CTA exits.
+            for (int u = issued > S ? issued - S : 0; u < issued; ++u)
+                drain_wait(is_x ? xfull_bar(u % S) : wfull_bar(u % S), (u / S) & 1);
+        }
+    } else if (warp == R::kMma) {
+        // The whole warp runs the loop (warp-uniform operands); the elected
+        // lane (always the lowest, the warp being converged) issues every MMA
+        // and every commit, so the commits track its MMAs.
+        int st = 0, sa = 0, tiles = 0;
+        uint32_t xph = 0, aph = 0;      // parities of the phases to wait for
+        TileInfo ti;
+        for (int id = blockIdx.x; tc_tile<kBatched>(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
+            // Accumulator of this tile and the wait for its previous readers.
+            const int db = kSep ? (tiles & 1) : 0;
+            const int uses = kSep ? (tiles >> 1) : tiles;     // earlier tiles on this buffer
+            if (uses > 0 &&
+                !__all_sync(0xffffffffu, mbar_wait(dempty_bar(db), (uses - 1) & 1, abort_flag, a.err)))
+                break;
+            tc_fence_after();
+            const uint32_t dcol = tmem_base + kTcDCol + uint32_t(db * a.bt);
+            const int g0 = ti.slice * a.gps;
+            const int g1 = min(n_groups, (ti.slice + 1) * a.gps);
+            bool ok = true;
+            for (int grp = g0; grp < g1; ++grp) {
+                if (!__all_sync(0xffffffffu, mbar_wait(xfull_bar(st), xph, abort_flag, a.err) &&
+                                                 mbar_wait(afull_bar(sa), aph, abort_flag, a.err))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                const uint32_t dcol = tmem_base + kTcDCol + uint32_t(db * a.bt);
-                const int g0 = ti.slice * a.gps;
-                const int g1 = min(n_groups, (ti.slice + 1) * a.gps);
-                bool ok = true;
-                for (int grp = g0; grp < g1; ++grp) {
-                    if (!mbar_wait(xfull_bar(st), xph, abort_flag, a.err) ||
-                        !mbar_wait(afull_bar(sa), aph, abort_flag, a.err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t xs = smem_u32(smem + L.off_x + st * L.x_stage);
-                    const uint32_t acol = tmem_base + uint32_t(a.dcols) + 64u * sa;
+                const uint32_t xs = smem_u32(smem + L.off_x + st * L.x_stage);
+                const uint32_t acol = tmem_base + uint32_t(a.dcols) + 64u * sa;
+                const uint64_t bdesc0 = tc_sdesc_sw128(xs);
+                const uint64_t bdesc1 = tc_sdesc_sw128(xs + x_bytes);
+                if (elect_one()) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint64_t bdesc = tc_sdesc_sw128(xs + h * x_bytes);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            tc_mma_ts(dcol, acol + 32u * h + 8u * j, bdesc + 2u * j,
+                            tc_mma_ts(dcol, acol + 32u * h + 8u * j, (h ? bdesc1 : bdesc0) + 2u * j,
                                       idesc, (grp > g0 || h > 0 || j > 0) ? 1u : 0u);
                     }
                     tc_commit(xempty_bar(st));
                     tc_commit(aempty_bar(sa));
-                    if (++st == S) { st = 0; xph ^= 1; }
-                    if (++sa == SA) { sa = 0; aph ^= 1; }
                 }
-                if (!ok) break;
-                tc_commit(dfull_bar(db));
-                ++tiles;
+                __syncwarp();
+                if (++st == SX) { st = 0; xph ^= 1; }
+                if (++sa == SA) { sa = 0; aph ^= 1; }
             }
-            // Every MMA this thread issued has completed before TMEM is freed.
-            tc_commit(done_bar);
-            drain_wait(done_bar, 0);
+            if (!ok) break;
+            if (elect_one()) tc_commit(dfull_bar(db));
+            __syncwarp();
+            ++tiles;
         }
-    } else if (warp < kTcDequantWarps) {
+        // Every MMA issued has completed before TMEM is freed.
+        if (elect_one()) tc_commit(done_bar);
+        __syncwarp();
+        drain_wait(done_bar, 0);
+    } else if (warp < R::kDequant) {
         // Dequantisers (and, without a separate epilogue, the epilogue).
-        const int sub = warp & 3;                   // TMEM sub-partition of this warp
-        const int half = warp >> 2;                 // which 16 lanes of the sub-partition
+        // q counts the CTA's groups in ring order; this warp's team takes
+        // those with q % kTeams == team, and its ring slots and phase
+        // parities advance kTeams positions per group it takes.
+        const int team = warp / kTcTeamWarps;
+        const int tw = warp % kTcTeamWarps;
+        const int sub = tw & 3;                     // TMEM sub-partition of this warp (warp % 4)
+        const int half = tw >> 2;                   // which 16 lanes of the sub-partition
         const int block = 2 * sub + half;           // 16-row block of the tile
         const int g = lane >> 2;
         const uint32_t lane_base = uint32_t(32 * sub + 16 * half) << 16;
         unsigned char *epi = smem + L.off_epi + warp * kEpiBytesPerWarp;
-        int st = 0, sa = 0, qa = 0, tiles = 0;
+        int q = 0, tiles = 0;
+        int st = team, sa = team;       // ring slots of this warp's next group (kTeams <= 2 <= SW, SA)
         uint32_t wph = 0;               // parity of the W-ring phase to wait for
         uint32_t eph = 1;               // parity of the A-ring empty phase (first lap: none)
-        const int S = SW;
+        auto advance = [](int &slot, uint32_t &par, int n) {
+            slot += R::kTeams;
+            if (slot >= n) {
+                slot -= n;
+                par ^= 1u;
+            }
+        };
         // Scales of the next group (possibly in the next tile), loaded one group
         // ahead so the dequantisers never wait on them.
         ScaleRaw<kSub> n0 = {}, n1 = {};
@@ -598,7 +620,8 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
             const uint16_t *sg = a.S + (unsigned long long)ti.group * a.s_group_stride;
             const uint8_t *zg = kZp ? Z + (unsigned long long)ti.group * a.s_group_stride : nullptr;
             bool ok = true;
-            for (int grp = g0; grp < g1; ++grp) {
+            for (int grp = g0; grp < g1; ++grp, ++q) {
+                if (R::kTeams > 1 && q % R::kTeams != team) continue;   // the other team's group
                 ScaleRaw<kSub> s0, s1;              // raw; paired after the stage wait
                 uint32_t z0 = 0, z1 = 0;
                 if (have_next) {
@@ -615,17 +638,22 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                     }
                 }
                 have_next = false;
-                if (grp + 1 < g1) {
-                    n0 = scales_raw<kSub>(sg, r0, a.N, size_t(r0) * n_sg + size_t(grp + 1) * kSub, svec);
-                    n1 = scales_raw<kSub>(sg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(grp + 1) * kSub, svec);
+                // This warp's next group: grp + kTeams in this tile, else the
+                // next tile's group number off (0 or 1) if it has one.
+                const int gnext = grp + R::kTeams;
+                const int off = gnext - g1;
+                const int nx_g1 = nx_ok ? min(n_groups, (nx.slice + 1) * a.gps) : 0;
+                if (gnext < g1) {
+                    n0 = scales_raw<kSub>(sg, r0, a.N, size_t(r0) * n_sg + size_t(gnext) * kSub, svec);
+                    n1 = scales_raw<kSub>(sg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(gnext) * kSub, svec);
                     if (kZp) {
-                        nz0 = zeros_raw<kSub>(zg, r0, a.N, size_t(r0) * n_sg + size_t(grp + 1) * kSub, zvec);
-                        nz1 = zeros_raw<kSub>(zg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(grp + 1) * kSub, zvec);
+                        nz0 = zeros_raw<kSub>(zg, r0, a.N, size_t(r0) * n_sg + size_t(gnext) * kSub, zvec);
+                        nz1 = zeros_raw<kSub>(zg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(gnext) * kSub, zvec);
                     }
                     have_next = true;
-                } else if (nx_ok) {
+                } else if (nx_ok && nx.slice * a.gps + off < nx_g1) {
                     const int rn = nx.ft * kTileRows + 16 * block + g;
-                    const int gn = nx.slice * a.gps;
+                    const int gn = nx.slice * a.gps + off;
                     const uint16_t *sn = a.S + (unsigned long long)nx.group * a.s_group_stride;
                     n0 = scales_raw<kSub>(sn, rn, a.N, size_t(rn) * n_sg + size_t(gn) * kSub, svec);
                     n1 = scales_raw<kSub>(sn, rn + 8, a.N, size_t(rn + 8) * n_sg + size_t(gn) * kSub, svec);
@@ -683,9 +711,9 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                     frag[4 * j + 2] = bf16x2_mul(minus136(magic_pair(wv[j] >> 4)), q1);
                     frag[4 * j + 3] = bf16x2_mul(minus136(magic_pair(wv[j] >> 12)), q1);
                 }
-                if (++st == S) { st = 0; wph ^= 1; }
+                advance(st, wph, SW);
                 flush();
-                if (qa >= SA && !__all_sync(0xffffffffu, mbar_wait(aempty_bar(sa), eph, abort_flag, a.err))) {
+                if (q >= SA && !__all_sync(0xffffffffu, mbar_wait(aempty_bar(sa), eph, abort_flag, a.err))) {
                     ok = false;
                     break;
                 }
@@ -693,18 +721,17 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                 tc_st_16x256b_x8(tmem_base + lane_base + uint32_t(a.dcols) + 64u * sa, frag);
                 pending = true;
                 sa_pend = sa;
-                ++qa;
-                if (++sa == SA) { sa = 0; eph ^= 1; }
+                advance(sa, eph, SA);
             }
             flush();
             if (!ok) break;
             if (kSep) continue;
-            // Epilogue: warp (sub, half) reads lanes 32 sub .. 32 sub + 31 (its
-            // weight rows) for every other 32-token column block.
+            // Epilogue: warp w reads lanes 32 (w % 4) .. + 31 (its weight rows)
+            // for the 32-token column blocks w / 4, w / 4 + kDequant / 4, ...
             if (!__all_sync(0xffffffffu, mbar_wait(dfull_bar(0), tiles & 1, abort_flag, a.err))) break;
             tc_fence_after();
             const int fb = ti.ft * kTileRows + 32 * sub;           // first weight row of the warp
-            for (int cb = half; cb * 32 < a.bt; cb += 2) {
+            for (int cb = warp >> 2; cb * 32 < a.bt; cb += R::kDequant / 4) {
                 uint32_t v[32];
                 tc_ld_32x32b_x32(tmem_base + (uint32_t(32 * sub) << 16) + kTcDCol + 32u * cb, v);
                 tc_wait_ld();
@@ -720,7 +747,7 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
         // 32 weight rows) for every 32-token column block of the tile's
         // accumulator, alternating between the two accumulators.
         const int sub = warp & 3;
-        unsigned char *epi = smem + L.off_epi + (warp - kTcEpiWarp0) * kEpiBytesPerWarp;
+        unsigned char *epi = smem + L.off_epi + (warp - R::kEpi0) * kEpiBytesPerWarp;
         int tiles = 0;
         TileInfo ti;
         for (int id = blockIdx.x; tc_tile<kBatched>(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
@@ -746,14 +773,14 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kTcMmaWarp) tc_dealloc(tmem_base, uint32_t(a.tmem_cols));
-    if (*abort_flag && warp < kTcDequantWarps) {
+    if (warp == R::kMma) tc_dealloc(tmem_base, uint32_t(a.tmem_cols));
+    if (*abort_flag && warp < R::kDequant) {
         // A wait ran out (the error word holds kErrWaitTimeout): every output
         // of this CTA's tiles becomes NaN, so an incomplete result is never a
         // plausible number.
         TileInfo ti;
         for (int id = blockIdx.x; tc_tile<kBatched>(a, tab_tiles, tab_rows, id, ti); id += gridDim.x) {
-            for (int e = threadIdx.x; e < ti.rows * kTileRows; e += kTcDequantWarps * 32) {
+            for (int e = threadIdx.x; e < ti.rows * kTileRows; e += R::kDequant * 32) {
                 const int m = ti.x_row0 + e / kTileRows;
                 const int f = ti.ft * kTileRows + e % kTileRows;
                 if (f >= a.N) continue;
@@ -766,13 +793,13 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
 }
 
 template <bool kSplit, bool kSep, bool kBatched, int kSub>
-__global__ void __launch_bounds__(kSep ? kTcThreadsSep : kTcThreads, kSep ? 1 : 2)
+__global__ void __launch_bounds__(TcRoles<kSep>::kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     tc_gemm_body<kSplit, kSep, kBatched, kSub, false>(tmap_x, a, nullptr);
 }
 
 template <bool kSplit, bool kSep, bool kBatched, int kSub>
-__global__ void __launch_bounds__(kSep ? kTcThreadsSep : kTcThreads, kSep ? 1 : 2)
+__global__ void __launch_bounds__(TcRoles<kSep>::kThreads, 1)
 tc_gemm_zp_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a,
                   const uint8_t *__restrict__ Z) {
     tc_gemm_body<kSplit, kSep, kBatched, kSub, true>(tmap_x, a, Z);
@@ -835,7 +862,7 @@ int tensor_tmem_cols(int bt, int occupancy, bool sep) {
 
 size_t tensor_smem_bytes(int bt, int x_stages, int w_stages, int occupancy, int num_groups, bool sep) {
     return size_t(tc_smem_layout(bt, x_stages, w_stages, tensor_a_stages(bt, occupancy, sep),
-                                 num_groups)
+                                 num_groups, sep)
                       .total) +
            1024;  // + alignment slack
 }
@@ -873,7 +900,7 @@ cudaError_t launch_tc_sub(const TensorPlan &p, const CUtensorMap &tmap, const Tc
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.ctas);
-    cfg.blockDim = dim3(p.sep_epilogue ? kTcThreadsSep : kTcThreads);
+    cfg.blockDim = dim3(sep ? TcRoles<true>::kThreads : TcRoles<false>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -893,8 +920,7 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
                           int batch_rows, const uint8_t *Z) {
     if (p.tile_tokens < 32 || p.tile_tokens > 256 || p.tile_tokens % 32 || p.x_stages < 2 ||
         p.w_stages < 2 ||
-        p.ctas < 1 || num_groups < 1 || num_groups > kMaxGroups || p.occupancy < 1 ||
-        p.occupancy > 2 || (p.sep_epilogue && p.occupancy != 1) ||
+        p.ctas < 1 || num_groups < 1 || num_groups > kMaxGroups || p.occupancy != 1 ||
         (p.sub != 1 && p.sub != 2 && p.sub != 4) ||
         tensor_a_stages(p.tile_tokens, p.occupancy, p.sep_epilogue) < 2)
         return cudaErrorInvalidValue;
