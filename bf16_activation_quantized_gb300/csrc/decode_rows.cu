@@ -13,7 +13,10 @@
 //
 // Consumer warp w takes block w % B and, in every stage, groups 2 (w / B) and
 // 2 (w / B) + 1 of the stage (P = 8 / B warps share a block, each covering a
-// quarter, half ... of K in interleaved pairs of groups).  Per group it builds
+// quarter, half ... of K in interleaved pairs of groups), for all M tokens:
+// MT = ceil(M / 8) token octets (up to two), each dequantised A fragment
+// feeding one m16n8k16 per octet, so the weights are streamed once.  Per
+// group it builds
 // the bf16 A fragments 128 + code with one LOP3 per register and removes 136
 // with one exact bf16x2 FMA (the magic-constant trick of "[ROCm][Kernel]
 // W4A16 skinny GEMM: hand-asm kernel for gfx1151", section 1), so
@@ -39,6 +42,12 @@ constexpr int kRowsThreads = (kRowsWarps + 1) * 32;   // + the producer warp
 constexpr int kRowsGW = 16 / kRowsWarps;              // groups per warp per stage
 constexpr int kRowsStageW = 16384;                    // packed weight bytes per stage
 constexpr int kRowsMaxStages = 8;
+// Two token octets at most.  Measured on GB300: with four (32 tokens, 128
+// rows per CTA, three 33 KB stages) a stage takes ~1.3 us -- the X fragments
+// (as many bytes per stage as the weights) hold each stage until its MMAs are
+// done, and the ring then keeps too few weight bytes in flight -- slower than
+// the tensor arm.
+constexpr int kRowsMaxTokens = 16;
 
 // c += A . B for one m16n8k16 bf16 tile, fp32 accumulators in place.
 __device__ __forceinline__ void mma_bf16_acc(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -94,8 +103,8 @@ __device__ __forceinline__ void rows_consumer_bar() {
 // wmap: the packed weights as uint32 [chunk rows][8 blocks][128] with a box of
 // {128, B, 2 SG}; wmap_tail: the same with a box of {128, B, 2 (G % SG)} for a
 // last stage of fewer groups (unused when SG divides G).  Batch entry b's
-// chunk rows follow entry b - 1's.
-template <int B>
+// chunk rows follow entry b - 1's.  MT: token octets (M <= 8 MT).
+template <int B, int MT>
 __global__ void __launch_bounds__(kRowsThreads, 2)
 decode_rows_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap wmap_tail,
                    const uint16_t *__restrict__ X, const uint16_t *__restrict__ S,
@@ -234,8 +243,15 @@ decode_rows_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_consta
         rows_consumer_bar();
     }
     const uint16_t *scol = s_scale + b * 16 + g;               // row g of this warp's block, group 0
-    const int xrow = min(g, M - 1);                            // absent tokens read the last row
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // Octet o's token g; absent tokens read the last row (their sums are dropped).
+    int xrow[MT];
+#pragma unroll
+    for (int o = 0; o < MT; ++o) xrow[o] = min(8 * o + g, M - 1);
+    float acc[MT][4];
+#pragma unroll
+    for (int o = 0; o < MT; ++o)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[o][r] = 0.f;
     bool alive = true;
     int slot = 0;
     uint32_t fpar = 0;       // parity of the slot's full phase
@@ -248,14 +264,16 @@ decode_rows_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_consta
         const unsigned char *st = ring + slot * L.stage_bytes;
         const int ng = min(SG, G - q * SG);
         // This warp's two groups of the stage: packed words (16 B of each of
-        // the group's two 64-column chunks) and the X fragments of its 8 k16
-        // steps (token g, columns 16 j + 4 t .. + 3: the k slots 2t, 2t+1,
-        // 2t+8, 2t+9 of the packed word j).  A group past the last (in a
-        // short final stage) is read and multiplied all the same -- its bytes
-        // lie inside the stage -- and only its sum is dropped, so the loads and
-        // MMAs carry no branches and interleave freely.
+        // the group's two 64-column chunks) and, per octet, the X fragments of
+        // its 8 k16 steps (token 8 o + g, columns 16 j + 4 t .. + 3: the k
+        // slots 2t, 2t+1, 2t+8, 2t+9 of the packed word j).  A group past the
+        // last (in a short final stage) is read and multiplied all the same --
+        // its bytes lie inside the stage -- and only its sum is dropped, so
+        // the loads and MMAs carry no branches and interleave freely.  With
+        // one octet the X fragments are loaded up front and the stage is
+        // released before the MMAs; with more they are loaded per k16 step
+        // (registers) and the stage is released after them.
         uint32_t wv[GW][8];
-        uint2 xf[GW][8];
 #pragma unroll
         for (int h = 0; h < GW; ++h) {
             const int gg = GW * kp + h;
@@ -263,18 +281,28 @@ decode_rows_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_consta
             const uint4 wb = *reinterpret_cast<const uint4 *>(st + ((2 * gg + 1) * B + b) * 512 + lane * 16);
             wv[h][0] = wa.x; wv[h][1] = wa.y; wv[h][2] = wa.z; wv[h][3] = wa.w;
             wv[h][4] = wb.x; wv[h][5] = wb.y; wv[h][6] = wb.z; wv[h][7] = wb.w;
-            const unsigned char *xs = st + kRowsStageW + xrow * L.x_stride + gg * kGroup * 2 + 8 * t;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) xf[h][j] = *reinterpret_cast<const uint2 *>(xs + 32 * j);
         }
-        // Operands are in registers: release the stage.
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-        float c[GW][4];
+        auto xfrag = [&](int o, int h, int j) {
+            return *reinterpret_cast<const uint2 *>(st + kRowsStageW + xrow[o] * L.x_stride +
+                                                    (GW * kp + h) * kGroup * 2 + 8 * t + 32 * j);
+        };
+        uint2 xf1[GW][8];             // MT == 1 only
+        if constexpr (MT == 1) {
+#pragma unroll
+            for (int h = 0; h < GW; ++h)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) xf1[h][j] = xfrag(0, h, j);
+            // Operands are in registers: release the stage.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+        }
+        float c[GW][MT][4];
 #pragma unroll
         for (int h = 0; h < GW; ++h)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) c[h][r] = 0.f;
+            for (int o = 0; o < MT; ++o)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) c[h][o][r] = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
 #pragma unroll
@@ -284,8 +312,17 @@ decode_rows_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_consta
                 // minus136: one exact bf16x2 FMA, (128 + code) * 1 - 136.
                 const uint32_t a[4] = {minus136(magic_pair(w)), minus136(magic_pair(w >> 4)),
                                        minus136(magic_pair(w >> 8)), minus136(magic_pair(w >> 12))};
-                mma_bf16_acc(c[h], a, xf[h][j].x, xf[h][j].y);
+#pragma unroll
+                for (int o = 0; o < MT; ++o) {
+                    const uint2 x = MT == 1 ? xf1[h][j] : xfrag(o, h, j);
+                    mma_bf16_acc(c[h][o], a, x.x, x.y);
+                }
             }
+        }
+        if constexpr (MT > 1) {
+            // The X fragments have been read: release the stage.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * slot);
         }
 #pragma unroll
         for (int h = 0; h < GW; ++h) {
@@ -293,10 +330,13 @@ decode_rows_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_consta
             if (GW * kp + h >= ng) continue;
             const float s0 = bf16_bits_to_f32(scol[gi * 16 * B]);
             const float s1 = bf16_bits_to_f32(scol[gi * 16 * B + 8]);
-            acc[0] = fmaf(s0, c[h][0], acc[0]);
-            acc[1] = fmaf(s0, c[h][1], acc[1]);
-            acc[2] = fmaf(s1, c[h][2], acc[2]);
-            acc[3] = fmaf(s1, c[h][3], acc[3]);
+#pragma unroll
+            for (int o = 0; o < MT; ++o) {
+                acc[o][0] = fmaf(s0, c[h][o][0], acc[o][0]);
+                acc[o][1] = fmaf(s0, c[h][o][1], acc[o][1]);
+                acc[o][2] = fmaf(s1, c[h][o][2], acc[o][2]);
+                acc[o][3] = fmaf(s1, c[h][o][3], acc[o][3]);
+            }
         }
         if (++slot == NS) {
             slot = 0;
@@ -304,44 +344,57 @@ decode_rows_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_consta
         }
     }
     // Add the K-parts in ascending order through ring stage 0 (every stage
-    // has been consumed, so the ring is idle); part 0's warps write Y.
+    // has been consumed, so the ring is idle; (8 - B) MT x 512 bytes fit in a
+    // stage); part 0's warps write Y.
     rows_consumer_bar();
     float4 *red = reinterpret_cast<float4 *>(ring);
-    if (kp > 0) red[((kp - 1) * B + b) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    if (kp > 0) {
+#pragma unroll
+        for (int o = 0; o < MT; ++o)
+            red[(((kp - 1) * B + b) * MT + o) * 32 + lane] = make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
+    }
     rows_consumer_bar();
     if (kp > 0) return;
 #pragma unroll
     for (int p = 1; p < P; ++p) {
-        const float4 v = red[((p - 1) * B + b) * 32 + lane];
-        acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
+#pragma unroll
+        for (int o = 0; o < MT; ++o) {
+            const float4 v = red[(((p - 1) * B + b) * MT + o) * 32 + lane];
+            acc[o][0] += v.x; acc[o][1] += v.y; acc[o][2] += v.z; acc[o][3] += v.w;
+        }
     }
     // A wait of this CTA ran out (every consumer warp has passed the barriers
     // above, so the flag covers them all): the outputs become NaN, never a
     // plausible partial result; the error word holds kErrWaitTimeout.
     if (!alive || *abort_flag) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) acc[r] = __int_as_float(0x7fc00000);
+        for (int o = 0; o < MT; ++o)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[o][r] = __int_as_float(0x7fc00000);
     }
     // Y may be read by the previous kernel on the stream: write it only after
     // that kernel has completed.
     pdl_wait();
     const int f0 = row0 + b * 16 + g;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int m = 2 * t + (r & 1);
-        const int f = f0 + ((r < 2) ? 0 : 8);
-        if (m < M && f < N) Y[size_t(m) * N + f] = f32_to_bf16_rn(acc[r]);
+    for (int o = 0; o < MT; ++o) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int m = 8 * o + 2 * t + (r & 1);
+            const int f = f0 + ((r < 2) ? 0 : 8);
+            if (m < M && f < N) Y[size_t(m) * N + f] = f32_to_bf16_rn(acc[o][r]);
+        }
     }
 }
 
-template <int B>
+template <int B, int MT>
 cudaError_t launch_rows_t(int ctas, int batch, const uint16_t *X, const uint8_t *Wp, const uint16_t *S,
                           uint16_t *Y, bool resident, int M, int N, int K, cudaStream_t s) {
     const int G = K / kGroup;
     const int KC = K / kChunkK;
     const int n_tiles = (N + kTileRows - 1) / kTileRows;
     const RowsSmem L = rows_smem_layout(B, M, G, kDecodeMaxSmem);
-    auto kern = decode_rows_kernel<B>;
+    auto kern = decode_rows_kernel<B, MT>;
     {
         static std::atomic<unsigned long long> opted{0};
         int dev = 0;
@@ -390,9 +443,9 @@ cudaError_t launch_rows_t(int ctas, int batch, const uint16_t *X, const uint8_t 
 }  // namespace
 
 bool decode_wk_fits(int M, int K, int B) {
-    if (M < 1 || M > 8 || (B != 1 && B != 2 && B != 4 && B != 8)) return false;
+    if (M < 1 || M > kRowsMaxTokens || (B != 1 && B != 2 && B != 4 && B != 8)) return false;
     const int G = K / kGroup;
-    if (B * G > 256) return false;                     // the CTA's scales in shared memory
+    if (B * G > 1024) return false;                    // the CTA's scales in shared memory
     const RowsSmem L = rows_smem_layout(B, M, G, kDecodeMaxSmem);
     return L.stages >= 3;
 }
@@ -401,13 +454,19 @@ cudaError_t launch_decode_wk(int B, int ctas, int batch, const uint16_t *X, cons
                              const uint16_t *S, uint16_t *Y, bool resident, int M, int N, int K,
                              cudaStream_t s) {
     if (!decode_wk_fits(M, K, B) || ctas < 1 || batch < 1 || batch > 65535) return cudaErrorInvalidValue;
+    // Token octets: 1 or 2.
+#define W4A16_ROWS_CASE(BB)                                                              \
+    case BB:                                                                             \
+        return M <= 8 ? launch_rows_t<BB, 1>(ctas, batch, X, Wp, S, Y, resident, M, N, K, s) \
+                      : launch_rows_t<BB, 2>(ctas, batch, X, Wp, S, Y, resident, M, N, K, s);
     switch (B) {
-        case 1: return launch_rows_t<1>(ctas, batch, X, Wp, S, Y, resident, M, N, K, s);
-        case 2: return launch_rows_t<2>(ctas, batch, X, Wp, S, Y, resident, M, N, K, s);
-        case 4: return launch_rows_t<4>(ctas, batch, X, Wp, S, Y, resident, M, N, K, s);
-        case 8: return launch_rows_t<8>(ctas, batch, X, Wp, S, Y, resident, M, N, K, s);
+        W4A16_ROWS_CASE(1)
+        W4A16_ROWS_CASE(2)
+        W4A16_ROWS_CASE(4)
+        W4A16_ROWS_CASE(8)
         default: return cudaErrorInvalidValue;
     }
+#undef W4A16_ROWS_CASE
 }
 
 }  // namespace w4a16

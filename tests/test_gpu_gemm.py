@@ -370,7 +370,10 @@ def test_resident_weights_chain_reads_x_after_the_previous_call():
 
 # ------------------------------------------------------ whole-K decode kernel
 WHOLE_K = [(1, 8192, 8192), (1, 17408, 5120), (1, 19456, 2560), (1, 2560, 9728), (2, 8192, 8192),
-           (4, 4096, 4096), (8, 2048, 2048), (3, 300, 640), (1, 7, 256), (5, 129, 384), (1, 256, 128)]
+           (4, 4096, 4096), (8, 2048, 2048), (3, 300, 640), (1, 7, 256), (5, 129, 384), (1, 256, 128),
+           # two token octets (9..16 tokens), ragged octets and rows
+           (9, 2048, 2048), (16, 19456, 2560), (16, 2560, 9728), (13, 300, 1024), (16, 4096, 4096),
+           (11, 129, 384)]
 
 
 @pytest.mark.parametrize("M,N,K", WHOLE_K)
@@ -387,9 +390,9 @@ def test_whole_k_kernel_full_output(M, N, K):
 
 
 def test_whole_k_kernel_refuses_what_it_cannot_stage():
-    # More than 8 tokens, or a CTA's scales beyond its shared memory (one
-    # 16-row block of K / 128 > 256 groups), are refused when forced.
-    for M, N, K in ((16, 2560, 9728), (9, 256, 512), (1, 256, 65536)):
+    # More than 16 tokens, or X columns and scales that leave fewer than three
+    # ring stages in a CTA's shared memory, are refused when forced.
+    for M, N, K in ((17, 256, 512), (16, 256, 131072), (1, 256, 262144)):
         with pytest.raises(w4.W4A16Error):
             w4.plan(M, N, K, arm="decode", decode_kernel="whole_k")
     assert not w4.plan(1, 8192, 8192, decode_kernel="k_slices")["whole_k"]

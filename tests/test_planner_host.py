@@ -159,13 +159,21 @@ def test_forced_arms(L):
 
 
 def test_whole_k_refused_where_it_does_not_fit(L):
-    # The whole-K kernel takes up to 8 tokens (their X columns travel in each
-    # ring stage) and keeps a CTA's scales in shared memory (K / 128 <= 256
-    # groups for one 16-row block).
+    # The whole-K kernel takes up to 16 tokens (two octets; their X columns
+    # travel in each ring stage, which must hold at least three stages next
+    # to the CTA's scales in shared memory).
     assert plan(L, 2, 2560, 8192, flags=2)[1].whole_k
     assert plan(L, 8, 2560, 8192, flags=2)[1].whole_k
-    assert plan(L, 9, 256, 512, flags=2)[0] == UNSUPPORTED
-    assert plan(L, 1, 256, 65536, flags=2)[0] == UNSUPPORTED
+    assert plan(L, 16, 2560, 9728, flags=2)[1].whole_k
+    assert plan(L, 17, 256, 512, flags=2)[0] == UNSUPPORTED
+    assert plan(L, 16, 256, 131072, flags=2)[0] == UNSUPPORTED     # X and scales: < 3 stages
+    assert plan(L, 1, 256, 262144, flags=2)[0] == UNSUPPORTED      # the scales alone
+
+
+def test_gate_up_at_16_tokens_takes_the_whole_k_kernel(L):
+    # Two token octets per dequantised fragment: 304 CTAs of 64 rows.
+    st, info = plan(L, 16, 19456, 2560)
+    assert st == OK and info.arm == 1 and info.whole_k and info.ctas == 2 * SMS
 
 
 def test_python_plan_for_sms_needs_no_gpu():

@@ -71,7 +71,7 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     # scratch than the array holds.
     shape = None
     for M, N, K in ((16, 19456, 2560), (8, 19456, 2560), (16, 17408, 5120), (16, 8192, 8192),
-                    (512, 7168, 8192), (16, 2560, 9728)):
+                    (512, 7168, 8192), (16, 2560, 9728), (128, 2560, 9728), (16, 8192, 16384)):
         assert L.w4a16_workspace_bytes(M, N, K, 128, ctypes.byref(nb)) == 0
         if nb.value > SCRATCH_MAX:
             shape = (M, N, K)
