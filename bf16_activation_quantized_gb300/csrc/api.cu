@@ -335,7 +335,7 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
 
 // batch: independent products of this shape in one launch (1: a plain call).
 // sub: scale groups per 128-wide block (128 / group_size).  W4A16_FLAG_ZERO_POINTS
-// in opts plans the zero-point kernels (plain products only).
+// in opts plans the zero-point kernels.
 // sms > 0: plan for a device with that many SMs instead of querying the
 // current one (host-only planning).
 w4a16_status plan_call(int M, int N, int K, const w4a16_options *opts, Plan *p, int batch = 1,

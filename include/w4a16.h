@@ -78,8 +78,9 @@ enum {
      * dispatcher chooses).  WHOLE_K: the kernel in which every CTA covers all
      * of K for a few 16-row blocks of W, its warps split K among themselves
      * and add their partial sums in shared memory, so K is never split across
-     * CTAs (no workspace, no reduce kernel); it takes up to 8 tokens whose X
-     * rows fit its shared-memory staging (M * K <= 16384), with 128-wide scale
+     * CTAs (no workspace, no reduce kernel); it takes up to 16 tokens whose X
+     * rows fit its shared-memory ring next to the CTA's scales (at least three
+     * stages of 16 KB of weights and their X columns), with 128-wide scale
      * groups; otherwise the call returns W4A16_ERR_UNSUPPORTED.  K_SLICES:
      * never that kernel.  Setting
      * both is W4A16_ERR_INVALID_ARG. */
