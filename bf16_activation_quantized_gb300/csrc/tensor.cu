@@ -617,8 +617,18 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
             const int g0 = ti.slice * a.gps;
             const int g1 = min(n_groups, (ti.slice + 1) * a.gps);
             const int r0 = ti.ft * kTileRows + 16 * block + g;     // weight rows r0, r0 + 8
-            const uint16_t *sg = a.S + (unsigned long long)ti.group * a.s_group_stride;
-            const uint8_t *zg = kZp ? Z + (unsigned long long)ti.group * a.s_group_stride : nullptr;
+            // Rows r0 and r0 + 8 of this tile's scales (and zero points), and
+            // of the next tile's, once per tile: a group's loads are then a
+            // constant offset from them.
+            const size_t so0 = (unsigned long long)ti.group * a.s_group_stride + size_t(r0) * n_sg;
+            const size_t so1 = so0 + size_t(8) * n_sg;
+            const uint16_t *sg0 = a.S + so0, *sg1 = a.S + so1;
+            const uint8_t *zg0 = kZp ? Z + so0 : nullptr, *zg1 = kZp ? Z + so1 : nullptr;
+            const int rn = nx.ft * kTileRows + 16 * block + g;
+            const int gn0 = nx.slice * a.gps;
+            const int nx_g1 = nx_ok ? min(n_groups, gn0 + a.gps) : 0;
+            const size_t no0 = nx_ok ? (unsigned long long)nx.group * a.s_group_stride + size_t(rn) * n_sg : 0;
+            const size_t no1 = no0 + size_t(8) * n_sg;
             bool ok = true;
             for (int grp = g0; grp < g1; ++grp, ++q) {
                 if (R::kTeams > 1 && q % R::kTeams != team) continue;   // the other team's group
@@ -630,39 +640,33 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                     z0 = nz0;
                     z1 = nz1;
                 } else {
-                    s0 = scales_raw<kSub>(sg, r0, a.N, size_t(r0) * n_sg + size_t(grp) * kSub, svec);
-                    s1 = scales_raw<kSub>(sg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(grp) * kSub, svec);
+                    s0 = scales_raw<kSub>(sg0, r0, a.N, size_t(grp) * kSub, svec);
+                    s1 = scales_raw<kSub>(sg1, r0 + 8, a.N, size_t(grp) * kSub, svec);
                     if (kZp) {
-                        z0 = zeros_raw<kSub>(zg, r0, a.N, size_t(r0) * n_sg + size_t(grp) * kSub, zvec);
-                        z1 = zeros_raw<kSub>(zg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(grp) * kSub, zvec);
+                        z0 = zeros_raw<kSub>(zg0, r0, a.N, size_t(grp) * kSub, zvec);
+                        z1 = zeros_raw<kSub>(zg1, r0 + 8, a.N, size_t(grp) * kSub, zvec);
                     }
                 }
-                have_next = false;
                 // This warp's next group: grp + kTeams in this tile, else the
-                // next tile's group number off (0 or 1) if it has one.
+                // next tile's group number gn0 + (grp + kTeams - g1) (0 or 1
+                // past its first) if it has one.
                 const int gnext = grp + R::kTeams;
-                const int off = gnext - g1;
-                const int nx_g1 = nx_ok ? min(n_groups, (nx.slice + 1) * a.gps) : 0;
+                have_next = gnext < g1 || (nx_ok && gn0 + (gnext - g1) < nx_g1);
                 if (gnext < g1) {
-                    n0 = scales_raw<kSub>(sg, r0, a.N, size_t(r0) * n_sg + size_t(gnext) * kSub, svec);
-                    n1 = scales_raw<kSub>(sg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(gnext) * kSub, svec);
+                    n0 = scales_raw<kSub>(sg0, r0, a.N, size_t(gnext) * kSub, svec);
+                    n1 = scales_raw<kSub>(sg1, r0 + 8, a.N, size_t(gnext) * kSub, svec);
                     if (kZp) {
-                        nz0 = zeros_raw<kSub>(zg, r0, a.N, size_t(r0) * n_sg + size_t(gnext) * kSub, zvec);
-                        nz1 = zeros_raw<kSub>(zg, r0 + 8, a.N, size_t(r0 + 8) * n_sg + size_t(gnext) * kSub, zvec);
+                        nz0 = zeros_raw<kSub>(zg0, r0, a.N, size_t(gnext) * kSub, zvec);
+                        nz1 = zeros_raw<kSub>(zg1, r0 + 8, a.N, size_t(gnext) * kSub, zvec);
                     }
-                    have_next = true;
-                } else if (nx_ok && nx.slice * a.gps + off < nx_g1) {
-                    const int rn = nx.ft * kTileRows + 16 * block + g;
-                    const int gn = nx.slice * a.gps + off;
-                    const uint16_t *sn = a.S + (unsigned long long)nx.group * a.s_group_stride;
-                    n0 = scales_raw<kSub>(sn, rn, a.N, size_t(rn) * n_sg + size_t(gn) * kSub, svec);
-                    n1 = scales_raw<kSub>(sn, rn + 8, a.N, size_t(rn + 8) * n_sg + size_t(gn) * kSub, svec);
+                } else if (have_next) {
+                    const size_t gi = size_t(gn0 + (gnext - g1)) * kSub;
+                    n0 = scales_raw<kSub>(a.S + no0, rn, a.N, gi, svec);
+                    n1 = scales_raw<kSub>(a.S + no1, rn + 8, a.N, gi, svec);
                     if (kZp) {
-                        const uint8_t *zn = Z + (unsigned long long)nx.group * a.s_group_stride;
-                        nz0 = zeros_raw<kSub>(zn, rn, a.N, size_t(rn) * n_sg + size_t(gn) * kSub, zvec);
-                        nz1 = zeros_raw<kSub>(zn, rn + 8, a.N, size_t(rn + 8) * n_sg + size_t(gn) * kSub, zvec);
+                        nz0 = zeros_raw<kSub>(Z + no0, rn, a.N, gi, zvec);
+                        nz1 = zeros_raw<kSub>(Z + no1, rn + 8, a.N, gi, zvec);
                     }
-                    have_next = true;
                 }
                 // Warp-uniform outcomes below: tcgen05.st needs every lane.
                 if (!__all_sync(0xffffffffu, mbar_wait(wfull_bar(st), wph, abort_flag, a.err))) {
