@@ -214,9 +214,9 @@ void plan_decode(int M, int N, int K, int sms, int forced_split, int wk, int bat
 // its tile count times (K blocks x that + a fixed per-tile cost), plus the
 // split-K round trip.
 // Ring depths for the CTA's shared-memory budget: the deepest X ring of 4, 3
-// or 2 stages that still leaves at least 3 W stages, then as many W stages
-// (8 KB each, up to kTensorMaxWStages) as fit.  Returns false if even 2 + 2
-// does not fit.
+// or 2 stages that still leaves at least 4 W stages (one per dequantiser
+// team), then as many W stages (8 KB each, up to kTensorMaxWStages) as fit.
+// Returns false if even 2 + 4 does not fit.
 bool tensor_rings(int bt, int num_groups, int occupancy, bool sep, int *x_stages, int *w_stages) {
     const size_t budget = size_t(tensor_smem_budget(occupancy));
     const size_t fixed = tensor_smem_bytes(bt, 0, 0, occupancy, num_groups, sep);
@@ -228,7 +228,7 @@ bool tensor_rings(int bt, int num_groups, int occupancy, bool sep, int *x_stages
         if (sx * x_stage > avail) continue;
         size_t sw = (avail - sx * x_stage) / w_stage;
         if (sw > size_t(kTensorMaxWStages)) sw = kTensorMaxWStages;
-        if (sw >= 3 || (sx == 2 && sw >= 2)) {
+        if (sw >= 4) {
             *x_stages = sx;
             *w_stages = int(sw);
             return true;

@@ -45,19 +45,23 @@ namespace w4a16 {
 
 namespace {
 
-// Warp roles (one CTA per SM).  Plain form: 16 dequantisers in two teams of
-// 8, team t taking the CTA's groups t, t + 2, t + 4, ... (the two warps of a
-// team on one SM sub-partition work on one group while the other team's two
-// work on the next, so one pair's waits overlap the other's arithmetic),
-// then the X producer, the W producer and the MMA warp.  With a separate
-// epilogue: one team of 8, the two producers, the MMA warp and 4 epilogue
-// warps that drain one TMEM accumulator while the dequantisers and the MMA
-// go on with the next tile in the other.
-constexpr int kTcTeamWarps = 8;
+// Warp roles (one CTA per SM).  A team is four dequantisers, one per TMEM
+// sub-partition, each converting the 32 weight rows (two 16-row blocks) of
+// a group that its sub-partition's lanes hold.  Plain form: four teams, team
+// t taking the CTA's groups t, t + 4, t + 8, ..., so four groups are in
+// flight and one team's waits (weights, TMEM store, A-ring slot) overlap the
+// others' arithmetic; then the X producer, the W producer and the MMA warp.
+// With a separate epilogue: two teams, the two producers, the MMA warp and 4
+// epilogue warps that drain one TMEM accumulator while the dequantisers and
+// the MMA go on with the next tile in the other.  (Measured on GB300 against
+// two teams of eight warps of one block each: prefill 1322x19456x2560 86.1 ->
+// 82.9 us, the grouped 8 x (2048x4096) 59.9 -> 56.3 us, 32x19456x2560 12.5 ->
+// 11.6 us.)
+constexpr int kTcTeamWarps = 4;
 constexpr int kTcEpiWarps = 4;
 template <bool kSep>
 struct TcRoles {
-    static constexpr int kTeams = kSep ? 1 : 2;
+    static constexpr int kTeams = kSep ? 2 : 4;
     static constexpr int kDequant = kTcTeamWarps * kTeams;     // warps 0 .. kDequant - 1
     static constexpr int kProducerX = kDequant;                 // the X ring
     static constexpr int kProducerW = kDequant + 1;             // the W ring
@@ -572,15 +576,11 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
         // those with q % kTeams == team, and its ring slots and phase
         // parities advance kTeams positions per group it takes.
         const int team = warp / kTcTeamWarps;
-        const int tw = warp % kTcTeamWarps;
-        const int sub = tw & 3;                     // TMEM sub-partition of this warp (warp % 4)
-        const int half = tw >> 2;                   // which 16 lanes of the sub-partition
-        const int block = 2 * sub + half;           // 16-row block of the tile
+        const int sub = warp % kTcTeamWarps;        // TMEM sub-partition of this warp (warp % 4)
         const int g = lane >> 2;
-        const uint32_t lane_base = uint32_t(32 * sub + 16 * half) << 16;
         unsigned char *epi = smem + L.off_epi + warp * kEpiBytesPerWarp;
         int q = 0, tiles = 0;
-        int st = team, sa = team;       // ring slots of this warp's next group (kTeams <= 2 <= SW, SA)
+        int st = team, sa = team;       // ring slots of this warp's next group (kTeams <= SW, SA)
         uint32_t wph = 0;               // parity of the W-ring phase to wait for
         uint32_t eph = 1;               // parity of the A-ring empty phase (first lap: none)
         auto advance = [](int &slot, uint32_t &par, int n) {
@@ -590,10 +590,10 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                 par ^= 1u;
             }
         };
-        // Scales of the next group (possibly in the next tile), loaded one group
-        // ahead so the dequantisers never wait on them.
-        ScaleRaw<kSub> n0 = {}, n1 = {};
-        uint32_t nz0 = 0, nz1 = 0;      // zero points of the next block (kZp)
+        // The warp's weight rows r0 + 8 e (e = 0..3): blocks 2 sub and 2 sub + 1.
+        // Scales of the next group, loaded one group ahead.
+        ScaleRaw<kSub> ns[4] = {};
+        uint32_t nz[4] = {};
         bool have_next = false;
         const bool svec = (a.opt_bits & kTcScaleVec) != 0;
         const bool zvec = (a.opt_bits & kTcZeroVec) != 0;
@@ -602,56 +602,42 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
             const bool nx_ok = tc_tile<kBatched>(a, tab_tiles, tab_rows, id + gridDim.x, nx);
             const int g0 = ti.slice * a.gps;
             const int g1 = min(n_groups, (ti.slice + 1) * a.gps);
-            const int r0 = ti.ft * kTileRows + 16 * block + g;     // weight rows r0, r0 + 8
-            // Rows r0 and r0 + 8 of this tile's scales (and zero points), and
-            // of the next tile's, once per tile: a group's loads are then a
-            // constant offset from them.
-            const size_t so0 = (unsigned long long)ti.group * a.s_group_stride + size_t(r0) * n_sg;
-            const size_t so1 = so0 + size_t(8) * n_sg;
-            const uint16_t *sg0 = a.S + so0, *sg1 = a.S + so1;
-            const uint8_t *zg0 = kZp ? Z + so0 : nullptr, *zg1 = kZp ? Z + so1 : nullptr;
-            const int rn = nx.ft * kTileRows + 16 * block + g;
+            const int r0 = ti.ft * kTileRows + 32 * sub + g;
+            const size_t so = (unsigned long long)ti.group * a.s_group_stride + size_t(r0) * n_sg;
+            const size_t rstep = size_t(8) * n_sg;
+            const int rn = nx.ft * kTileRows + 32 * sub + g;
             const int gn0 = nx.slice * a.gps;
             const int nx_g1 = nx_ok ? min(n_groups, gn0 + a.gps) : 0;
-            const size_t no0 = nx_ok ? (unsigned long long)nx.group * a.s_group_stride + size_t(rn) * n_sg : 0;
-            const size_t no1 = no0 + size_t(8) * n_sg;
+            const size_t no = nx_ok ? (unsigned long long)nx.group * a.s_group_stride + size_t(rn) * n_sg : 0;
             bool ok = true;
             for (int grp = g0; grp < g1; ++grp, ++q) {
-                if (R::kTeams > 1 && q % R::kTeams != team) continue;   // the other team's group
-                ScaleRaw<kSub> s0, s1;              // raw; paired after the stage wait
-                uint32_t z0 = 0, z1 = 0;
+                if (R::kTeams > 1 && q % R::kTeams != team) continue;   // another team's group
+                ScaleRaw<kSub> s[4];
+                uint32_t z[4] = {0, 0, 0, 0};
                 if (have_next) {
-                    s0 = n0;
-                    s1 = n1;
-                    z0 = nz0;
-                    z1 = nz1;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) { s[e] = ns[e]; z[e] = nz[e]; }
                 } else {
-                    s0 = scales_raw<kSub>(sg0, r0, a.N, size_t(grp) * kSub, svec);
-                    s1 = scales_raw<kSub>(sg1, r0 + 8, a.N, size_t(grp) * kSub, svec);
-                    if (kZp) {
-                        z0 = zeros_raw<kSub>(zg0, r0, a.N, size_t(grp) * kSub, zvec);
-                        z1 = zeros_raw<kSub>(zg1, r0 + 8, a.N, size_t(grp) * kSub, zvec);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        s[e] = scales_raw<kSub>(a.S + so + e * rstep, r0 + 8 * e, a.N, size_t(grp) * kSub, svec);
+                        if (kZp) z[e] = zeros_raw<kSub>(Z + so + e * rstep, r0 + 8 * e, a.N, size_t(grp) * kSub, zvec);
                     }
                 }
-                // This warp's next group: grp + kTeams in this tile, else the
-                // next tile's group number gn0 + (grp + kTeams - g1) (0 or 1
-                // past its first) if it has one.
                 const int gnext = grp + R::kTeams;
                 have_next = gnext < g1 || (nx_ok && gn0 + (gnext - g1) < nx_g1);
                 if (gnext < g1) {
-                    n0 = scales_raw<kSub>(sg0, r0, a.N, size_t(gnext) * kSub, svec);
-                    n1 = scales_raw<kSub>(sg1, r0 + 8, a.N, size_t(gnext) * kSub, svec);
-                    if (kZp) {
-                        nz0 = zeros_raw<kSub>(zg0, r0, a.N, size_t(gnext) * kSub, zvec);
-                        nz1 = zeros_raw<kSub>(zg1, r0 + 8, a.N, size_t(gnext) * kSub, zvec);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        ns[e] = scales_raw<kSub>(a.S + so + e * rstep, r0 + 8 * e, a.N, size_t(gnext) * kSub, svec);
+                        if (kZp) nz[e] = zeros_raw<kSub>(Z + so + e * rstep, r0 + 8 * e, a.N, size_t(gnext) * kSub, zvec);
                     }
                 } else if (have_next) {
                     const size_t gi = size_t(gn0 + (gnext - g1)) * kSub;
-                    n0 = scales_raw<kSub>(a.S + no0, rn, a.N, gi, svec);
-                    n1 = scales_raw<kSub>(a.S + no1, rn + 8, a.N, gi, svec);
-                    if (kZp) {
-                        nz0 = zeros_raw<kSub>(Z + no0, rn, a.N, gi, zvec);
-                        nz1 = zeros_raw<kSub>(Z + no1, rn + 8, a.N, gi, zvec);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        ns[e] = scales_raw<kSub>(a.S + no + e * rstep, rn + 8 * e, a.N, gi, svec);
+                        if (kZp) nz[e] = zeros_raw<kSub>(Z + no + e * rstep, rn + 8 * e, a.N, gi, zvec);
                     }
                 }
                 // Warp-uniform outcomes below: tcgen05.st needs every lane.
@@ -659,60 +645,65 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                     ok = false;
                     break;
                 }
-                const unsigned char *wsrc = smem + L.off_w + st * kGroupBytes + block * kBlockBytes + lane * 16;
-                const uint4 wa = *reinterpret_cast<const uint4 *>(wsrc);
-                const uint4 wb = *reinterpret_cast<const uint4 *>(wsrc + kChunkBytes);
-                const uint32_t wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+                const unsigned char *wsrc = smem + L.off_w + st * kGroupBytes + (2 * sub) * kBlockBytes + lane * 16;
+                uint32_t wv[2][8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint4 wa = *reinterpret_cast<const uint4 *>(wsrc + h * kBlockBytes);
+                    const uint4 wb = *reinterpret_cast<const uint4 *>(wsrc + h * kBlockBytes + kChunkBytes);
+                    wv[h][0] = wa.x; wv[h][1] = wa.y; wv[h][2] = wa.z; wv[h][3] = wa.w;
+                    wv[h][4] = wb.x; wv[h][5] = wb.y; wv[h][6] = wb.z; wv[h][7] = wb.w;
+                }
                 // The stage's bytes are in registers: hand it back to the producer.
                 __syncwarp();
                 if (lane == 0) mbar_arrive(wempty_bar(st));
-                uint32_t p0[kSub], p1[kSub];
+                advance(st, wph, SW);
 #pragma unroll
-                for (int i = 0; i < kSub; ++i) {
-                    p0[i] = scale_pair_of<kSub>(s0, i);
-                    p1[i] = scale_pair_of<kSub>(s1, i);
-                }
-                uint32_t zo0[kSub], zo1[kSub];      // kZp: offset pairs per scale group
-                if constexpr (kZp) {
-                    const uint32_t m0 = z0 & 0x0F0F0F0Fu, m1 = z1 & 0x0F0F0F0Fu;
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t p0[kSub], p1[kSub];
 #pragma unroll
                     for (int i = 0; i < kSub; ++i) {
-                        zo0[i] = neg_offset_pair(m0, i);
-                        zo1[i] = neg_offset_pair(m1, i);
+                        p0[i] = scale_pair_of<kSub>(s[2 * h], i);
+                        p1[i] = scale_pair_of<kSub>(s[2 * h + 1], i);
                     }
-                }
-                uint32_t frag[32];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    // Repetition j of the 16x256b store: {row g: pair 0, pair 1},
-                    // {row g+8: pair 0, pair 1} of columns 16j + 4t of the group.
-                    const uint32_t q0 = p0[j * kSub / 8], q1 = p1[j * kSub / 8];
+                    uint32_t zo0[kSub], zo1[kSub];
                     if constexpr (kZp) {
-                        const uint32_t o0 = zo0[j * kSub / 8];
-                        const uint32_t o1 = zo1[j * kSub / 8];
-                        frag[4 * j + 0] = bf16x2_mul(bf16x2_add_pair(magic_pair(wv[j]), o0), q0);
-                        frag[4 * j + 1] = bf16x2_mul(bf16x2_add_pair(magic_pair(wv[j] >> 8), o0), q0);
-                        frag[4 * j + 2] = bf16x2_mul(bf16x2_add_pair(magic_pair(wv[j] >> 4), o1), q1);
-                        frag[4 * j + 3] = bf16x2_mul(bf16x2_add_pair(magic_pair(wv[j] >> 12), o1), q1);
-                        continue;
+                        const uint32_t m0 = z[2 * h] & 0x0F0F0F0Fu, m1 = z[2 * h + 1] & 0x0F0F0F0Fu;
+#pragma unroll
+                        for (int i = 0; i < kSub; ++i) {
+                            zo0[i] = neg_offset_pair(m0, i);
+                            zo1[i] = neg_offset_pair(m1, i);
+                        }
                     }
-                    frag[4 * j + 0] = bf16x2_mul(minus136(magic_pair(wv[j])), q0);
-                    frag[4 * j + 1] = bf16x2_mul(minus136(magic_pair(wv[j] >> 8)), q0);
-                    frag[4 * j + 2] = bf16x2_mul(minus136(magic_pair(wv[j] >> 4)), q1);
-                    frag[4 * j + 3] = bf16x2_mul(minus136(magic_pair(wv[j] >> 12)), q1);
+                    uint32_t frag[32];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t q0 = p0[j * kSub / 8], q1 = p1[j * kSub / 8];
+                        const uint32_t w = wv[h][j];
+                        if constexpr (kZp) {
+                            const uint32_t o0 = zo0[j * kSub / 8];
+                            const uint32_t o1 = zo1[j * kSub / 8];
+                            frag[4 * j + 0] = bf16x2_mul(bf16x2_add_pair(magic_pair(w), o0), q0);
+                            frag[4 * j + 1] = bf16x2_mul(bf16x2_add_pair(magic_pair(w >> 8), o0), q0);
+                            frag[4 * j + 2] = bf16x2_mul(bf16x2_add_pair(magic_pair(w >> 4), o1), q1);
+                            frag[4 * j + 3] = bf16x2_mul(bf16x2_add_pair(magic_pair(w >> 12), o1), q1);
+                            continue;
+                        }
+                        frag[4 * j + 0] = bf16x2_mul(minus136(magic_pair(w)), q0);
+                        frag[4 * j + 1] = bf16x2_mul(minus136(magic_pair(w >> 8)), q0);
+                        frag[4 * j + 2] = bf16x2_mul(minus136(magic_pair(w >> 4)), q1);
+                        frag[4 * j + 3] = bf16x2_mul(minus136(magic_pair(w >> 12)), q1);
+                    }
+                    if (h == 0) {
+                        if (q >= SA && !__all_sync(0xffffffffu, mbar_wait(aempty_bar(sa), eph, abort_flag, a.err))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    tc_st_16x256b_x8(tmem_base + (uint32_t(32 * sub + 16 * h) << 16) + uint32_t(a.dcols) + 64u * sa, frag);
                 }
-                advance(st, wph, SW);
-                if (q >= SA && !__all_sync(0xffffffffu, mbar_wait(aempty_bar(sa), eph, abort_flag, a.err))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                tc_st_16x256b_x8(tmem_base + lane_base + uint32_t(a.dcols) + 64u * sa, frag);
-                // Hand the stage to the MMA warp as soon as the store has
-                // landed.  (Measured on GB300: deferring this wait until the
-                // warp's next group was dequantised, to overlap the store
-                // latency, held each A stage ~0.7 us longer and cost 3-4 % on
-                // the prefill shapes.)
+                if (!ok) break;
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -914,7 +905,7 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
                           int *status, int num_groups, int M_total, int N, int K, cudaStream_t s,
                           int batch_rows, const uint8_t *Z) {
     if (p.tile_tokens < 32 || p.tile_tokens > 256 || p.tile_tokens % 32 || p.x_stages < 2 ||
-        p.w_stages < 2 ||
+        p.w_stages < (p.sep_epilogue ? TcRoles<true>::kTeams : TcRoles<false>::kTeams) ||
         p.ctas < 1 || num_groups < 1 || num_groups > kMaxGroups || p.occupancy != 1 ||
         (p.sub != 1 && p.sub != 2 && p.sub != 4) ||
         tensor_a_stages(p.tile_tokens, p.occupancy, p.sep_epilogue) < 2)
