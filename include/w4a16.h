@@ -64,15 +64,18 @@ typedef enum {
 
 /* w4a16_options.flags bits. */
 enum {
-    /* W_packed and scales are resident: no kernel still running on the stream
-     * when the call is made writes them (they were written before that kernel
-     * started, e.g. when the model was loaded).  The call's kernel is launched
-     * with programmatic dependent launch and may then start streaming the
-     * weights into shared memory while the previous kernel on the stream is
-     * still running; only X is read after that kernel has completed.  Without
-     * the flag nothing is read before it has completed.  Do not set it when
-     * W_packed or scales alias the output or workspace of a call just before
-     * on the same stream. */
+    /* W_packed, scales and zero points are resident: no kernel still running
+     * on the stream when the call is made writes them (they were written
+     * before that kernel started, e.g. when the model was loaded).  The call's
+     * kernel is launched with programmatic dependent launch and may then start
+     * streaming the weights into shared memory while the previous kernel on
+     * the stream is still running; X is read, and Y and the workspace are
+     * written, only after that kernel has completed.  Without the flag nothing
+     * is read before it has completed.  The decode arm uses it; the tensor arm
+     * (one large CTA per SM, which cannot start beside the previous call's)
+     * reads nothing before the previous kernel has completed either way.  Do
+     * not set it when W_packed, scales or zero points alias the output or
+     * workspace of a call just before on the same stream. */
     W4A16_FLAG_RESIDENT_WEIGHTS = 1,
     /* Decode-arm kernel choice (for tests and tuning; by default the
      * dispatcher chooses).  WHOLE_K: the kernel in which every CTA covers all

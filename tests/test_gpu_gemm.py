@@ -317,30 +317,36 @@ def test_splitk_reduce_bit_exact(S, M, N):
 
 
 # ------------------------------------------------------------ resident weights
-@pytest.mark.parametrize("M,N,K", [(1, 8192, 8192), (16, 2560, 9728), (3, 300, 640), (8, 19456, 2560)])
-def test_resident_weights_give_the_same_bits(M, N, K):
+@pytest.mark.parametrize("M,N,K,arm", [(1, 8192, 8192, None), (16, 2560, 9728, None), (3, 300, 640, None),
+                                       (8, 19456, 2560, None), (64, 2048, 2048, "tensor"),
+                                       (256, 1536, 4096, "tensor"), (40, 640, 1280, "tensor")])
+def test_resident_weights_give_the_same_bits(M, N, K, arm):
     # The flag only moves the weight stream ahead of the dependency wait.
     p = problem(M, N, K)
-    a = bf16_to_u16(run(p))
-    b = bf16_to_u16(run(p, resident_weights=True))
+    a = bf16_to_u16(run(p, arm=arm))
+    b = bf16_to_u16(run(p, arm=arm, resident_weights=True))
     assert np.array_equal(a, b)
 
 
-def test_resident_weights_chain_reads_x_after_the_previous_call():
-    # Y of one call is X of the next (a chain of layers, same stream, inside one
-    # graph): each call streams its weights early but must read X only after the
-    # call before it has completed.
+@pytest.mark.parametrize("M,arm", [(1, None), (64, "tensor")])
+def test_resident_weights_chain_reads_x_after_the_previous_call(M, arm):
+    # A chain of layers on one stream inside one graph, through two ping-pong
+    # buffers: the Y of one call is the X of the next, and each call writes
+    # the buffer the call before it read as X.  Each call streams its weights
+    # early but must read X, and write Y, only after the call before it has
+    # completed.
     K = 2048
-    layers = [DeviceProblem(syn.make_gemm_inputs(1, K, K, seed=50 + i)) for i in range(4)]
+    layers = [DeviceProblem(syn.make_gemm_inputs(M, K, K, seed=50 + i)) for i in range(4)]
     x0 = layers[0].x.clone()
+    bufs = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
 
     def chain(resident):
-        x = x0
+        bufs[0].copy_(x0)
         outs = []
-        for lp in layers:
-            y = w4.gemm(x, lp.w_packed, lp.scales, resident_weights=resident)
-            outs.append(y)
-            x = y
+        for i, lp in enumerate(layers):
+            x, y = bufs[i % 2], bufs[(i + 1) % 2]
+            w4.gemm(x, lp.w_packed, lp.scales, out=y, arm=arm, resident_weights=resident)
+            outs.append(y.clone())
         return outs
 
     eager = [bf16_to_u16(y) for y in chain(False)]
@@ -362,9 +368,9 @@ def test_resident_weights_chain_reads_x_after_the_previous_call():
             assert np.array_equal(bf16_to_u16(y), e)
     # and the chain itself is right: the last layer against the oracle, fed the
     # previous layer's bf16 output
-    xin = bf16_to_u16(outs[-2]).reshape(1, K)
+    xin = bf16_to_u16(outs[-2]).reshape(M, K)
     last = layers[-1].inp
-    ref = oracle.gemm(xin, last.w_canon, last.scales, 1, K, K)
+    ref = oracle.gemm(xin, last.w_canon, last.scales, M, K, K)
     assert_close(bf16_to_f64(outs[-1]), ref, what="chain")
 
 
