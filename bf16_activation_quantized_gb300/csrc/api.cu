@@ -307,9 +307,12 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                 // 76.3 us, unsplit 51.9 us; 2048x8192x8192 split 2 288 us,
                 // unsplit 199 us).
                 const double e_split = 1500.0 * std::max(1.0, (bt / 128.0) * (bt / 128.0));
-                const double epi = sep ? 1500.0
-                                 : sk > 1 ? 1500.0 + (per_cta_tiles - 1) * e_split
-                                          : per_cta_tiles * 1500.0;
+                // The plain form's in-line drain of a bf16 tile before the
+                // CTA's next tile stalls the same way (measured on GB300:
+                // 4096x19456x2560 in plain 256-token tiles 312 us, in
+                // separate-epilogue 192-token tiles 248 us; 2048x19456x2560
+                // 158 vs 125 us).
+                const double epi = sep ? 1500.0 : 1500.0 + (per_cta_tiles - 1) * e_split;
                 double time = (per_cta_tiles * conc * 2.0 * gps * kb + epi) / kClockHz;
                 if (sk > 1) time += 2.0 * sk * double(M) * N * 4.0 / kL2BytesPerS + kTensorReduceSeconds;
                 if (time < best * 0.999) {
