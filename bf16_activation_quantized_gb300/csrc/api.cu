@@ -49,6 +49,10 @@ constexpr int kDecodeInFlight = 3;            // bulk copies (ring stages) in th
 constexpr double kHbmBytesPerS = 6.5e12;      // planning figures, not measurements
 constexpr double kCtaBytesPerS = 25e9;        // one CTA's streaming rate (32 KB in flight)
 constexpr double kL2BytesPerS = 20e12;
+// The tensor arm's fp32 partials (up to tens of MB for a long prefill) are
+// charged at HBM speed: measured on GB300, 2048x2560x9728 split 2 (42 MB of
+// partials) took 88.4 us against 78.4 us unsplit in 160-token tiles.
+constexpr double kTensorPartialBytesPerS = 6.5e12;
 // Measured on GB300 with per-CTA %globaltimer timelines of back-to-back
 // calls: after the decode kernel's last CTA, the reduce kernel waits about
 // 0.7 us for the grid to complete, works about 0.85 us, and the next kernel
@@ -314,7 +318,7 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                 // 158 vs 125 us).
                 const double epi = sep ? 1500.0 : 1500.0 + (per_cta_tiles - 1) * e_split;
                 double time = (per_cta_tiles * conc * 2.0 * gps * kb + epi) / kClockHz;
-                if (sk > 1) time += 2.0 * sk * double(M) * N * 4.0 / kL2BytesPerS + kTensorReduceSeconds;
+                if (sk > 1) time += 2.0 * sk * double(M) * N * 4.0 / kTensorPartialBytesPerS + kTensorReduceSeconds;
                 if (time < best * 0.999) {
                     best = time;
                     t->tile_tokens = bt;
