@@ -232,7 +232,7 @@ bool tensor_rings(int bt, int num_groups, int occupancy, bool sep, int *x_stages
         if (sx * x_stage > avail) continue;
         size_t sw = (avail - sx * x_stage) / w_stage;
         if (sw > size_t(kTensorMaxWStages)) sw = kTensorMaxWStages;
-        if (sw >= 4) {
+        if (sw >= size_t(kTensorTeamsPlain)) {
             *x_stages = sx;
             *w_stages = int(sw);
             return true;
@@ -242,7 +242,7 @@ bool tensor_rings(int bt, int num_groups, int occupancy, bool sep, int *x_stages
 }
 
 // Tensor-arm tiles: 128 weight rows x bt tokens, K split into sk slices, one
-// CTA per SM (576 threads in the plain form, 448 with a separate epilogue).
+// CTA per SM (608 threads in the plain form, 480 with a separate epilogue).
 // Per K block an SM needs at least max(MMA: 2 bt cycles, a dequant floor,
 // weight bytes at its HBM share + activation bytes at its L2 share), and a
 // CTA cannot go faster than its dependency chain (kTcChainClk per K block).
@@ -266,7 +266,8 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
             // the plain form; a separate epilogue
             const int occ = 1;
             const bool sep = variant == 1;
-            if (tensor_a_stages(bt, occ, sep) < 2) continue;  // TMEM share too small
+            // TMEM share too small for one A stage per dequantiser team
+            if (tensor_a_stages(bt, occ, sep) < (sep ? kTensorTeamsSep : kTensorTeamsPlain)) continue;
             int sx = 0, sw = 0;
             if (!tensor_rings(bt, num_groups, occ, sep, &sx, &sw)) continue;
             const int max_sk = grouped ? 1 : (groups < 16 ? groups : 16);

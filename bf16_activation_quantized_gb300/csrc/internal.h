@@ -35,7 +35,7 @@ struct TensorPlan {
     int ctas;             // persistent CTAs launched
     int x_stages;         // X ring depth (groups of X in shared memory)
     int w_stages;         // W ring depth (groups of packed weights in shared memory)
-    int occupancy;        // CTAs per SM the resources are sized for (1 or 2)
+    int occupancy;        // CTAs per SM the resources are sized for (the planner: always 1)
     bool sep_epilogue;    // two TMEM accumulators drained by dedicated epilogue warps (occupancy 1)
     int sub;              // scale groups per 128-wide block: 1, 2 or 4 (groups of 128, 64, 32)
     size_t smem_bytes;
@@ -84,6 +84,10 @@ constexpr int kTensorMaxSmem = 227 * 1024;     // per-CTA opt-in maximum
 constexpr int kSmemPerSm = 228 * 1024;         // shared memory of one SM
 constexpr int kSmemReservedPerCta = 1024;      // the runtime's share of each resident CTA
 constexpr int kMaxGroups = 1024;
+// Tensor arm: dequantiser teams (four warps each) of the plain and the
+// separate-epilogue forms; the W and A rings hold one slot per team at least.
+constexpr int kTensorTeamsPlain = 4;
+constexpr int kTensorTeamsSep = 2;
 // Dynamic shared memory a CTA may use when `occupancy` CTAs share an SM.
 inline int tensor_smem_budget(int occupancy) {
     const int b = kSmemPerSm / occupancy - kSmemReservedPerCta;

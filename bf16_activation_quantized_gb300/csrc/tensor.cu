@@ -61,7 +61,7 @@ constexpr int kTcTeamWarps = 4;
 constexpr int kTcEpiWarps = 4;
 template <bool kSep>
 struct TcRoles {
-    static constexpr int kTeams = kSep ? 2 : 4;
+    static constexpr int kTeams = kSep ? kTensorTeamsSep : kTensorTeamsPlain;
     static constexpr int kDequant = kTcTeamWarps * kTeams;     // warps 0 .. kDequant - 1
     static constexpr int kProducerX = kDequant;                 // the X ring
     static constexpr int kProducerW = kDequant + 1;             // the W ring
@@ -914,7 +914,9 @@ cudaError_t launch_tensor(const TensorPlan &p, const uint16_t *X, const uint8_t 
         p.w_stages < (p.sep_epilogue ? TcRoles<true>::kTeams : TcRoles<false>::kTeams) ||
         p.ctas < 1 || num_groups < 1 || num_groups > kMaxGroups || p.occupancy != 1 ||
         (p.sub != 1 && p.sub != 2 && p.sub != 4) ||
-        tensor_a_stages(p.tile_tokens, p.occupancy, p.sep_epilogue) < 2)
+        // one W and one A ring slot per dequantiser team at least
+        tensor_a_stages(p.tile_tokens, p.occupancy, p.sep_epilogue) <
+            (p.sep_epilogue ? TcRoles<true>::kTeams : TcRoles<false>::kTeams))
         return cudaErrorInvalidValue;
     CUtensorMap tmap;
     const cuuint64_t gdim[2] = {cuuint64_t(K), cuuint64_t(M_total)};
