@@ -186,3 +186,25 @@ def test_python_plan_for_sms_needs_no_gpu():
     assert w4.plan(1, 19456, 2560, sms=SMS, group_size=32, zero_points=True)["whole_k"] is False
     with pytest.raises(w4.W4A16Error):
         w4.plan(1, 256, 512, sms=SMS, group_size=16)
+
+
+# Tensor-arm plans pinned by measurements on GB300 (graphs of back-to-back
+# calls, rotating weights).  Each case names the plan that measured fastest
+# among the tile widths and splits tried for it.
+@pytest.mark.parametrize("M,N,K,bt,split", [
+    # long prefills: separate-epilogue 192-token tiles beat plain 256-token ones
+    # (2048x19456x2560 127 vs 158 us, 4096x19456x2560 247 vs 312 us,
+    # 2048x8192x8192 172 vs 203 us)
+    (2048, 19456, 2560, 192, 1), (4096, 19456, 2560, 192, 1), (2048, 8192, 8192, 192, 1),
+    (1322, 19456, 2560, 192, 1), (1322, 2560, 9728, 192, 1),
+    # unsplit 160-token tiles beat split 2 (78.0 vs 88.4 us: 42 MB of partials)
+    (2048, 2560, 9728, 160, 1),
+    # one tile per CTA: the plain 256-token form, unsplit (split 4 measured 47 % slower)
+    (512, 7168, 8192, 256, 1),
+    # split 2 beats split 16 (19.4 vs 27.5 us); unsplit 64-token tiles beat split 3 (7.3 vs 11.9 us)
+    (33, 8192, 8192, 64, 2), (300, 2560, 1024, 64, 1),
+])
+def test_measured_tensor_plans(L, M, N, K, bt, split):
+    st, info = plan(L, M, N, K)
+    assert st == OK and info.arm == 2
+    assert (info.tile_tokens, info.split_k) == (bt, split), (info.tile_tokens, info.split_k)
