@@ -580,7 +580,13 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
         // Dequantisers (and, without a separate epilogue, the epilogue).
         // q counts the CTA's groups in ring order; this warp's team takes
         // those with q % kTeams == team, and its ring slots and phase
-        // parities advance kTeams positions per group it takes.
+        // parities advance kTeams positions per group it takes.  Within a
+        // team, warp `sub` converts the 32 weight rows of TMEM sub-partition
+        // `sub` (16-row blocks 2 sub and 2 sub + 1): per group it loads both
+        // blocks' packed words, hands the W stage back, builds and stores
+        // block 2 sub's fragments, waits for its A stage's slot only before
+        // that first store, then builds and stores block 2 sub + 1's, and
+        // hands the A stage to the MMA warp once both stores have landed.
         const int team = warp / kTcTeamWarps;
         const int sub = warp % kTcTeamWarps;        // TMEM sub-partition of this warp (warp % 4)
         const int g = lane >> 2;
@@ -596,8 +602,9 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap &tmap_x, const Tc
                 par ^= 1u;
             }
         };
-        // The warp's weight rows r0 + 8 e (e = 0..3): blocks 2 sub and 2 sub + 1.
-        // Scales of the next group, loaded one group ahead.
+        // The warp's weight rows are r0 + 8 e (e = 0..3; rows g and g + 8 of
+        // its two blocks).  Their scales (and zero points) of the warp's next
+        // group are loaded one group ahead.
         ScaleRaw<kSub> ns[4] = {};
         uint32_t nz[4] = {};
         bool have_next = false;
