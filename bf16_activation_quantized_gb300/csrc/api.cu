@@ -318,7 +318,18 @@ w4a16_status plan_tensor(int M, int N, int K, int sms, int forced_split, int for
                 // separate-epilogue 192-token tiles 248 us; 2048x19456x2560
                 // 158 vs 125 us).
                 const double epi = sep ? 1500.0 : 1500.0 + (per_cta_tiles - 1) * e_split;
-                double time = (per_cta_tiles * conc * 2.0 * gps * kb + epi) / kClockHz;
+                // Plain tiles wider than 192 tokens keep only two 64 KB X
+                // stages next to their in-line drain; with several tiles per
+                // CTA they measure ~1.6x the per-K-block time of
+                // separate-epilogue 192-token tiles where the terms above give
+                // ~1.2x (GB300: 1024x19456x2560 79.7 against 68.9 us,
+                // 4096x8192x8192 357 against 336 us, 2048x4096x4096 58.0
+                // against 54.4 us).  With the penalty the narrower plans
+                // chosen measured faster on every shape it moved
+                // (2048x4096x4096 at 160 tokens 52.1 us, 1024x7168x8192
+                // 96.5 against 103.4 us).
+                const double wide = (!sep && bt > 192 && per_cta_tiles > 1) ? 1.25 : 1.0;
+                double time = (per_cta_tiles * conc * 2.0 * gps * kb * wide + epi) / kClockHz;
                 if (sk > 1) time += 2.0 * sk * double(M) * N * 4.0 / kTensorPartialBytesPerS + kTensorReduceSeconds;
                 if (time < best * 0.999) {
                     best = time;

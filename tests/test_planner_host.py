@@ -203,6 +203,12 @@ def test_python_plan_for_sms_needs_no_gpu():
     (512, 7168, 8192, 256, 1),
     # split 2 beats split 16 (19.4 vs 27.5 us); unsplit 64-token tiles beat split 3 (7.3 vs 11.9 us)
     (33, 8192, 8192, 64, 2), (300, 2560, 1024, 64, 1),
+    # several tiles per CTA: plain tiles above 192 tokens lose to narrower ones
+    # (1024x19456x2560 192: 68.9 vs 256: 79.7 us; 512x19456x2560 37.4 vs 40.9 us;
+    # 2048x4096x4096 160: 52.1 vs 256: 58.0 us; 2048x7168x8192 161.3 vs 163.4 us;
+    # 1024x7168x8192 160: 96.5 vs 224: 103.4 us)
+    (1024, 19456, 2560, 192, 1), (512, 19456, 2560, 192, 1), (2048, 4096, 4096, 160, 1),
+    (2048, 7168, 8192, 160, 1), (1024, 7168, 8192, 160, 1),
 ])
 def test_measured_tensor_plans(L, M, N, K, bt, split):
     st, info = plan(L, M, N, K)
