@@ -107,3 +107,16 @@ def test_batched_in_a_graph_replays_exactly():
         g.replay()
         torch.cuda.synchronize()
         assert np.array_equal(bf16_to_u16(out), eager)
+
+
+def test_batched_workload_sampled():
+    # Two 2048x7168x8192 products through the planner's choice (160-token
+    # tensor tiles, several per CTA): every token on a sample of features.
+    B, M, N, K = 2, 2048, 7168, 8192
+    assert w4.plan_batched(B, M, N, K)["arm"] == "tensor"
+    bt = Batch(B, M, N, K, seed=21)
+    y = bt.run()
+    rng = np.random.default_rng(5)
+    cols = np.unique(np.r_[rng.choice(N, 40, replace=False), 0, 127, 128, N - 1])
+    for b in range(B):
+        assert_close(bf16_to_f64(y[b])[:, cols], bt.reference(b, cols), what=f"entry {b} of {B}x{M}x{N}x{K}")
