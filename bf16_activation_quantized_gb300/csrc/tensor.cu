@@ -2,22 +2,31 @@
 // in TMEM, tcgen05.mma with fp32 accumulators in TMEM.  One persistent kernel
 // serves the plain product (optionally split along K) and the grouped product.
 //
-// Roles in a CTA (320 threads):
-//   warp 8      producer: per 128-wide group two TMA 2-D loads of the X tile
-//               [tokens x 64] (128-byte swizzle) into the X ring and one 8 KB
-//               bulk copy of the packed weights into the W ring.  The rings are
-//               separate: the W ring is released by the dequantisers as soon as
-//               they have read it and can run many groups ahead of the MMA
-//               (HBM latency), the X ring is released by the MMA commit.  One
-//               thread polls both rings and issues whichever has room.
-//   warp 9      TMEM owner and MMA issuer: four tcgen05.mma (K = 16 each) per
-//               K block, A = weights from TMEM, B = X from shared memory,
+// Roles in a CTA (one per SM; 608 threads in the plain form, 480 with a
+// separate epilogue; warp numbers for the plain form):
+//   warps 0-15  dequantisers in four teams of four (two teams with a separate
+//               epilogue).  Team t takes the CTA's groups q with
+//               q % teams == t, in ring order; its warp w converts the 32
+//               weight rows that TMEM sub-partition w % 4 holds (two 16-row
+//               blocks): one LOP3 per bf16 pair gives 128 + code, one
+//               bf16x2 FMA removes 136 exactly, one bf16x2 multiply applies
+//               the group scale with a single rounding; two 16x256b
+//               tcgen05.st per group, and the A stage goes to the MMA warp as
+//               soon as the stores land.  In the plain form the same warps
+//               then drain the tile's accumulator.
+//   warp 16     X producer: per 128-wide group two TMA 2-D loads of the X
+//               tile [tokens x 64] (128-byte swizzle); the X ring is released
+//               by the MMA commit.
+//   warp 17     W producer: one 8 KB bulk copy of the group's packed weights;
+//               the W ring is released by the dequantisers once read, so it
+//               runs many groups ahead of the MMA (HBM latency).
+//   warp 18     TMEM owner and MMA issuer: eight tcgen05.mma (K = 16) per
+//               group, A = weights from TMEM, B = X from shared memory,
 //               D = fp32 in TMEM; tcgen05.commit releases the stages.
-//   warps 0-7   dequantisers, then the epilogue: warp w owns 16 weight rows,
-//               turns each packed word into its 16x256b TMEM fragment (one
-//               LOP3 per bf16 pair gives 128 + code; one bf16x2 FMA removes
-//               136 exactly; one bf16x2 multiply applies the group scale with a
-//               single rounding) and stores it with tcgen05.st.
+//   (separate form) four epilogue warps drain one of two accumulators while
+//               the next tile runs into the other.
+// Producers and the MMA issuer run their loops as whole warps and issue
+// from one elected lane.
 // The page this follows for the data flow is "[ROCm][Kernel] W4A16 skinny
 // GEMM: hand-asm kernel for gfx1151" (magic-constant dequant, section 1;
 // loads pipelined ahead of the math, section 2); the tile, the TMEM operand
