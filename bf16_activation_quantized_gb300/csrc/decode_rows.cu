@@ -16,13 +16,12 @@
 // quarter, half ... of K in interleaved pairs of groups), for all M tokens:
 // MT = ceil(M / 8) token octets (up to two), each dequantised A fragment
 // feeding one m16n8k16 per octet, so the weights are streamed once.  Per
-// group it builds
-// the bf16 A fragments 128 + code with one LOP3 per register and removes 136
-// with one exact bf16x2 FMA (the magic-constant trick of "[ROCm][Kernel]
-// W4A16 skinny GEMM: hand-asm kernel for gfx1151", section 1), so
-// the m16n8k16 chain over the group multiplies exact codes - 8 by the bf16 X
-// fragments taken from the stage as they are; the fp32 group scale multiplies
-// the chain's sum.  At the end the P warps of a block add their sums in shared
+// group it builds the bf16 A fragments 128 + code with one LOP3 per register
+// and removes 136 with one exact bf16x2 FMA (the magic-constant trick of
+// "[ROCm][Kernel] W4A16 skinny GEMM: hand-asm kernel for gfx1151", section
+// 1), so the m16n8k16 chain over the group multiplies exact codes - 8 by the
+// bf16 X fragments taken from the stage as they are; the fp32 group scale
+// multiplies the chain's sum.  At the end the P warps of a block add their sums in shared
 // memory in ascending order and the first writes Y.
 #include <atomic>
 

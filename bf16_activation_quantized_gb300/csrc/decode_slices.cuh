@@ -12,8 +12,7 @@
 // lanes, consecutive bytes -- the access pattern the Q4_K decode issue on
 // "gfx1151: 61.7% of Qwen3.8-27B's per-token byte budget ..." shows is needed
 // to reach the memory ceiling), and it releases the stage as soon as the words
-// are in registers.  The CTA's slice of X is staged once
-// in shared memory.
+// are in registers.  The CTA's slice of X is staged once in shared memory.
 //
 // Each 32-bit word becomes, with one LOP3 per register, the A fragment of an
 // m16n8k16 fp16 mma.sync holding 1024 + code (the magic-constant trick of that
